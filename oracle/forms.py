@@ -1,0 +1,250 @@
+"""Independent float64 restatements of the forms the pages give -- TEST
+INFRASTRUCTURE ONLY (see the package docstring).
+
+Each function works on ONE head (no batch/head axes) and follows one passage.
+They are written from the mathematics, not from the printed listings, and are
+used on tiny inputs to pin the C oracle (``oracle.fwd``), which implements only
+the token-by-token recurrence.
+
+Page titles used in citations:
+  [DR] "08 · linear 路线（三）：delta rule 与 DPLR 统一框架" (llm-infra-atlas)
+  [DP] "DeltaProduct：通过 Householder 乘积增强线性 RNN 的状态追踪" (reading notes)
+
+Conventions: the state S is [dk, dv]; the readout is o = S^T q after the
+update; keys are not normalised here.
+"""
+from __future__ import annotations
+
+import numpy as np
+from scipy.linalg import solve_triangular
+
+
+# --------------------------------------------------------------------------
+# single-step forms ([DR] section 1)
+# --------------------------------------------------------------------------
+def step_erase_write(S, k, v, beta):
+    """[DR] §1.1 erase-write view: erase the value stored under k, then write
+    the interpolation beta*v + (1-beta)*v_old."""
+    v_old = S.T @ k
+    v_new = beta * v + (1.0 - beta) * v_old
+    return S - np.outer(k, v_old) + np.outer(k, v_new)
+
+
+def step_householder(S, k, v, beta):
+    """[DR] §1.2 simplified form: S' = (I - beta k k^T) S + beta k v^T."""
+    F = np.eye(len(k)) - beta * np.outer(k, k)
+    return F @ S + beta * np.outer(k, v)
+
+
+def step_gradient(S, k, v, beta):
+    """[DR] §1.3 online-GD view: one gradient step with learning rate beta on
+    L(S) = 1/2 ||S^T k - v||^2, whose gradient is k (S^T k - v)^T."""
+    grad = np.outer(k, S.T @ k - v)
+    return S - beta * grad
+
+
+# --------------------------------------------------------------------------
+# DeltaProduct algebra ([DP] sections 2.2-2.6)
+# --------------------------------------------------------------------------
+def householder_factor(k, beta):
+    """F = I - beta k k^T ([DP] §2.2)."""
+    return np.eye(len(k)) - beta * np.outer(k, k)
+
+
+def householder_product(ks, betas):
+    """A = F_{n_h} ... F_2 F_1: earlier factors sit on the right ([DP] §2.3)."""
+    A = np.eye(ks.shape[1])
+    for kj, bj in zip(ks, betas):
+        A = householder_factor(kj, bj) @ A
+    return A
+
+
+def write_term(ks, vs, betas):
+    """B = sum_j F_{n_h} ... F_{j+1} C_j with C_j = beta_j k_j v_j^T ([DP] §2.3)."""
+    n = len(betas)
+    Bm = np.zeros((ks.shape[1], vs.shape[1]))
+    for j in range(n):
+        Cj = betas[j] * np.outer(ks[j], vs[j])
+        for i in range(j + 1, n):
+            Cj = householder_factor(ks[i], betas[i]) @ Cj
+        Bm += Cj
+    return Bm
+
+
+def extend_sequence(q, k, v, beta, g, n_h):
+    """[DP] §4.1 extended sequence: interleave the n_h keys/values of every
+    token into one sequence of length n_h*T; the gate becomes
+    (g_1, 1, ..., 1, g_2, 1, ...), applied once per original token; only the
+    last sub-step of each token is read out.
+
+    q [T,dk], k [T,n_h,dk], v [T,n_h,dv], beta [T,n_h], g [T] or None.
+    Returns (qx [L,dk], kx [L,dk], vx [L,dv], bx [L], gx [L], readout_idx [T]).
+    """
+    T, dk = q.shape
+    L = T * n_h
+    kx = k.reshape(L, dk)
+    vx = v.reshape(L, v.shape[-1])
+    bx = beta.reshape(L)
+    gx = np.ones(L)
+    if g is not None:
+        gx[0::n_h] = g
+    qx = np.repeat(q, n_h, axis=0)
+    idx = np.arange(T) * n_h + (n_h - 1)
+    return qx, kx, vx, bx, gx, idx
+
+
+# --------------------------------------------------------------------------
+# sequence forms for DeltaNet / Gated DeltaNet (one step per row)
+# --------------------------------------------------------------------------
+def recurrent_householder(q, k, v, beta, g=None, S0=None):
+    """Token loop written with explicit transition matrices:
+    S_t = g_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T, o_t = S_t^T q_t
+    ([DR] §1.2 and §3; the scalar gate commutes with the Householder factor)."""
+    L, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((L, dv))
+    for t in range(L):
+        gt = 1.0 if g is None else g[t]
+        S = gt * (householder_factor(k[t], beta[t]) @ S) + beta[t] * np.outer(k[t], v[t])
+        o[t] = S.T @ q[t]
+    return o, S
+
+
+def wy_chunk(q, k, v, beta, S0=None, C=16):
+    """[DR] §2.1 WY representation, ungated.  Inside a chunk starting from
+    state S0, the product of Householder factors is I - sum_i k_i w_i^T and the
+    accumulated writes are sum_i k_i u_i^T, with
+        w_r = beta_r (k_r - sum_{i<r} w_i (k_i^T k_r)),
+        u_r = beta_r (v_r - sum_{i<r} u_i (k_i^T k_r)),
+    so S_r = S0 + sum_{i<=r} k_i (u_i - S0^T w_i)^T.  Recursions run row by row."""
+    L, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((L, dv))
+    for s in range(0, L, C):
+        e = min(s + C, L)
+        n = e - s
+        w = np.zeros((n, dk))
+        u = np.zeros((n, dv))
+        for r in range(n):
+            kr = k[s + r]
+            w_acc = kr.copy()
+            u_acc = v[s + r].copy()
+            for i in range(r):
+                c = k[s + i] @ kr
+                w_acc -= w[i] * c
+                u_acc -= u[i] * c
+            w[r] = beta[s + r] * w_acc
+            u[r] = beta[s + r] * u_acc
+        for r in range(n):
+            Sr = S.copy()
+            for i in range(r + 1):
+                Sr += np.outer(k[s + i], u[i] - S.T @ w[i])
+            o[s + r] = Sr.T @ q[s + r]
+        Snew = S.copy()
+        for i in range(n):
+            Snew += np.outer(k[s + i], u[i] - S.T @ w[i])
+        S = Snew
+    return o, S
+
+
+def ut_chunk(q, k, v, beta, log_g=None, S0=None, C=16):
+    """[DR] §2.2-§2.3 (UT transform + chunkwise algorithm) and §3 (the gated
+    chunkwise form with the within-chunk cumulative decay).  Per chunk:
+        gc_r   = sum_{e<=r} log g_e          (restarts every chunk, inclusive)
+        Gam_ij = exp(gc_i - gc_j) for j <= i, else 0   (masked BEFORE exp)
+        A      = strictLower(diag(beta) (Gam * K K^T))
+        T      = (I + A)^{-1} diag(beta)      (unit lower triangular solve)
+        W      = T (K * exp(gc)),  U = T V
+        Vt     = U - W S                      (pseudo-values)
+        O      = (Q * exp(gc)) S + (Q K^T * Gam) Vt
+        S     <- exp(gc_C) S + (K * exp(gc_C - gc))^T Vt
+    A ragged tail is padded with identity steps (k = 0, v = 0, beta = 0,
+    log g = 0), which leave the state unchanged."""
+    L, dk = k.shape
+    dv = v.shape[1]
+    if log_g is None:
+        log_g = np.zeros(L)
+    NT = -(-L // C)
+    Lp = NT * C
+    pad = Lp - L
+
+    def padrows(x):
+        return np.concatenate([x, np.zeros((pad,) + x.shape[1:])]) if pad else x
+
+    Q, K, V = padrows(q), padrows(k), padrows(v)
+    bt, lg = padrows(np.asarray(beta, float)), padrows(np.asarray(log_g, float))
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((Lp, dv))
+    incl = np.tril(np.ones((C, C), dtype=bool))
+    strict = np.tril(np.ones((C, C), dtype=bool), -1)
+    for n in range(NT):
+        sl = slice(n * C, (n + 1) * C)
+        Kc, Vc, Qc, bc = K[sl], V[sl], Q[sl], bt[sl]
+        gc = np.cumsum(lg[sl])
+        diff = np.where(incl, gc[:, None] - gc[None, :], -np.inf)
+        Gam = np.exp(diff)
+        A = np.where(strict, bc[:, None] * (Kc @ Kc.T) * Gam, 0.0)
+        Tm = solve_triangular(np.eye(C) + A, np.diag(bc), lower=True,
+                              unit_diagonal=True)
+        W = Tm @ (Kc * np.exp(gc)[:, None])
+        U = Tm @ Vc
+        Vt = U - W @ S
+        o[sl] = (Qc * np.exp(gc)[:, None]) @ S + ((Qc @ Kc.T) * Gam) @ Vt
+        S = np.exp(gc[-1]) * S + (Kc * np.exp(gc[-1] - gc)[:, None]).T @ Vt
+    return o[:L], S
+
+
+def parallel_form(q, k, v, beta):
+    """[DR] §2.4 fully parallel form (ungated, zero initial state): the whole
+    sequence is one block, T = (I + strictLower(diag(beta) K K^T))^{-1} diag(beta),
+    and the attention-like matrix is (Q K^T * M) T with M the causal mask
+    including the diagonal; o = (Q K^T * M) T V."""
+    L = k.shape[0]
+    A = np.tril(beta[:, None] * (k @ k.T), -1)
+    Tm = solve_triangular(np.eye(L) + A, np.diag(beta), lower=True,
+                          unit_diagonal=True)
+    Amap = np.tril(q @ k.T) @ Tm
+    return Amap @ v
+
+
+def dplr(q, w, a, b, kk, vv, S0=None):
+    """[DR] §5 DPLR loop: S_t = (Diag(w_t) + a_t b_t^T) S_{t-1} + kk_t vv_t^T,
+    o_t = S_t^T q_t.  b_t^T acts on the UNdecayed previous state."""
+    L, dk = q.shape
+    dv = vv.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((L, dv))
+    for t in range(L):
+        S = w[t][:, None] * S + np.outer(a[t], b[t] @ S) + np.outer(kk[t], vv[t])
+        o[t] = S.T @ q[t]
+    return o, S
+
+
+def product_expansion(q, k, v, beta, S0=None):
+    """[DR] §2, the intra-chunk expansion (GDN paper Eq. 3), materialising the
+    dk x dk products explicitly -- the naive O(d^2) per step form:
+        P^r = prod_{i=1..r} (I - beta_i k_i k_i^T)   (left to right),
+        H^r = sum_i beta_i v_i k_i^T prod_{j=i+1..r} (I - beta_j k_j k_j^T),
+    written for a [dv, dk] state; transposed to [dk, dv] it reads
+    S^r = (P^r)^T S0 + (H^r)^T.  The whole sequence is one block."""
+    L, dk = k.shape
+    dv = v.shape[1]
+    S0 = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((L, dv))
+    I = np.eye(dk)
+    S = S0
+    for r in range(L):
+        P = I.copy()
+        for i in range(r + 1):
+            P = P @ (I - beta[i] * np.outer(k[i], k[i]))
+        Hm = np.zeros((dv, dk))
+        for i in range(r + 1):
+            term = beta[i] * np.outer(v[i], k[i])
+            for j in range(i + 1, r + 1):
+                term = term @ (I - beta[j] * np.outer(k[j], k[j]))
+            Hm += term
+        S = P.T @ S0 + Hm.T
+        o[r] = S.T @ q[r]
+    return o, S

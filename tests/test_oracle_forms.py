@@ -1,0 +1,156 @@
+"""The C oracle (token-by-token recurrence) against independent float64
+restatements of the other forms on the pages (CPU only, tiny inputs).
+
+Tolerances come from the agreement the pages report for these rewrites
+(golden fixture ``dr_reported_agreement.txt``) with a margin of x100.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import forms, rel_l2
+from pins import read_golden, unit, f32
+
+GOLD = read_golden("dr_reported_agreement.txt")
+TOL = GOLD["margin"] * max(GOLD["deltanet_chunk_vs_recurrent"],
+                           GOLD["gdn_chunk_vs_recurrent"])
+
+
+def head_inputs(rng, L, dk, dv, gated=True, beta_hi=1.0, g_lo=0.3):
+    q = f32(rng.standard_normal((L, dk)))
+    k = f32(unit(rng.standard_normal((L, dk))))
+    v = f32(rng.standard_normal((L, dv)))
+    beta = f32(rng.uniform(0, beta_hi, L))
+    g = f32(rng.uniform(g_lo, 1.0, L)) if gated else None
+    S0 = f32(rng.standard_normal((dk, dv)) * 0.5)
+    return q, k, v, beta, g, S0
+
+
+def run_oracle(q, k, v, beta, g, S0):
+    L, dk = q.shape
+    dv = v.shape[1]
+    o, s = oracle.fwd(q.reshape(1, L, 1, dk), k.reshape(1, L, 1, dk),
+                      v.reshape(1, L, 1, dv), beta.reshape(1, L, 1),
+                      None if g is None else g.reshape(1, L, 1),
+                      None if S0 is None else S0.reshape(1, 1, dk, dv))
+    return o[0, :, 0], s[0, 0]
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_householder_loop(gated):
+    rng = np.random.default_rng(1)
+    q, k, v, beta, g, S0 = head_inputs(rng, 37, 8, 6, gated, beta_hi=2.0)
+    o, s = run_oracle(q, k, v, beta, g, S0)
+    o2, s2 = forms.recurrent_householder(q, k, v, beta, g, S0)
+    assert rel_l2(o, o2) < TOL and rel_l2(s, s2) < TOL
+
+
+@pytest.mark.parametrize("C", [1, 3, 7, 16])
+def test_wy_representation(C):
+    rng = np.random.default_rng(2)
+    q, k, v, beta, _, S0 = head_inputs(rng, 41, 8, 5, gated=False)
+    o, s = run_oracle(q, k, v, beta, None, S0)
+    o2, s2 = forms.wy_chunk(q, k, v, beta, S0, C)
+    assert rel_l2(o, o2) < TOL and rel_l2(s, s2) < TOL
+
+
+@pytest.mark.parametrize("C", [1, 7, 16, 50, 64])
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("beta_hi", [1.0, 2.0])
+def test_ut_chunkwise(C, gated, beta_hi):
+    rng = np.random.default_rng(3 + C)
+    L = 50  # ragged against 7, 16 and 64
+    q, k, v, beta, g, S0 = head_inputs(rng, L, 16, 8, gated, beta_hi)
+    o, s = run_oracle(q, k, v, beta, g, S0)
+    lg = None if g is None else np.log(g)
+    o2, s2 = forms.ut_chunk(q, k, v, beta, lg, S0, C)
+    assert rel_l2(o, o2) < TOL, rel_l2(o, o2)
+    assert rel_l2(s, s2) < TOL, rel_l2(s, s2)
+
+
+def test_ut_chunkwise_deltaproduct_extended():
+    """[DP] §4.1: the chunkwise DeltaNet form run on the extended sequence with
+    the expanded gate equals the DeltaProduct oracle (readout at each token's
+    last sub-step), also when token groups straddle chunk boundaries."""
+    rng = np.random.default_rng(4)
+    T, n_h, dk, dv = 23, 3, 8, 6
+    q = f32(rng.standard_normal((1, T, 1, dk)))
+    k = f32(unit(rng.standard_normal((1, T, n_h, 1, dk))))
+    v = f32(rng.standard_normal((1, T, n_h, 1, dv)))
+    beta = f32(2.0 * rng.uniform(0, 1, (1, T, n_h, 1)))
+    g = f32(rng.uniform(0.3, 1, (1, T, 1)))
+    o, s = oracle.fwd(q, k, v, beta, g, None, n_h=n_h)
+    qx, kx, vx, bx, gx, idx = forms.extend_sequence(
+        q[0, :, 0], k[0, :, :, 0], v[0, :, :, 0], beta[0, :, :, 0], g[0, :, 0], n_h)
+    for C in (4, 16, 64):
+        ox, sx = forms.ut_chunk(qx, kx, vx, bx, np.log(gx), None, C)
+        assert rel_l2(ox[idx], o[0, :, 0]) < TOL
+        assert rel_l2(sx, s[0, 0]) < TOL
+
+
+def test_gate_zero_with_log_clamp():
+    """A zero gate has log g = -inf; the chunkwise form takes log g clamped at
+    -80 (e^-80 ~ 1.8e-35).  It must match the oracle's exact reset."""
+    rng = np.random.default_rng(5)
+    q, k, v, beta, g, S0 = head_inputs(rng, 40, 8, 8, gated=True)
+    g[[3, 17, 18, 39]] = 0.0
+    o, s = run_oracle(q, k, v, beta, g, S0)
+    lg = np.maximum(np.log(np.maximum(g, 1e-300)), -80.0)
+    o2, s2 = forms.ut_chunk(q, k, v, beta, lg, S0, 16)
+    assert rel_l2(o, o2) < TOL and rel_l2(s, s2) < TOL
+
+
+def test_parallel_form():
+    rng = np.random.default_rng(6)
+    q, k, v, beta, _, _ = head_inputs(rng, 30, 8, 5, gated=False)
+    o, _ = run_oracle(q, k, v, beta, None, None)
+    o2 = forms.parallel_form(q, k, v, beta)
+    assert rel_l2(o, o2) < TOL
+
+
+def test_dplr_reductions():
+    """[DR] §5: DeltaNet is DPLR with w = 1, a = -beta k, b = k, write beta k v^T;
+    Gated DeltaNet has w = alpha, a = -beta k, b = alpha k."""
+    rng = np.random.default_rng(7)
+    L, dk, dv = 25, 6, 4
+    q, k, v, beta, g, S0 = head_inputs(rng, L, dk, dv, gated=True)
+    ones = np.ones((L, dk))
+    o, s = run_oracle(q, k, v, beta, None, S0)
+    o2, s2 = forms.dplr(q, ones, -beta[:, None] * k, k, beta[:, None] * k, v, S0)
+    assert rel_l2(o, o2) < GOLD["margin"] * GOLD["dplr_deltanet"] * 10
+    assert rel_l2(s, s2) < GOLD["margin"] * GOLD["dplr_deltanet"] * 10
+    o, s = run_oracle(q, k, v, beta, g, S0)
+    o2, s2 = forms.dplr(q, g[:, None] * ones, -beta[:, None] * k,
+                        g[:, None] * k, beta[:, None] * k, v, S0)
+    assert rel_l2(o, o2) < GOLD["margin"] * GOLD["dplr_gdn"] * 10
+    assert rel_l2(s, s2) < GOLD["margin"] * GOLD["dplr_gdn"] * 10
+
+
+def test_product_expansion():
+    rng = np.random.default_rng(8)
+    q, k, v, beta, _, S0 = head_inputs(rng, 9, 5, 4, gated=False, beta_hi=2.0)
+    o, s = run_oracle(q, k, v, beta, None, S0)
+    o2, s2 = forms.product_expansion(q, k, v, beta, S0)
+    assert rel_l2(o, o2) < TOL and rel_l2(s, s2) < TOL
+
+
+def test_batched_heads_are_independent():
+    """Every (b, h) head is an independent sequence: running the batch at once
+    equals running each head alone (also checks the oracle's layouts)."""
+    rng = np.random.default_rng(9)
+    B, T, H, dk, dv, n_h = 2, 13, 3, 6, 5, 2
+    q = f32(rng.standard_normal((B, T, H, dk)))
+    k = f32(unit(rng.standard_normal((B, T, n_h, H, dk))))
+    v = f32(rng.standard_normal((B, T, n_h, H, dv)))
+    beta = f32(rng.uniform(0, 2, (B, T, n_h, H)))
+    g = f32(rng.uniform(0, 1, (B, T, H)))
+    h0 = f32(rng.standard_normal((B, H, dk, dv)))
+    o, s = oracle.fwd(q, k, v, beta, g, h0, n_h=n_h, threads=4)
+    for b in range(B):
+        for h in range(H):
+            o1, s1 = oracle.fwd(q[b:b+1, :, h:h+1], k[b:b+1, :, :, h:h+1],
+                                v[b:b+1, :, :, h:h+1], beta[b:b+1, :, :, h:h+1],
+                                g[b:b+1, :, h:h+1], h0[b:b+1, h:h+1], n_h=n_h,
+                                threads=1)
+            assert np.array_equal(o1[0, :, 0], o[b, :, h])
+            assert np.array_equal(s1[0, 0], s[b, h])
