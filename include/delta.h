@@ -1,0 +1,120 @@
+/*
+ * delta.h -- C ABI of libdelta: the forward pass of delta-rule linear
+ * attention (DeltaNet, Gated DeltaNet, Gated DeltaProduct) and its
+ * single-token decode step, for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  For every batch row b and head h, independently, a state
+ * S in R^{dk x dv} runs through the recurrence
+ *
+ *     S <- g_t * S                                    (once per token)
+ *     for j = 0 .. n_h-1:                             (n_h sub-steps)
+ *         S <- (I - beta_tj k_tj k_tj^T) S + beta_tj k_tj v_tj^T
+ *     o_t = S^T q_t                                   (after the update)
+ *
+ * as defined in "08 · linear 路线（三）：delta rule 与 DPLR 统一框架"
+ * (llm-infra-atlas), §1.2 (the simplified Householder form) and §3 (Gated
+ * DeltaNet, scalar gate), and in "DeltaProduct：通过 Householder 乘积增强线性
+ * RNN 的状态追踪" (reading notes), §2.2 (n_h Householder sub-steps per token)
+ * and §2.6 (the gate applied once, before the sub-steps).  delta_fwd computes
+ * it chunkwise through the WY representation and the UT transform
+ * (§2.1-§2.3 and §3 "chunkwise 形式" of the first page), treating DeltaProduct
+ * as DeltaNet on the extended sequence of length n_h*T (§4.1 of the second).
+ *
+ * Conventions common to both calls
+ *   - There is no query scale: callers pre-scale q.
+ *   - Inputs are used as given: keys are not normalised and beta is not
+ *     clamped (||k|| = 1 and beta in [0, 2] keep the recurrence stable).
+ *   - g is the LINEAR gate in [0, 1]; g = 0 resets the state.  NULL means 1.
+ *   - Every pointer is device memory owned by the caller, contiguous in the
+ *     layout given, and 16-byte aligned.  The library allocates no device
+ *     memory per call and keeps no state between calls; it is thread-safe.
+ *   - Both calls only enqueue work on `stream` and return; they never
+ *     synchronise.  Argument errors are returned before anything is enqueued.
+ *     A failed launch returns DELTA_ERR_CUDA.  NaN/Inf inputs propagate and
+ *     are not detected.
+ *   - `out` must not overlap any input.  `hT`/`state` may be updated in place
+ *     (hT == h0 is allowed) but must not partially overlap anything else.
+ *
+ * Supported set: dk, dv in {16, 32, 64, 128}; chunk in {16, 32, 64};
+ * 1 <= n_h <= 4; B, H, T >= 0 with B*H < 2^31.  Anything else returns
+ * DELTA_ERR_UNSUPPORTED.  Empty problems (B*H*T == 0) are valid.
+ */
+#ifndef DELTA_H_
+#define DELTA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* == cudaStream_t; NULL is the legacy default stream */
+
+typedef enum {
+    DELTA_OK = 0,
+    DELTA_ERR_INVALID = -1,     /* NULL pointer, negative size, bad dtype, overlap */
+    DELTA_ERR_UNSUPPORTED = -2, /* outside the supported set above */
+    DELTA_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+    DELTA_ERR_CUDA = -4         /* a CUDA call failed; see delta_last_error() */
+} delta_status;
+
+typedef enum {
+    DELTA_F32 = 0,  /* q, k, v, out are float32 */
+    DELTA_BF16 = 1  /* q, k, v, out are bfloat16 (outputs rounded to nearest even) */
+} delta_dtype;
+
+/*
+ * delta_fwd -- chunked forward over a whole sequence.
+ *
+ *   q    [B, T, H, dk]        dtype   queries, one per token
+ *   k    [B, T, n_h, H, dk]   dtype   keys, one per sub-step
+ *   v    [B, T, n_h, H, dv]   dtype   values, one per sub-step
+ *   beta [B, T, n_h, H]       float32 write strengths
+ *   g    [B, T, H]            float32 linear gate per token, or NULL (=> 1)
+ *   h0   [B, H, dk, dv]       float32 initial state (row = key index), or NULL (=> 0)
+ *   out  [B, T, H, dv]        dtype   o_t after token t's last sub-step
+ *   hT   [B, H, dk, dv]       float32 state after the last token, or NULL (=> not written)
+ *   chunk                      rows of the extended sequence per chunk
+ *
+ * For n_h == 1 the sub-step axis has extent 1, i.e. k is [B, T, H, dk].
+ */
+int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
+              const float *g, const float *h0, void *out, float *hT,
+              int B, int H, int T, int dk, int dv, int n_h, int chunk,
+              delta_dtype dtype, struct CUstream_st *stream);
+
+/*
+ * delta_step -- one decode token for every (b, h): the recurrent form of
+ * "08 · linear 路线（三）" §2.3 (the decode path) with the sub-steps and gate of
+ * "DeltaProduct" §2.6.  The float32 state is read once and written once, in
+ * place.
+ *
+ *   q     [B, H, dk]          dtype
+ *   k     [B, n_h, H, dk]     dtype
+ *   v     [B, n_h, H, dv]     dtype
+ *   beta  [B, n_h, H]         float32
+ *   g     [B, H]              float32 linear gate, or NULL (=> 1)
+ *   state [B, H, dk, dv]      float32, in/out
+ *   out   [B, H, dv]          dtype
+ */
+int delta_step(const void *q, const void *k, const void *v, const float *beta,
+               const float *g, float *state, void *out,
+               int B, int H, int dk, int dv, int n_h,
+               delta_dtype dtype, struct CUstream_st *stream);
+
+/* Static English text for a delta_status value. */
+const char *delta_status_string(int status);
+
+/*
+ * Detail of the last non-OK status returned on the calling thread (for
+ * DELTA_ERR_CUDA the CUDA error name and the call that failed).  The pointer
+ * stays valid until the next call on the same thread.
+ */
+const char *delta_last_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int delta_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DELTA_H_ */

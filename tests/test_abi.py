@@ -1,0 +1,133 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+symbol include/delta.h declares, and rejects bad arguments before touching
+CUDA (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_rnn_gb300 as wr
+from weight_rnn_gb300 import build as wbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "delta.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    wbuild.build()
+    return wr.load_library()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(delta_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(wr.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_has_no_cudart_runtime_dependency():
+    # the CUDA runtime is linked statically so the library loads without a GPU
+    with open(wr.library_path(), "rb") as f:
+        data = f.read()
+    assert b"libcudart.so" not in data
+
+
+def test_status_strings(lib):
+    assert wr.delta_status_string(wr.DELTA_OK) == "success"
+    for st in (wr.DELTA_ERR_INVALID, wr.DELTA_ERR_UNSUPPORTED, wr.DELTA_ERR_ALIGN,
+               wr.DELTA_ERR_CUDA):
+        assert wr.delta_status_string(st) not in ("success", "unknown status")
+    assert wr.delta_status_string(12345) == "unknown status"
+    assert wr.delta_version() >= 100
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, beta=FAKE * 4, g=None, h0=None,
+             out=FAKE * 5, hT=None, B=1, H=1, T=4, dk=16, dv=16, n_h=1, chunk=16,
+             dtype=wr.DELTA_F32)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_fwd(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["beta"]), vp(a["g"]),
+                         vp(a["h0"]), vp(a["out"]), vp(a["hT"]), a["B"], a["H"], a["T"],
+                         a["dk"], a["dv"], a["n_h"], a["chunk"], a["dtype"], None)
+
+
+def step(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, beta=FAKE * 4, g=None, state=FAKE * 5,
+             out=FAKE * 6, B=1, H=1, dk=16, dv=16, n_h=1, dtype=wr.DELTA_F32)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_step(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["beta"]), vp(a["g"]),
+                          vp(a["state"]), vp(a["out"]), a["B"], a["H"], a["dk"], a["dv"],
+                          a["n_h"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=48), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(dv=256), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(chunk=128), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(chunk=8), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(n_h=0), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(n_h=5), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(B=-1), wr.DELTA_ERR_INVALID),
+    (dict(T=-3), wr.DELTA_ERR_INVALID),
+    (dict(dtype=7), wr.DELTA_ERR_INVALID),
+    (dict(q=None), wr.DELTA_ERR_INVALID),
+    (dict(beta=None), wr.DELTA_ERR_INVALID),
+    (dict(out=None), wr.DELTA_ERR_INVALID),
+    (dict(k=FAKE + 8), wr.DELTA_ERR_ALIGN),
+    (dict(hT=FAKE * 7 + 4), wr.DELTA_ERR_ALIGN),
+    (dict(out=FAKE + 16), wr.DELTA_ERR_INVALID),         # out overlaps q
+    (dict(hT=FAKE * 3), wr.DELTA_ERR_INVALID),           # hT overlaps v
+    (dict(h0=FAKE * 8, hT=FAKE * 8 + 16), wr.DELTA_ERR_INVALID),  # partial overlap
+    (dict(B=1 << 16, H=1 << 15), wr.DELTA_ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_before_launch(lib, kw, status):
+    assert fwd(lib, **kw) == status
+    assert wr.delta_last_error() != ""
+
+
+def test_fwd_empty_batch_is_ok_without_gpu(lib):
+    # B*H == 0 is a valid empty problem: nothing is enqueued
+    assert fwd(lib, B=0) == wr.DELTA_OK
+    assert fwd(lib, H=0, q=None, k=None, v=None, beta=None, out=None) == wr.DELTA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=8), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(n_h=9), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(H=-2), wr.DELTA_ERR_INVALID),
+    (dict(state=None), wr.DELTA_ERR_INVALID),
+    (dict(g=FAKE * 9 + 2), wr.DELTA_ERR_ALIGN),
+    (dict(out=FAKE + 32), wr.DELTA_ERR_INVALID),
+    (dict(state=FAKE * 2), wr.DELTA_ERR_INVALID),
+])
+def test_step_rejects_before_launch(lib, kw, status):
+    assert step(lib, **kw) == status
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 4, 1, 16)
+    with pytest.raises(ValueError):
+        wr.delta_fwd(q, q, torch.zeros(1, 4, 1, 16), torch.zeros(1, 4, 1))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(wr, "_lib", None)
+    monkeypatch.setattr(wr, "library_path", lambda: str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        wr.load_library()

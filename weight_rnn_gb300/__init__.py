@@ -1,0 +1,195 @@
+"""weight_rnn_gb300 -- delta-rule linear attention forward for one GB300.
+
+A thin Python binding over the C ABI of ``libdelta.so`` (declared in
+``include/delta.h``).  The functions keep the ABI's names and only marshal
+arguments: shape/dtype checks, output allocation through PyTorch, the
+current CUDA stream, and status-to-exception mapping.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback, and a
+missing library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["delta_fwd", "delta_step", "delta_status_string", "delta_last_error",
+           "delta_version", "DeltaError", "library_path", "load_library",
+           "DELTA_OK", "DELTA_ERR_INVALID", "DELTA_ERR_UNSUPPORTED",
+           "DELTA_ERR_ALIGN", "DELTA_ERR_CUDA", "DELTA_F32", "DELTA_BF16",
+           "EXPORTED_SYMBOLS"]
+
+DELTA_OK = 0
+DELTA_ERR_INVALID = -1
+DELTA_ERR_UNSUPPORTED = -2
+DELTA_ERR_ALIGN = -3
+DELTA_ERR_CUDA = -4
+DELTA_F32 = 0
+DELTA_BF16 = 1
+
+#: every extern "C" entry point include/delta.h declares
+EXPORTED_SYMBOLS = ("delta_fwd", "delta_step", "delta_status_string",
+                    "delta_last_error", "delta_version")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class DeltaError(RuntimeError):
+    """A libdelta call returned a non-OK status."""
+
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{delta_status_string(status)} ({status}): {detail}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libdelta.so")
+
+
+def load_library():
+    """Open libdelta.so and declare the ABI; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m weight_rnn_gb300.build` "
+                "(the CUDA library is required; there is no fallback)")
+        lib = ctypes.CDLL(path)
+        p, i = ctypes.c_void_p, ctypes.c_int
+        lib.delta_fwd.restype = i
+        lib.delta_fwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.delta_step.restype = i
+        lib.delta_step.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, p]
+        lib.delta_status_string.restype = ctypes.c_char_p
+        lib.delta_status_string.argtypes = [i]
+        lib.delta_last_error.restype = ctypes.c_char_p
+        lib.delta_last_error.argtypes = []
+        lib.delta_version.restype = i
+        lib.delta_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def delta_status_string(status: int) -> str:
+    return load_library().delta_status_string(int(status)).decode()
+
+
+def delta_last_error() -> str:
+    return load_library().delta_last_error().decode()
+
+
+def delta_version() -> int:
+    return int(load_library().delta_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(dt):
+    if dt == torch.bfloat16:
+        return DELTA_BF16
+    if dt == torch.float32:
+        return DELTA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {dt}")
+
+
+def _check(t, name, shape, dtype, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def delta_fwd(q, k, v, beta, g=None, h0=None, out=None, hT=None, *, n_h=1,
+              chunk=64, want_state=True, stream=None):
+    """Chunked forward of Gated DeltaProduct (DeltaNet for n_h = 1, g = None).
+
+    q [B,T,H,dk]; k [B,T,n_h,H,dk] (or [B,T,H,dk] when n_h = 1);
+    v [B,T,n_h,H,dv] (or [B,T,H,dv]); beta [B,T,n_h,H] (or [B,T,H]) float32;
+    g [B,T,H] float32 linear gate or None; h0 [B,H,dk,dv] float32 or None.
+    q/k/v share one dtype (bfloat16 or float32), which ``out`` takes too.
+    Returns ``(out [B,T,H,dv], hT [B,H,dk,dv] float32 or None)``; ``hT`` may be
+    passed as ``h0`` to update the state in place.
+    """
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("delta_fwd needs CUDA tensors")
+    dt = q.dtype
+    code = _dtype_code(dt)
+    if n_h == 1 and k.dim() == 4:
+        kshape, vshape, bshape = (B, T, H, dk), (B, T, H, v.shape[-1]), (B, T, H)
+    else:
+        kshape, vshape, bshape = (B, T, n_h, H, dk), (B, T, n_h, H, v.shape[-1]), (B, T, n_h, H)
+    dv = v.shape[-1]
+    _check(q, "q", (B, T, H, dk), dt, dev)
+    _check(k, "k", kshape, dt, dev)
+    _check(v, "v", vshape, dt, dev)
+    _check(beta, "beta", bshape, torch.float32, dev)
+    _check(g, "g", (B, T, H), torch.float32, dev)
+    _check(h0, "h0", (B, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=dt, device=dev)
+    _check(out, "out", (B, T, H, dv), dt, dev)
+    if hT is None and want_state:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(hT, "hT", (B, H, dk, dv), torch.float32, dev)
+    st = lib.delta_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                       _ptr(out), _ptr(hT), B, H, T, dk, dv, n_h, chunk, code,
+                       _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return out, hT
+
+
+def delta_step(q, k, v, beta, g, state, out=None, *, n_h=1, stream=None):
+    """One decode token; ``state`` [B,H,dk,dv] float32 is updated in place.
+
+    q [B,H,dk]; k [B,n_h,H,dk]; v [B,n_h,H,dv]; beta [B,n_h,H] float32;
+    g [B,H] float32 or None.  Returns ``out`` [B,H,dv] in q's dtype.
+    """
+    lib = load_library()
+    B, H, dk = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("delta_step needs CUDA tensors")
+    dt = q.dtype
+    code = _dtype_code(dt)
+    dv = v.shape[-1]
+    _check(q, "q", (B, H, dk), dt, dev)
+    _check(k, "k", (B, n_h, H, dk), dt, dev)
+    _check(v, "v", (B, n_h, H, dv), dt, dev)
+    _check(beta, "beta", (B, n_h, H), torch.float32, dev)
+    _check(g, "g", (B, H), torch.float32, dev)
+    _check(state, "state", (B, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=dt, device=dev)
+    _check(out, "out", (B, H, dv), dt, dev)
+    st = lib.delta_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(state),
+                        _ptr(out), B, H, dk, dv, n_h, code, _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return out

@@ -1,0 +1,166 @@
+// api.cu -- the C ABI declared in include/delta.h: argument validation,
+// kernel selection and error reporting.  No device memory is allocated here
+// and nothing is synchronised: each call enqueues kernels on the caller's
+// stream and returns.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstdarg>
+#include <cstring>
+
+#include "../../include/delta.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "no error";
+
+int fail(int status, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int status, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t err, const char *what) {
+  return fail(DELTA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err),
+              cudaGetErrorString(err));
+}
+
+bool supported_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool supported_chunk(int c) { return c == 16 || c == 32 || c == 64; }
+bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+Range range(const void *p, int64_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Range{lo, lo + (uintptr_t)bytes};
+}
+bool overlap(Range a, Range b) {
+  return a.lo != 0 && b.lo != 0 && a.hi > a.lo && b.hi > b.lo && a.lo < b.hi && b.lo < a.hi;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *delta_status_string(int status) {
+  switch (status) {
+    case DELTA_OK: return "success";
+    case DELTA_ERR_INVALID: return "invalid argument";
+    case DELTA_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case DELTA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case DELTA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char *delta_last_error(void) { return g_last_error; }
+
+int delta_version(void) { return 100; }
+
+int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
+              const float *g, const float *h0, void *out, float *hT, int B, int H,
+              int T, int dk, int dv, int n_h, int chunk, delta_dtype dtype,
+              struct CUstream_st *stream) {
+  if (B < 0 || H < 0 || T < 0)
+    return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d T=%d", B, H, T);
+  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
+    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (!supported_dim(dk) || !supported_dim(dv))
+    return fail(DELTA_ERR_UNSUPPORTED, "dk=%d dv=%d not in {16,32,64,128}", dk, dv);
+  if (!supported_chunk(chunk))
+    return fail(DELTA_ERR_UNSUPPORTED, "chunk=%d not in {16,32,64}", chunk);
+  if (n_h < 1 || n_h > 4) return fail(DELTA_ERR_UNSUPPORTED, "n_h=%d not in [1,4]", n_h);
+  if ((int64_t)B * H >= (int64_t(1) << 31))
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
+
+  const int64_t esz = dtype == DELTA_BF16 ? 2 : 4;
+  const int64_t BH = (int64_t)B * H;
+  const int64_t L = (int64_t)T * n_h;
+  const int64_t state_bytes = BH * dk * dv * 4;
+  if (BH == 0) return DELTA_OK;
+  if (T > 0 && (!q || !k || !v || !beta || !out))
+    return fail(DELTA_ERR_INVALID, "q, k, v, beta and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) ||
+      !aligned16(g) || !aligned16(h0) || !aligned16(out) || !aligned16(hT))
+    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+
+  const Range r_out = range(out, BH * T * dv * esz);
+  const Range r_hT = range(hT, state_bytes);
+  const Range inputs[] = {range(q, BH * T * dk * esz), range(k, BH * L * dk * esz),
+                          range(v, BH * L * dv * esz),  range(beta, BH * L * 4),
+                          range(g, g ? BH * T * 4 : 0), range(h0, h0 ? state_bytes : 0)};
+  for (const Range &r : inputs)
+    if (overlap(r_out, r)) return fail(DELTA_ERR_INVALID, "out overlaps an input");
+  for (int i = 0; i < 5; ++i)
+    if (overlap(r_hT, inputs[i])) return fail(DELTA_ERR_INVALID, "hT overlaps an input");
+  if (overlap(r_hT, r_out)) return fail(DELTA_ERR_INVALID, "hT overlaps out");
+  if (hT && h0 && (const void *)hT != (const void *)h0 && overlap(r_hT, inputs[5]))
+    return fail(DELTA_ERR_INVALID, "hT partially overlaps h0");
+
+  delta::FwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.h0 = h0;
+  a.out = out; a.hT = hT;
+  a.B = B; a.H = H; a.T = T; a.L = L;
+  a.dk = dk; a.dv = dv; a.n_h = n_h; a.chunk = chunk;
+  a.bf16 = dtype == DELTA_BF16;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  cudaError_t err;
+  if (T == 0) {
+    err = delta::launch_state_passthrough(a, s);
+    return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "state passthrough launch");
+  }
+  if (delta::chunk_tc_supports(a)) {
+    err = delta::launch_chunk_tc(a, s);
+    return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "tensor-core chunk kernel launch");
+  }
+  err = delta::launch_chunk_generic(a, s);
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "generic chunk kernel launch");
+}
+
+int delta_step(const void *q, const void *k, const void *v, const float *beta,
+               const float *g, float *state, void *out, int B, int H, int dk, int dv,
+               int n_h, delta_dtype dtype, struct CUstream_st *stream) {
+  if (B < 0 || H < 0) return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d", B, H);
+  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
+    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (!supported_dim(dk) || !supported_dim(dv))
+    return fail(DELTA_ERR_UNSUPPORTED, "dk=%d dv=%d not in {16,32,64,128}", dk, dv);
+  if (n_h < 1 || n_h > 4) return fail(DELTA_ERR_UNSUPPORTED, "n_h=%d not in [1,4]", n_h);
+  if ((int64_t)B * H >= (int64_t(1) << 31))
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
+  const int64_t BH = (int64_t)B * H;
+  if (BH == 0) return DELTA_OK;
+  if (!q || !k || !v || !beta || !state || !out)
+    return fail(DELTA_ERR_INVALID, "q, k, v, beta, state and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) ||
+      !aligned16(g) || !aligned16(state) || !aligned16(out))
+    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+  const int64_t esz = dtype == DELTA_BF16 ? 2 : 4;
+  const Range r_state = range(state, BH * dk * dv * 4);
+  const Range r_out = range(out, BH * dv * esz);
+  const Range inputs[] = {range(q, BH * dk * esz), range(k, BH * n_h * dk * esz),
+                          range(v, BH * n_h * dv * esz), range(beta, BH * n_h * 4),
+                          range(g, g ? BH * 4 : 0)};
+  for (const Range &r : inputs) {
+    if (overlap(r_out, r)) return fail(DELTA_ERR_INVALID, "out overlaps an input");
+    if (overlap(r_state, r)) return fail(DELTA_ERR_INVALID, "state overlaps an input");
+  }
+  if (overlap(r_state, r_out)) return fail(DELTA_ERR_INVALID, "state overlaps out");
+
+  delta::StepArgs a;
+  a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.state = state; a.out = out;
+  a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.n_h = n_h;
+  a.bf16 = dtype == DELTA_BF16;
+  const cudaError_t err = delta::launch_step(a, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "decode step launch");
+}
+
+}  // extern "C"

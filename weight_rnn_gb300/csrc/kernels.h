@@ -1,0 +1,48 @@
+// kernels.h -- internal launch interface between the C-ABI layer (api.cu)
+// and the CUDA kernels.  Not installed; callers use include/delta.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace delta {
+
+// Arguments of one forward call after validation.  Sizes are widened to
+// 64 bits; `L` is the extended sequence length n_h * T.
+struct FwdArgs {
+  const void *q, *k, *v;
+  const float *beta, *g, *h0;
+  void *out;
+  float *hT;
+  int64_t B, H, T, L;
+  int dk, dv, n_h, chunk;
+  bool bf16;
+};
+
+struct StepArgs {
+  const void *q, *k, *v;
+  const float *beta, *g;
+  float *state;
+  void *out;
+  int64_t B, H;
+  int dk, dv, n_h;
+  bool bf16;
+};
+
+// Generic chunked forward on CUDA cores, float32 arithmetic, any supported
+// shape.  Returns the launch error (cudaSuccess if enqueued).
+cudaError_t launch_chunk_generic(const FwdArgs &a, cudaStream_t s);
+
+// Tensor-core chunked forward (tcgen05 + TMEM + TMA) for bf16 I/O with
+// dk = dv = 128 and chunk = 64.  Returns cudaErrorNotSupported when the
+// shape is outside that set.
+cudaError_t launch_chunk_tc(const FwdArgs &a, cudaStream_t s);
+bool chunk_tc_supports(const FwdArgs &a);
+
+// hT <- h0 (or 0) for an empty sequence (T == 0).
+cudaError_t launch_state_passthrough(const FwdArgs &a, cudaStream_t s);
+
+// One decode step, state updated in place.
+cudaError_t launch_step(const StepArgs &a, cudaStream_t s);
+
+}  // namespace delta
