@@ -110,6 +110,16 @@ const char *delta_status_string(int status);
  */
 const char *delta_last_error(void);
 
+/*
+ * delta_check_device -- diagnostic, SYNCHRONOUS: waits for all work on the
+ * current device, then reports whether a library kernel gave up on one of its
+ * bounded internal waits since the last check (DELTA_ERR_CUDA with the detail
+ * in delta_last_error()) and clears that record.  A kernel that gives up ends
+ * early instead of hanging; the outputs of that call are then invalid.
+ * Also returns DELTA_ERR_CUDA for any pending CUDA error on the device.
+ */
+int delta_check_device(void);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int delta_version(void);
 

@@ -34,6 +34,7 @@ def gpu_fwd(inp, w: synth.Workload, device="cuda", h0_gpu=None, chunk=None):
     out, hT = wr.delta_fwd(q, k, v, beta, g, h0, n_h=w.n_h,
                            chunk=chunk or w.chunk)
     torch.cuda.synchronize(dev)
+    wr.delta_check_device()
     return out, hT
 
 

@@ -16,6 +16,7 @@ import threading
 import torch
 
 __all__ = ["delta_fwd", "delta_step", "delta_status_string", "delta_last_error",
+           "delta_check_device",
            "delta_version", "DeltaError", "library_path", "load_library",
            "DELTA_OK", "DELTA_ERR_INVALID", "DELTA_ERR_UNSUPPORTED",
            "DELTA_ERR_ALIGN", "DELTA_ERR_CUDA", "DELTA_F32", "DELTA_BF16",
@@ -31,7 +32,7 @@ DELTA_BF16 = 1
 
 #: every extern "C" entry point include/delta.h declares
 EXPORTED_SYMBOLS = ("delta_fwd", "delta_step", "delta_status_string",
-                    "delta_last_error", "delta_version")
+                    "delta_last_error", "delta_check_device", "delta_version")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -73,6 +74,8 @@ def load_library():
         lib.delta_last_error.argtypes = []
         lib.delta_version.restype = i
         lib.delta_version.argtypes = []
+        lib.delta_check_device.restype = i
+        lib.delta_check_device.argtypes = []
         _lib = lib
         return lib
 
@@ -87,6 +90,14 @@ def delta_last_error() -> str:
 
 def delta_version() -> int:
     return int(load_library().delta_version())
+
+
+def delta_check_device() -> None:
+    """Synchronise the device and raise DeltaError if a library kernel gave up
+    on one of its bounded internal waits since the last check."""
+    st = load_library().delta_check_device()
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
 
 
 def _ptr(t):

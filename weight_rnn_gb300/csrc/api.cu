@@ -64,6 +64,17 @@ const char *delta_last_error(void) { return g_last_error; }
 
 int delta_version(void) { return 100; }
 
+int delta_check_device(void) {
+  unsigned int word = 0;
+  const cudaError_t err = delta::read_and_clear_tc_error(&word);
+  if (err != cudaSuccess) return cuda_fail(err, "device check");
+  if (word != 0)
+    return fail(DELTA_ERR_CUDA,
+                "a kernel wait gave up (role %u, barrier %u): results of that call are invalid",
+                (word & 0xffu) - 1, word >> 8);
+  return DELTA_OK;
+}
+
 int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
               const float *g, const float *h0, void *out, float *hT, int B, int H,
               int T, int dk, int dv, int n_h, int chunk, delta_dtype dtype,

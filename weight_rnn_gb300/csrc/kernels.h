@@ -39,6 +39,10 @@ cudaError_t launch_chunk_generic(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_chunk_tc(const FwdArgs &a, cudaStream_t s);
 bool chunk_tc_supports(const FwdArgs &a);
 
+// Read and clear the word the tensor-core kernel sets when one of its bounded
+// waits gives up (0 = no error).  Synchronises the device.
+cudaError_t read_and_clear_tc_error(unsigned int *word);
+
 // hT <- h0 (or 0) for an empty sequence (T == 0).
 cudaError_t launch_state_passthrough(const FwdArgs &a, cudaStream_t s);
 
