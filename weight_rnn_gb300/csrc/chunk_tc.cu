@@ -330,6 +330,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       const int t_lo = e0 / n_h;
       uint8_t *st = sm.stage(s);
       if (lane == 0) {
+        // keep the chunks after the ones in the ring warm in L2
+        for (int pf = (n == 0 ? NS : n + NS); pf <= n + NS + 1 && pf < NT; ++pf) {
+          const int pe = pf * C, pt = pe / n_h;
+          tma_prefetch_4d(&map_k, 0, h, pe, b);
+          tma_prefetch_4d(&map_k, 64, h, pe, b);
+          tma_prefetch_4d(&map_v, 0, h, pe, b);
+          tma_prefetch_4d(&map_v, 64, h, pe, b);
+          tma_prefetch_4d(&map_q, 0, h, pt, b);
+          tma_prefetch_4d(&map_q, 64, h, pt, b);
+        }
         mbar_arrive_expect_tx(sm.bar(B_FULL + s), 2u * (8192u + 8192u + (uint32_t)QR * 128u));
         uint64_t *fb = sm.bar(B_FULL + s);
         tma_load_4d(st + 0, &map_k, fb, 0, h, e0, b);
@@ -425,9 +435,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           mma_ts(tmem + TM_S, tmem + (GATED ? TM_VDEC : TM_VBF) + k * 8,
                  sdesc_sw128(kq + k * 2048, 16384, 1024), id_s, true);
         mma_commit(sm.bar(B_SFULL));
-        // U, W of the next chunk: W^T is on the next chunk's critical path
-        if (n + 1 < NT && !prep_uw(n + 1)) break;
-        // O^T = S^T (Q * exp gc)^T + Vt^T P^T
+        // O^T = S^T (Q * exp gc)^T + Vt^T P^T; afterwards the stage is free
         if (n >= 1 && !wait_bar(sm, B_OFREE, (n - 1) & 1, 1)) break;
         tc_fence_after();
         const uint32_t qb = GATED ? smem_u32(sm.base + OFF_QG) + (n & 1) * 8192 : kq + 8192;
@@ -442,6 +450,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mma_commit(sm.bar(B_OFULL));
         mma_commit(sm.bar(B_EMPTY + s));
         mma_commit(sm.bar(B_PQFREE0 + (n & 1)));
+        // U, W of the next chunk
+        if (n + 1 < NT && !prep_uw(n + 1)) break;
       }
       mma_commit(sm.bar(B_DRAIN));
       wait_bar(sm, B_DRAIN, 0, 1);
@@ -482,18 +492,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const int i = L;
         const float bi = sb[i];
         const float gi = GATED ? gcp[i] : 0.f;
+        uint32_t r[64];
+        tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+        tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+        tmem_wait_ld_regs(r);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem_addr(tmem + TM_GW, q4 * 32, c0), r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int j = c0 + u;
-            float a = 0.f;
-            if (j < i) a = bi * __uint_as_float(r[u]) * (GATED ? fast_exp2(gi - gcp[j]) : 1.f);
-            At[swz(j, i)] = a;
-          }
+        for (int j = 0; j < 64; ++j) {
+          float a = 0.f;
+          if (j < i) a = bi * __uint_as_float(r[j]) * (GATED ? fast_exp2(gi - gcp[j]) : 1.f);
+          At[swz(j, i)] = a;
         }
       } else {
         // row r of P = (q_r . k_j) Gam, j <= pos(r)
@@ -503,27 +510,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const float gp = (GATED && valid) ? gcp[pos] : 0.f;
         if (m >= 2) wait_bar(sm, B_PQFREE0 + (m & 1), ((m >> 1) - 1) & 1, 2);
         uint8_t *ptile = sm.base + OFF_P + (m & 1) * 8192;
+        uint32_t g64[64];
+        tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&g64[0]));
+        tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&g64[32]));
+        tmem_wait_ld_regs(g64);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-          uint32_t g16[16];
-          tmem_ld16(tmem_addr(tmem + TM_GW, q4 * 32, c0), g16);
-          tmem_wait_ld();
+        for (int q = 0; q < 8; ++q) {
+          uint32_t pk[4];
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int j0 = c0 + q * 8 + 2 * u;
-              const float v0 = (j0 <= pos) ? __uint_as_float(g16[q * 8 + 2 * u]) *
-                                                 (GATED ? fast_exp2(gp - gcp[j0]) : 1.f)
-                                           : 0.f;
-              const float v1 = (j0 + 1 <= pos) ? __uint_as_float(g16[q * 8 + 2 * u + 1]) *
-                                                     (GATED ? fast_exp2(gp - gcp[j0 + 1]) : 1.f)
-                                               : 0.f;
-              pk[u] = pack_bf16(v0, v1);
-            }
-            st_chunk(ptile, sw128_offset(r, c0 + q * 8, 64), pk);
+          for (int u = 0; u < 4; ++u) {
+            const int j0 = q * 8 + 2 * u;
+            const float v0 =
+                (j0 <= pos) ? __uint_as_float(g64[j0]) * (GATED ? fast_exp2(gp - gcp[j0]) : 1.f) : 0.f;
+            const float v1 = (j0 + 1 <= pos)
+                                 ? __uint_as_float(g64[j0 + 1]) * (GATED ? fast_exp2(gp - gcp[j0 + 1]) : 1.f)
+                                 : 0.f;
+            pk[u] = pack_bf16(v0, v1);
           }
+          st_chunk(ptile, sw128_offset(r, q * 8, 64), pk);
         }
       }
       tc_fence_before();
@@ -673,7 +677,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       for (int half = 0; half < 2; ++half) {
         uint32_t r[32];
         tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, half * 32), r);
-        tmem_wait_ld();
+        tmem_wait_ld_regs(r);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t pk[4];
@@ -733,7 +737,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           tmem_ld32(tmem_addr(tmem + TM_UV, q4 * 32, half * 32), r);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(r);
           uint32_t pk[16], pd[16];
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
@@ -763,7 +767,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32], pk[16];
           tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0), r);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(r);
 #pragma unroll
           for (int u = 0; u < 16; ++u)
             pk[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
@@ -777,14 +781,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(sm.bar(B_SREADY));
-        convert_w(n + 1);
       } else if (p.hT) {
         float *hT = p.hT + (size_t)bh * D * D;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32];
           tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0), r);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(r);
 #pragma unroll
           for (int u = 0; u < 32; ++u) hT[(size_t)(c0 + u) * D + L] = __uint_as_float(r[u]);
         }
@@ -803,12 +806,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t r[32];
           tmem_ld32(tmem_addr(tmem + TM_O, q4 * 32, c0), r);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(r);
 #pragma unroll
           for (int u = 0; u < 32; ++u) stg[(c0 + u) * D + L] = __float2bfloat16_rn(__uint_as_float(r[u]));
         }
         tc_fence_before();
         mbar_arrive(sm.bar(B_OFREE));
+        // W^T of the next chunk before the copy-out: it gates the next chain step
+        if (n + 1 < NT) convert_w(n + 1);
         if (named_sync_or(2, *sm.abort_flag() != 0)) break;
         // rows of 256 bytes: 16 threads per row, 8 rows per pass
         const int chunk16 = ct & 15;
