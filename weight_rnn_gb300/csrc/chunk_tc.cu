@@ -25,20 +25,23 @@
 //   U^T   = V^T T^T                    SS  M=128 N=64  K=64    (TMEM, becomes Vt^T)
 //   W^T   = K^T (T diag(exp gc))^T     SS  M=128 N=64  K=64    (TMEM -> smem bf16)
 //   Vt^T += S^T (-W^T)                 TS  M=128 N=64  K=128   (A = S^T bf16 in TMEM)
-//   O^T   = S^T (Q * exp gc)^T         TS  M=128 N=64  K=128
-//   O^T  += Vt^T P^T                   TS  M=128 N=64  K=64    (A = Vt^T bf16 in TMEM)
 //   S^T  += (Vt^T diag(exp(gc_C-gc))) K  TS M=128 N=128 K=64   (S^T pre-scaled by exp gc_C)
+//   O1^T  = S^T Q^T                    TS  M=128 N=64  K=128
+//   O2^T  = Vt^T P^T                   TS  M=128 N=64  K=64    (A = Vt^T bf16 in TMEM)
+//   out   = exp(gc) * O1 + O2          (epilogue; O2 accumulates into O1 when ungated)
 //
 // W and U never leave the SM.  HBM traffic is q, k, v, beta, g in and out,
-// h0/hT once per head.
+// h0/hT once per head.  The UT solve runs on the CUDA cores: 16x16 diagonal
+// blocks by forward substitution in registers (rows exchanged with warp
+// shuffles), then two block merges on the warp-level tensor cores (tf32).
 //
 // Warp roles (320 threads):
-//   warp 0      TMA producer: K/Q/V tiles (128-byte swizzle) + beta/log-gate rows
+//   warp 0      TMA producer: K/Q/V tiles (128-byte swizzle, 3 stages, the
+//               next chunk prefetched into L2) + beta/log-gate rows
 //   warp 1      TMEM owner and the single MMA-issuing thread
-//   warps 2-5   "prep": G -> UT solve -> T tiles, P = Q K^T * Gam, gated Q,
-//               then W^T (TMEM) -> bf16 smem operand        (S-independent)
+//   warps 2-5   "prep": G -> A, P -> UT solve -> T tiles     (S-independent)
 //   warps 6-9   "chain": Vt^T -> bf16 TMEM operands, S^T -> bf16 copy and
-//               gate decay, output epilogue, final state     (S-dependent)
+//               gate decay, W^T -> smem operand, output epilogue, final state
 // The prep stage of chunk n+1 overlaps the state-dependent chain of chunk n.
 // Every mbarrier wait is bounded; a timeout sets a device error word and the
 // kernel winds down instead of hanging.
@@ -58,7 +61,7 @@ using namespace sm100;
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int NS = 2;  // TMA stages
+constexpr int NS = 3;  // TMA stages
 constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLogGateFloor = -80.0f;
@@ -69,22 +72,22 @@ constexpr uint32_t OFF_W = NS * STAGE_BYTES;     // W^T bf16 [128 d][64 c], MN-m
 constexpr uint32_t OFF_TU = OFF_W + 16384;       // T    bf16 [64][64], K-major
 constexpr uint32_t OFF_TW = OFF_TU + 8192;       // T diag(exp gc)
 constexpr uint32_t OFF_P = OFF_TW + 8192;        // 2 x P bf16 [64][64]
-constexpr uint32_t OFF_QG = OFF_P + 16384;       // 2 x gated Q, interleaved blocks
-constexpr uint32_t OFF_AT = OFF_QG + 32768;      // A^T fp32 [64][64]
-constexpr uint32_t OFF_X = OFF_AT + 16384;       // X = (I + A)^{-1} fp32 [64][64]
-constexpr uint32_t OFF_STG = OFF_X + 16384;      // output staging bf16 [64][128]
-constexpr uint32_t OFF_SMALL = OFF_STG + 16384;
-// small region
-constexpr uint32_t SM_BETA = 0;                  // float [NS][64]
-constexpr uint32_t SM_LAM = SM_BETA + NS * 256;  // float [NS][64]  (log2 units)
-constexpr uint32_t SM_GCP = SM_LAM + NS * 256;   // float [64] prep's cumsum (log2 units)
-constexpr uint32_t SM_DEC = SM_GCP + 256;        // float [64] chain's exp2(gc_C - gc)
-constexpr uint32_t SM_BAR = SM_DEC + 256;        // mbarriers
-constexpr int NBARS = 2 * NS + 15;
-constexpr uint32_t SM_TMEM = SM_BAR + NBARS * 8;
-constexpr uint32_t SM_ABORT = SM_TMEM + 4;
-constexpr uint32_t SMALL_BYTES = SM_ABORT + 12;
-constexpr uint32_t SMEM_TOTAL = OFF_SMALL + SMALL_BYTES;
+constexpr uint32_t OFF_A = OFF_P + 16384;        // A^T fp32 [64][64] (entry (j, i) = A_ij)
+constexpr uint32_t OFF_X = OFF_A + 16384;        // X = (I + A)^{-1} fp32 [64][64]
+constexpr uint32_t SMEM_TOTAL = OFF_X + 16384;
+// A^T rows 32..63 only ever hold entries of columns 32..63 (A_ij with
+// i > j >= 32): the first 128 bytes of each of those rows are free and carry
+// the small per-chunk arrays and the barriers, one 128-byte slice per row.
+constexpr int SL_BETA = 0;    // [NS] arrays of 64 floats, 2 slices each
+constexpr int SL_LAM = SL_BETA + 2 * NS;
+constexpr int SL_GCP = SL_LAM + 2 * NS;
+constexpr int SL_DEC = SL_GCP + 2;   // [2]
+constexpr int SL_GAM = SL_DEC + 4;   // [2]
+constexpr int SL_BGC = SL_GAM + 4;
+constexpr int SL_BAR = SL_BGC + 2;   // 16 barriers per slice
+constexpr int NBARS = 2 * NS + 14;
+constexpr int SL_MISC = SL_BAR + (NBARS + 15) / 16;
+static_assert(SL_MISC < 32, "small region must fit in the free slices of A^T");
 constexpr uint32_t SMEM_ALLOC = SMEM_TOTAL + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
@@ -92,8 +95,8 @@ static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 constexpr uint32_t TM_S = 0;        // S^T fp32            [dv][dk]   128 cols
 constexpr uint32_t TM_SBF = 128;    // 2 x S^T bf16 (packed)         2x64 cols
 constexpr uint32_t TM_GW = 256;     // G, then W^T fp32                64 cols
-constexpr uint32_t TM_UV = 320;     // U^T -> Vt^T fp32                64 cols
-constexpr uint32_t TM_O = 384;      // O^T fp32                        64 cols
+constexpr uint32_t TM_UV = 320;     // U^T -> Vt^T -> (gated) O2^T     64 cols
+constexpr uint32_t TM_O = 384;      // O1^T fp32                       64 cols
 constexpr uint32_t TM_VBF = 448;    // Vt^T bf16 (packed)              32 cols
 constexpr uint32_t TM_VDEC = 480;   // Vt^T diag(exp(gc_C - gc)) bf16  32 cols
 constexpr uint32_t TM_COLS = 512;
@@ -103,18 +106,18 @@ enum {
   B_FULL = 0,             // [NS] producer -> consumers (count 2 + tx)
   B_EMPTY = NS,           // [NS] MMA commit -> producer
   B_GFULL = 2 * NS,       // MMA -> prep: G ready in TMEM
-  B_TFULL,                // prep -> MMA: T, P, gated Q in smem (128)
-  B_WFULL,                // MMA -> prep, chain: U, W^T ready (T tiles free)
-  B_WREADY,               // chain -> MMA: W in smem, TMEM W free (128)
+  B_TFULL,                // prep -> MMA: T, P in smem (128)
+  B_WFULL,                // MMA -> chain, prep: U, W^T ready (T tiles consumed)
+  B_WREADY,               // chain -> MMA: W in smem, TMEM GW free (128)
   B_WFREE,                // MMA -> chain: W smem consumed
   B_SREADY,               // chain -> MMA: S^T bf16 ready, S^T decayed (128)
   B_VTFULL,               // MMA -> chain: Vt^T ready
   B_VTREADY,              // chain -> MMA: Vt^T bf16 operands ready (128)
   B_SFULL,                // MMA -> chain: S^T updated
-  B_OFULL,                // MMA -> chain: O^T complete
-  B_OFREE,                // chain -> MMA: O^T read (128)
-  B_PQFREE0,              // MMA -> prep: P / gated Q buffer 0 free
-  B_PQFREE1,              //                                  1
+  B_OFULL,                // MMA -> chain: O1 (and O2) complete
+  B_OFREE,                // chain -> MMA: O1 / O2 read (128)
+  B_PQFREE0,              // MMA -> prep: P buffer 0 free
+  B_PQFREE1,              //                          1
   B_DRAIN,                // MMA: everything issued has completed
 };
 
@@ -125,17 +128,31 @@ struct TcParams {
   int H, T, L, n_h, nchunks;
 };
 
+// 64 floats split over two 128-byte slices.
+struct Arr64 {
+  uint8_t *p0, *p1;
+  __device__ float &operator[](int e) const {
+    return reinterpret_cast<float *>(e < 32 ? p0 : p1)[e & 31];
+  }
+};
+
 struct Smem {
   uint8_t *base;
   __device__ uint8_t *stage(int s) const { return base + s * STAGE_BYTES; }
-  __device__ float *beta(int s) const { return reinterpret_cast<float *>(base + OFF_SMALL + SM_BETA) + s * 64; }
-  __device__ float *lam(int s) const { return reinterpret_cast<float *>(base + OFF_SMALL + SM_LAM) + s * 64; }
-  __device__ float *gcp() const { return reinterpret_cast<float *>(base + OFF_SMALL + SM_GCP); }
-  __device__ float *dec() const { return reinterpret_cast<float *>(base + OFF_SMALL + SM_DEC); }
-  __device__ uint64_t *bar(int i) const { return reinterpret_cast<uint64_t *>(base + OFF_SMALL + SM_BAR) + i; }
-  __device__ uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(base + OFF_SMALL + SM_TMEM); }
-  __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(base + OFF_SMALL + SM_ABORT); }
-  __device__ float *At() const { return reinterpret_cast<float *>(base + OFF_AT); }
+  __device__ uint8_t *slice(int k) const { return base + OFF_A + (32 + k) * 256; }
+  __device__ Arr64 arr(int k) const { return Arr64{slice(k), slice(k + 1)}; }
+  __device__ Arr64 beta(int s) const { return arr(SL_BETA + 2 * s); }
+  __device__ Arr64 lam(int s) const { return arr(SL_LAM + 2 * s); }
+  __device__ Arr64 gcp() const { return arr(SL_GCP); }
+  __device__ Arr64 dec(int b) const { return arr(SL_DEC + 2 * b); }
+  __device__ Arr64 gam(int b) const { return arr(SL_GAM + 2 * b); }
+  __device__ Arr64 bgc() const { return arr(SL_BGC); }
+  __device__ uint64_t *bar(int i) const {
+    return reinterpret_cast<uint64_t *>(slice(SL_BAR + (i >> 4))) + (i & 15);
+  }
+  __device__ uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(slice(SL_MISC)); }
+  __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(slice(SL_MISC) + 4); }
+  __device__ float *At() const { return reinterpret_cast<float *>(base + OFF_A); }
   __device__ float *X() const { return reinterpret_cast<float *>(base + OFF_X); }
 };
 
@@ -156,13 +173,9 @@ __device__ __forceinline__ bool wait_bar(const Smem &sm, int idx, uint32_t parit
 // contiguous and makes the tf32 MMA fragment loads below conflict-free.
 __device__ __forceinline__ int swz(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
 
-// D(16x8) += A(16x8) B(8x8) on the warp-level tensor-core path, tf32 inputs.
+// D(16x8) += A(16x8) B(8x8) on the warp-level tensor-core path, tf32 inputs
+// (fp32 bit patterns; the MMA ignores the low mantissa bits).
 // Fragments: a = {A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]},
 // b = {B[t][g], B[t+4][g]}, d = {D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1]}
 // with g = lane / 4, t = lane % 4.
@@ -175,32 +188,58 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// One warp: D(16x8) = M1[r0.., k0..k0+K) * M2[k0'.., n0..] with both operands
-// read from swizzled fp32 smem.  M1 is read through its transpose when
-// `m1_transposed` (At holds A^T).  K is a multiple of 8.
-template <int K>
-__device__ __forceinline__ void warp_gemm_16x8(float (&d)[4], const float *M1, bool m1_transposed,
-                                               int r0, int k0, const float *M2, int k2, int n0,
-                                               int lane) {
+// One warp: D(16x8) (+)= M1[r0.., k0..k0+K) * M2[k2.., n0..n0+8) (and a second
+// tile at n0 + 8 when TWO) with both operands read from swizzled fp32 smem;
+// M1 is read through its transpose when `m1t` (A^T holds A).  The fp32 bits
+// are fed to the tf32 MMA as they are (the low mantissa bits are ignored).
+template <int K, bool TWO>
+__device__ __forceinline__ void warp_gemm(float (&d0)[4], float (&d1)[4], const float *M1, bool m1t,
+                                          int r0, int k0, const float *M2, int k2, int n0, int lane) {
   const int g = lane >> 2, t = lane & 3;
+  uint32_t a[K / 8][4], b0[K / 8][2], b1[K / 8][2];
 #pragma unroll
   for (int ks = 0; ks < K / 8; ++ks) {
     const int c = k0 + 8 * ks;
-    uint32_t a[4];
-    if (m1_transposed) {
-      a[0] = to_tf32(M1[swz(c + t, r0 + g)]);
-      a[1] = to_tf32(M1[swz(c + t, r0 + g + 8)]);
-      a[2] = to_tf32(M1[swz(c + t + 4, r0 + g)]);
-      a[3] = to_tf32(M1[swz(c + t + 4, r0 + g + 8)]);
+    if (m1t) {
+      a[ks][0] = __float_as_uint(M1[swz(c + t, r0 + g)]);
+      a[ks][1] = __float_as_uint(M1[swz(c + t, r0 + g + 8)]);
+      a[ks][2] = __float_as_uint(M1[swz(c + t + 4, r0 + g)]);
+      a[ks][3] = __float_as_uint(M1[swz(c + t + 4, r0 + g + 8)]);
     } else {
-      a[0] = to_tf32(M1[swz(r0 + g, c + t)]);
-      a[1] = to_tf32(M1[swz(r0 + g + 8, c + t)]);
-      a[2] = to_tf32(M1[swz(r0 + g, c + t + 4)]);
-      a[3] = to_tf32(M1[swz(r0 + g + 8, c + t + 4)]);
+      a[ks][0] = __float_as_uint(M1[swz(r0 + g, c + t)]);
+      a[ks][1] = __float_as_uint(M1[swz(r0 + g + 8, c + t)]);
+      a[ks][2] = __float_as_uint(M1[swz(r0 + g, c + t + 4)]);
+      a[ks][3] = __float_as_uint(M1[swz(r0 + g + 8, c + t + 4)]);
     }
     const int kr = k2 + 8 * ks;
-    const uint32_t b[2] = {to_tf32(M2[swz(kr + t, n0 + g)]), to_tf32(M2[swz(kr + t + 4, n0 + g)])};
-    mma_tf32(d, a, b);
+    b0[ks][0] = __float_as_uint(M2[swz(kr + t, n0 + g)]);
+    b0[ks][1] = __float_as_uint(M2[swz(kr + t + 4, n0 + g)]);
+    if (TWO) {
+      b1[ks][0] = __float_as_uint(M2[swz(kr + t, n0 + 8 + g)]);
+      b1[ks][1] = __float_as_uint(M2[swz(kr + t + 4, n0 + 8 + g)]);
+    }
+  }
+#pragma unroll
+  for (int ks = 0; ks < K / 8; ++ks) {
+    mma_tf32(d0, a[ks], b0[ks]);
+    if (TWO) mma_tf32(d1, a[ks], b1[ks]);
+  }
+}
+
+// T_U = x * beta_j and T_W = x * beta_j exp(gc_j) of a 16x8 fragment of
+// (scale * D) at rows r0.., columns n0.. of the bf16 T tiles.
+__device__ __forceinline__ void frag_to_t(uint8_t *tu, uint8_t *tw, int r0, int n0,
+                                          const float (&d)[4], float scale, const Arr64 &bcol,
+                                          const Arr64 &bgcol, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const int c = n0 + 2 * t;
+  const float b0 = bcol[c], b1 = bcol[c + 1], w0 = bgcol[c], w1 = bgcol[c + 1];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const float x0 = d[2 * hh] * scale, x1 = d[2 * hh + 1] * scale;
+    const int r = r0 + g + 8 * hh;
+    *reinterpret_cast<uint32_t *>(tu + sw128_offset(r, c, 64)) = pack_bf16(x0 * b0, x1 * b1);
+    *reinterpret_cast<uint32_t *>(tw + sw128_offset(r, c, 64)) = pack_bf16(x0 * w0, x1 * w1);
   }
 }
 
@@ -243,7 +282,7 @@ __device__ __forceinline__ bool named_sync_or(int id, bool cond) {
 
 // Inclusive prefix sum over the 64 log-gate entries of a chunk, per warp:
 // lane holds entries lane and lane + 32.
-__device__ __forceinline__ void warp_scan64(const float *lam, int lane, float &lo, float &hi) {
+__device__ __forceinline__ void warp_scan64(const Arr64 &lam, int lane, float &lo, float &hi) {
   lo = lam[lane];
   hi = lam[lane + 32];
 #pragma unroll
@@ -277,11 +316,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const int n_h = p.n_h, NT = p.nchunks;
   const int QR = n_h == 1 ? 64 : 32;  // query rows loaded per chunk
 
-  // ---- set-up: zero the operand buffers, init barriers, allocate TMEM ----
+  // ---- set-up: zero shared memory, init barriers, allocate TMEM ----
   {
     uint4 *z = reinterpret_cast<uint4 *>(sm.base);
-    for (uint32_t i = tid; i < OFF_SMALL / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    for (uint32_t i = tid; i < SMEM_TOTAL / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
   }
+  __syncthreads();
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(sm.bar(B_FULL + s), 2);
@@ -330,8 +370,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       const int t_lo = e0 / n_h;
       uint8_t *st = sm.stage(s);
       if (lane == 0) {
-        // keep the chunks after the ones in the ring warm in L2
-        for (int pf = (n == 0 ? NS : n + NS); pf <= n + NS + 1 && pf < NT; ++pf) {
+        // keep the chunk after the ones in the ring warm in L2
+        for (int pf = (n == 0 ? NS : n + NS); pf <= n + NS && pf < NT; ++pf) {
           const int pe = pf * C, pt = pe / n_h;
           tma_prefetch_4d(&map_k, 0, h, pe, b);
           tma_prefetch_4d(&map_k, 64, h, pe, b);
@@ -349,7 +389,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         tma_load_4d(st + 32768, &map_v, fb, 0, h, e0, b);
         tma_load_4d(st + 40960, &map_v, fb, 64, h, e0, b);
       }
-      float *sb = sm.beta(s), *sl = sm.lam(s);
+      const Arr64 sb = sm.beta(s), sl = sm.lam(s);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int r = lane + 32 * k;
@@ -370,6 +410,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // ===================================================== MMA issuer
     if (lane == 0) {
       bool ok = true;
+      const uint32_t id_g = idesc_bf16(128, 64, false, false);
       const uint32_t id_uw = idesc_bf16(128, 64, true, false);
       const uint32_t id_vt = idesc_bf16(128, 64, false, true, true);  // B = W^T MN-major, negated
       const uint32_t id_o = idesc_bf16(128, 64, false, false);
@@ -377,8 +418,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       const uint32_t a_tu = smem_u32(sm.base + OFF_TU), a_tw = smem_u32(sm.base + OFF_TW);
       const uint32_t a_w = smem_u32(sm.base + OFF_W);
 
-      const uint32_t id_g = idesc_bf16(128, 64, false, false);
-      auto prep_g = [&](int m) -> bool {  // G(m) = [K;Q] K^T
+      auto issue_g = [&](int m) -> bool {  // G(m) = [K;Q] K^T
         const int s = m % NS;
         if (!wait_bar(sm, B_FULL + s, (m / NS) & 1, 1)) return false;
         tc_fence_after();
@@ -392,25 +432,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mma_commit(sm.bar(B_GFULL));
         return true;
       };
-      auto prep_uw = [&](int m) -> bool {  // U(m)^T, W(m)^T
-        const int s = m % NS;
-        if (!wait_bar(sm, B_TFULL, m & 1, 1)) return false;
-        tc_fence_after();
-        const uint32_t kq = smem_u32(sm.stage(s));
-        const uint32_t vv = kq + 32768;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + TM_UV, sdesc_sw128(vv + k * 2048, 8192, 1024),
-                 sdesc_sw128(a_tu + k * 32, 0, 1024), id_uw, k > 0);
+      auto issue_w = [&](int m) {  // W(m)^T = K^T (T diag(exp gc))^T
+        const uint32_t kq = smem_u32(sm.stage(m % NS));
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_ss(tmem + TM_GW, sdesc_sw128(kq + k * 2048, 16384, 1024),
                  sdesc_sw128(a_tw + k * 32, 0, 1024), id_uw, k > 0);
-        mma_commit(sm.bar(B_WFULL));
-        return true;
+      };
+      auto issue_u = [&](int m) {  // U(m)^T = V^T T^T
+        const uint32_t vv = smem_u32(sm.stage(m % NS)) + 32768;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tmem + TM_UV, sdesc_sw128(vv + k * 2048, 8192, 1024),
+                 sdesc_sw128(a_tu + k * 32, 0, 1024), id_uw, k > 0);
       };
 
-      ok = prep_g(0) && prep_uw(0);
+      ok = issue_g(0) && wait_bar(sm, B_TFULL, 0, 1);
+      if (ok) {
+        tc_fence_after();
+        issue_w(0);
+        issue_u(0);
+        mma_commit(sm.bar(B_WFULL));
+      }
       for (int n = 0; ok && n < NT; ++n) {
         const int s = n % NS;
         const uint32_t kq = smem_u32(sm.stage(s));
@@ -418,7 +461,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         if (!wait_bar(sm, B_WREADY, n & 1, 1)) break;
         // G of the next chunk as soon as W^T(n) has left TMEM: its solve
         // overlaps this chunk's state-dependent chain
-        if (n + 1 < NT && !prep_g(n + 1)) break;
+        if (n + 1 < NT && !issue_g(n + 1)) break;
         if (!wait_bar(sm, B_SREADY, n & 1, 1)) break;
         tc_fence_after();
         // Vt^T = U^T - S^T W^T                                (critical chain)
@@ -435,23 +478,34 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           mma_ts(tmem + TM_S, tmem + (GATED ? TM_VDEC : TM_VBF) + k * 8,
                  sdesc_sw128(kq + k * 2048, 16384, 1024), id_s, true);
         mma_commit(sm.bar(B_SFULL));
-        // O^T = S^T (Q * exp gc)^T + Vt^T P^T; afterwards the stage is free
+        // O1^T = S^T Q^T ; O2^T = Vt^T P^T (into the same accumulator when ungated)
         if (n >= 1 && !wait_bar(sm, B_OFREE, (n - 1) & 1, 1)) break;
         tc_fence_after();
-        const uint32_t qb = GATED ? smem_u32(sm.base + OFF_QG) + (n & 1) * 8192 : kq + 8192;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + TM_O, sbf + k * 8, sdesc_sw128(qb + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024),
-                 id_o, k > 0);
+          mma_ts(tmem + TM_O, sbf + k * 8,
+                 sdesc_sw128(kq + 8192 + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024), id_o, k > 0);
         const uint32_t pb = smem_u32(sm.base + OFF_P) + (n & 1) * 8192;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + TM_O, tmem + TM_VBF + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_o, true);
+          mma_ts(tmem + (GATED ? TM_UV : TM_O), tmem + TM_VBF + k * 8,
+                 sdesc_sw128(pb + k * 32, 0, 1024), id_o, GATED ? (k > 0) : true);
         mma_commit(sm.bar(B_OFULL));
         mma_commit(sm.bar(B_EMPTY + s));
         mma_commit(sm.bar(B_PQFREE0 + (n & 1)));
-        // U, W of the next chunk
-        if (n + 1 < NT && !prep_uw(n + 1)) break;
+        // W (and U) of the next chunk
+        if (n + 1 < NT) {
+          if (!wait_bar(sm, B_TFULL, (n + 1) & 1, 1)) break;
+          tc_fence_after();
+          issue_w(n + 1);
+          if (GATED) {
+            // U overwrites O2(n) in TMEM: wait until the epilogue has read it
+            if (!wait_bar(sm, B_OFREE, n & 1, 1)) break;
+            tc_fence_after();
+          }
+          issue_u(n + 1);
+          mma_commit(sm.bar(B_WFULL));
+        }
       }
       mma_commit(sm.bar(B_DRAIN));
       wait_bar(sm, B_DRAIN, 0, 1);
@@ -461,15 +515,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // ===================================================== prep warps
     const int q4 = warp & 3;              // TMEM lane quarter
     const int L = q4 * 32 + lane;         // TMEM lane of this thread
-    float *At = sm.At();
+    const int pw = warp - 2;              // 0..3
+    const int pt = tid - 64;              // 0..127 within the group
+    float *At = sm.At();                  // A^T: entry (j, i) holds A_ij
     float *X = sm.X();
-    float *gcp = sm.gcp();
+    const Arr64 gcp = sm.gcp();
+    const Arr64 bgc = sm.bgc();
+    uint8_t *tu = sm.base + OFF_TU;
+    uint8_t *tw = sm.base + OFF_TW;
     for (int m = 0; m < NT; ++m) {
       const int s = m % NS;
       // a failed wait sets the abort flag; every thread still reaches the
       // next named barrier and all of them leave together after it
       wait_bar(sm, B_FULL + s, (m / NS) & 1, 2);
-      const float *sb = sm.beta(s);
+      const Arr64 sb = sm.beta(s);
       if (GATED && warp == 2) {
         float lo, hi;
         warp_scan64(sm.lam(s), lane, lo, hi);
@@ -477,43 +536,42 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         gcp[lane + 32] = hi;
       }
       if (named_sync_or(1, *sm.abort_flag() != 0)) break;
+      if (pt < 64) bgc[pt] = GATED ? sb[pt] * fast_exp2(gcp[pt]) : sb[pt];
       const int e0 = m * C;
       const int t_lo = e0 / n_h;
       int t_hi = (e0 + C - n_h) / n_h;
       if (t_hi > p.T - 1) t_hi = p.T - 1;
       const int Cp = t_hi - t_lo + 1;  // readout rows of this chunk
 
-      // ---- one row of G = [K;Q] K^T per thread (TMEM lane L), 16 columns at a time ----
-      const int pw = warp - 2;  // 0..3
+      // ---- one row of G = [K;Q] K^T per thread (TMEM lane L) ----
       wait_bar(sm, B_GFULL, m & 1, 2);
       tc_fence_after();
+      uint32_t g[64];
+      tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&g[0]));
+      tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&g[32]));
+      tmem_wait_ld_regs(g);
+      tc_fence_before();
+
       if (L < 64) {
-        // row i of A = beta_i Gam_ij (k_i . k_j) for j < i, stored transposed
-        const int i = L;
+        // ---- row i of A = beta_i Gam_ij (k_i . k_j), j < i, into A^T; blocks
+        //      right of the diagonal block are never read and not stored ----
+        const int i = L, blk = i >> 4;
         const float bi = sb[i];
         const float gi = GATED ? gcp[i] : 0.f;
-        uint32_t r[64];
-        tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-        tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
-        tmem_wait_ld_regs(r);
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          float a = 0.f;
-          if (j < i) a = bi * __uint_as_float(r[j]) * (GATED ? fast_exp2(gi - gcp[j]) : 1.f);
-          At[swz(j, i)] = a;
+          if ((j >> 4) > blk) continue;
+          const float v = bi * __uint_as_float(g[j]) * (GATED ? fast_exp2(gi - gcp[j]) : 1.f);
+          At[swz(j, i)] = ((j >> 4) == blk && j >= i) ? 0.f : v;
         }
       } else {
-        // row r of P = (q_r . k_j) Gam, j <= pos(r)
+        // ---- row r of P = (q_r . k_j) Gam, j <= pos(r) ----
         const int r = L - 64;
         const bool valid = r < Cp;
         const int pos = valid ? (t_lo + r) * n_h + (n_h - 1) - e0 : -1;
         const float gp = (GATED && valid) ? gcp[pos] : 0.f;
         if (m >= 2) wait_bar(sm, B_PQFREE0 + (m & 1), ((m >> 1) - 1) & 1, 2);
         uint8_t *ptile = sm.base + OFF_P + (m & 1) * 8192;
-        uint32_t g64[64];
-        tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&g64[0]));
-        tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&g64[32]));
-        tmem_wait_ld_regs(g64);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           uint32_t pk[4];
@@ -521,147 +579,94 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int u = 0; u < 4; ++u) {
             const int j0 = q * 8 + 2 * u;
             const float v0 =
-                (j0 <= pos) ? __uint_as_float(g64[j0]) * (GATED ? fast_exp2(gp - gcp[j0]) : 1.f) : 0.f;
+                (j0 <= pos) ? __uint_as_float(g[j0]) * (GATED ? fast_exp2(gp - gcp[j0]) : 1.f) : 0.f;
             const float v1 = (j0 + 1 <= pos)
-                                 ? __uint_as_float(g64[j0 + 1]) * (GATED ? fast_exp2(gp - gcp[j0 + 1]) : 1.f)
+                                 ? __uint_as_float(g[j0 + 1]) * (GATED ? fast_exp2(gp - gcp[j0 + 1]) : 1.f)
                                  : 0.f;
             pk[u] = pack_bf16(v0, v1);
           }
           st_chunk(ptile, sw128_offset(r, q * 8, 64), pk);
         }
       }
-      tc_fence_before();
-      if (named_sync_or(1, *sm.abort_flag() != 0)) break;  // A^T complete
+      // the T tiles are rewritten from here on: U/W of the previous chunk
+      // must have consumed them
+      if (m >= 1) wait_bar(sm, B_WFULL, (m - 1) & 1, 2);
+      if (named_sync_or(1, *sm.abort_flag() != 0)) break;  // A^T, P, bgc ready
 
-      if (L < 64) {
-        // ---- diagonal 16x16 blocks of X = (I + A)^{-1}: column jj of block
-        //      b, right-looking forward substitution, next column prefetched ----
-        const int o = (L >> 4) * 16, jj = L & 15;
-        float acc[16];
+      {
+        // ---- 16x16 diagonal blocks of X = (I + A)^{-1}: column jj of block
+        //      blk, rows split over a lane pair, right-looking forward
+        //      substitution; X and the T tiles written as columns finish ----
+        const int blk = pt >> 5, jj = (pt >> 1) & 15, half = pt & 1, o = 16 * blk;
+        const int col = o + jj;
+        const float bcol = sb[col], wcol = bgc[col];
+        float acc[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-        float4 nx[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) nx[q] = *reinterpret_cast<const float4 *>(At + swz(o, o + 4 * q));
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        float4 n0 = *reinterpret_cast<const float4 *>(At + swz(o, o + 8 * half));
+        float4 n1 = *reinterpret_cast<const float4 *>(At + swz(o, o + 8 * half + 4));
 #pragma unroll
         for (int mm = 0; mm < 16; ++mm) {
-          float cur[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            cur[4 * q] = nx[q].x; cur[4 * q + 1] = nx[q].y;
-            cur[4 * q + 2] = nx[q].z; cur[4 * q + 3] = nx[q].w;
-          }
+          const float cur[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
           if (mm + 1 < 16) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              nx[q] = *reinterpret_cast<const float4 *>(At + swz(o + mm + 1, o + 4 * q));
+            n0 = *reinterpret_cast<const float4 *>(At + swz(o + mm + 1, o + 8 * half));
+            n1 = *reinterpret_cast<const float4 *>(At + swz(o + mm + 1, o + 8 * half + 4));
           }
-          const float x = (mm == jj) ? 1.f : ((mm > jj) ? -acc[mm] : 0.f);
-          X[swz(o + mm, o + jj)] = x;
-#pragma unroll
-          for (int i = mm + 1; i < 16; ++i) acc[i] = fmaf(cur[i], x, acc[i]);
-        }
-      } else if (GATED) {
-        // ---- gated query row r: q_r * exp(gc_pos), zero beyond the readout set ----
-        const int r = L - 64;
-        const bool valid = r < Cp;
-        const int pos = valid ? (t_lo + r) * n_h + (n_h - 1) - e0 : 0;
-        const float sc = valid ? fast_exp2(gcp[pos]) : 0.f;
-        const uint8_t *qt = sm.stage(s) + 8192;
-        uint8_t *qg = sm.base + OFF_QG + (m & 1) * 8192;
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t off = blk * 16384 + sw128_offset(r, q * 8, 64);
-            const uint4 v = *reinterpret_cast<const uint4 *>(qt + off);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              __nv_bfloat162 b2;
-              *reinterpret_cast<uint32_t *>(&b2) = w[u];
-              const float2 f = __bfloat1622float2(b2);
-              o4[u] = pack_bf16(f.x * sc, f.y * sc);
-            }
-            st_chunk(qg, off, o4);
+          const int owner = mm >> 3;
+          const float xo = (mm == jj) ? 1.f : ((mm > jj) ? -acc[mm & 7] : 0.f);
+          const float x = __shfl_sync(0xffffffffu, xo, (lane & ~1) | owner);
+          if (half == owner) {
+            X[swz(o + mm, col)] = x;
+            const uint32_t off = sw128_offset(o + mm, col, 64);
+            *reinterpret_cast<__nv_bfloat16 *>(tu + off) = __float2bfloat16_rn(x * bcol);
+            *reinterpret_cast<__nv_bfloat16 *>(tw + off) = __float2bfloat16_rn(x * wcol);
           }
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (8 * half + i > mm) acc[i] = fmaf(cur[i], x, acc[i]);
         }
       }
-      named_sync(1);  // diagonal blocks of X done
+      named_sync(1);
       {
         // ---- merge 16 -> 32: X21' = -X22' (A21' X11') in each 32-row half ----
         const int o = (pw >> 1) * 32, nt = pw & 1;
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-        warp_gemm_16x8<16>(y, At, true, o + 16, o, X, o, o + 8 * nt, lane);
+        float y[4] = {0.f, 0.f, 0.f, 0.f}, unused[4];
+        warp_gemm<16, false>(y, unused, At, true, o + 16, o, X, o, o + 8 * nt, lane);
         // scratch: the unused upper-right 32x32 block of X
         const int sr = (pw >> 1) * 16, scol = 32 + (pw >> 1) * 16 + 8 * nt;
         warp_store_16x8(X, sr, scol, y, 1.f, lane);
         __syncwarp();
         float z[4] = {0.f, 0.f, 0.f, 0.f};
-        warp_gemm_16x8<16>(z, X, false, o + 16, o + 16, X, sr, scol, lane);
+        warp_gemm<16, false>(z, unused, X, false, o + 16, o + 16, X, sr, scol, lane);
         warp_store_16x8(X, o + 16, o + 8 * nt, z, -1.f, lane);
+        frag_to_t(tu, tw, o + 16, o + 8 * nt, z, -1.f, sb, bgc, lane);
       }
       named_sync(1);
       {
-        // ---- merge 32 -> 64: Y = A21 X11 into the upper-right block ----
+        // ---- merge 32 -> 64: Y = A21 X11 into the upper-right block, then
+        //      X21 = -X22 Y straight into the T tiles ----
         const int mr = (pw >> 1) * 16, nc = (pw & 1) * 16;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          float y[4] = {0.f, 0.f, 0.f, 0.f};
-          warp_gemm_16x8<32>(y, At, true, 32 + mr, 0, X, 0, nc + 8 * nt, lane);
-          warp_store_16x8(X, mr, 32 + nc + 8 * nt, y, 1.f, lane);
-        }
+        float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_gemm<32, true>(y0, y1, At, true, 32 + mr, 0, X, 0, nc, lane);
+        warp_store_16x8(X, mr, 32 + nc, y0, 1.f, lane);
+        warp_store_16x8(X, mr, 32 + nc + 8, y1, 1.f, lane);
         named_sync(1);
-        // ---- X21 = -X22 Y ----
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          float z[4] = {0.f, 0.f, 0.f, 0.f};
-          warp_gemm_16x8<32>(z, X, false, 32 + mr, 32, X, 0, 32 + nc + 8 * nt, lane);
-          warp_store_16x8(X, 32 + mr, nc + 8 * nt, z, -1.f, lane);
-        }
-      }
-      named_sync(1);
-      if (m >= 1) wait_bar(sm, B_WFULL, (m - 1) & 1, 2);  // T tiles consumed by U/W(m-1)
-      // ---- T = X diag(beta) and T diag(beta exp gc) as bf16 operand tiles
-      //      (entries above the diagonal of X hold scratch: masked) ----
-      {
-        const int i = (tid & 127) >> 1, jh = (tid & 1) * 32;
-        uint8_t *tu = sm.base + OFF_TU;
-        uint8_t *tw = sm.base + OFF_TW;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t pu[4], pwv[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = jh + q * 8 + 2 * u;
-            const float2 x2 = *reinterpret_cast<const float2 *>(X + swz(i, j));
-            const float u0 = (j <= i) ? x2.x * sb[j] : 0.f;
-            const float u1 = (j + 1 <= i) ? x2.y * sb[j + 1] : 0.f;
-            pu[u] = pack_bf16(u0, u1);
-            if (GATED)
-              pwv[u] = pack_bf16(u0 * fast_exp2(gcp[j]), u1 * fast_exp2(gcp[j + 1]));
-            else
-              pwv[u] = pu[u];
-          }
-          st_chunk(tu, sw128_offset(i, jh + q * 8, 64), pu);
-          st_chunk(tw, sw128_offset(i, jh + q * 8, 64), pwv);
-        }
+        float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_gemm<32, true>(z0, z1, X, false, 32 + mr, 32, X, 0, 32 + nc, lane);
+        frag_to_t(tu, tw, 32 + mr, nc, z0, -1.f, sb, bgc, lane);
+        frag_to_t(tu, tw, 32 + mr, nc + 8, z1, -1.f, sb, bgc, lane);
       }
       fence_proxy_async_smem();
       mbar_arrive(sm.bar(B_TFULL));
-
     }
   } else {
     // ===================================================== chain warps
     const int q4 = warp & 3;
     const int L = q4 * 32 + lane;  // TMEM lane = value column dv
-    const int ct = tid - 192;      // 0..127 within the chain group
-    float *dec = sm.dec();
     // gate of a chunk: 2^(sum of its log2 gates)
     auto chunk_decay = [&](int n) -> float {
       if (!GATED) return 1.f;
-      const float *lam = sm.lam(n % NS);
+      const Arr64 lam = sm.lam(n % NS);
       float t = lam[lane] + lam[lane + 32];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
@@ -673,19 +678,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       if (m >= 1) wait_bar(sm, B_WFREE, (m - 1) & 1, 3);
       tc_fence_after();
       uint8_t *wt = sm.base + OFF_W;
+      uint32_t r[64];
+      tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+      tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+      tmem_wait_ld_regs(r);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, half * 32), r);
-        tmem_wait_ld_regs(r);
+      for (int q = 0; q < 8; ++q) {
+        uint32_t pk[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            pk[u] = pack_bf16(__uint_as_float(r[q * 8 + 2 * u]), __uint_as_float(r[q * 8 + 2 * u + 1]));
-          st_chunk(wt, sw128_offset(L, half * 32 + q * 8, 128), pk);
-        }
+        for (int u = 0; u < 4; ++u)
+          pk[u] = pack_bf16(__uint_as_float(r[q * 8 + 2 * u]), __uint_as_float(r[q * 8 + 2 * u + 1]));
+        st_chunk(wt, sw128_offset(L, q * 8, 128), pk);
       }
       tc_fence_before();
       fence_proxy_async_smem();
@@ -718,9 +721,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     }
     for (int n = 0; ok && n < NT; ++n) {
       const int s = n % NS;
+      const int e0 = n * C;
+      const int t_lo = e0 / n_h;
+      int t_hi = (e0 + C - n_h) / n_h;
+      if (t_hi > p.T - 1) t_hi = p.T - 1;
+      const int Cp = t_hi - t_lo + 1;
       // ---- pseudo-values: Vt^T -> bf16 operands ----
       wait_bar(sm, B_VTFULL, n & 1, 3);
       tc_fence_after();
+      const Arr64 dec = sm.dec(n & 1);
+      const Arr64 gam = sm.gam(n & 1);
       if (GATED) {
         wait_bar(sm, B_FULL + s, (n / NS) & 1, 3);
         if (warp == 6) {
@@ -729,24 +739,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           const float tot = __shfl_sync(0xffffffffu, hi, 31);
           dec[lane] = fast_exp2(tot - lo);
           dec[lane + 32] = fast_exp2(tot - hi);
+          gam[lane] = fast_exp2(lo);
+          gam[lane + 32] = fast_exp2(hi);
         }
         if (named_sync_or(2, *sm.abort_flag() != 0)) break;
       }
       {
-        uint32_t r[32];
+        uint32_t r[64];
+        tmem_ld32(tmem_addr(tmem + TM_UV, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+        tmem_ld32(tmem_addr(tmem + TM_UV, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+        tmem_wait_ld_regs(r);
+        uint32_t pk[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld32(tmem_addr(tmem + TM_UV, q4 * 32, half * 32), r);
-          tmem_wait_ld_regs(r);
-          uint32_t pk[16], pd[16];
+        for (int u = 0; u < 32; ++u)
+          pk[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+        tmem_st32(tmem_addr(tmem + TM_VBF, q4 * 32, 0), pk);
+        if (GATED) {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float a = __uint_as_float(r[2 * u]), c = __uint_as_float(r[2 * u + 1]);
-            pk[u] = pack_bf16(a, c);
-            if (GATED) pd[u] = pack_bf16(a * dec[half * 32 + 2 * u], c * dec[half * 32 + 2 * u + 1]);
-          }
-          tmem_st16(tmem_addr(tmem + TM_VBF, q4 * 32, half * 16), pk);
-          if (GATED) tmem_st16(tmem_addr(tmem + TM_VDEC, q4 * 32, half * 16), pd);
+          for (int u = 0; u < 32; ++u)
+            pk[u] = pack_bf16(__uint_as_float(r[2 * u]) * dec[2 * u],
+                              __uint_as_float(r[2 * u + 1]) * dec[2 * u + 1]);
+          tmem_st32(tmem_addr(tmem + TM_VDEC, q4 * 32, 0), pk);
         }
         tmem_wait_st();
       }
@@ -764,18 +777,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         const uint32_t sbf = tmem + TM_SBF + ((n + 1) & 1) * 64;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32], pk[16];
-          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0), r);
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t r[64], pk[32];
+          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0 + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
           tmem_wait_ld_regs(r);
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
+          for (int u = 0; u < 32; ++u)
             pk[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-          tmem_st16(tmem_addr(sbf, q4 * 32, c0 / 2), pk);
+          tmem_st32(tmem_addr(sbf, q4 * 32, c0 / 2), pk);
           if (GATED) {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * dn);
-            tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, c0), r);
+            for (int u = 0; u < 64; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * dn);
+            tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, c0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+            tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, c0 + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
           }
         }
         tmem_wait_st();
@@ -792,38 +807,66 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int u = 0; u < 32; ++u) hT[(size_t)(c0 + u) * D + L] = __uint_as_float(r[u]);
         }
       }
-      // ---- epilogue: token outputs of this chunk, staged for 16-byte stores ----
+      // ---- outputs of this chunk: o = exp(gc) O1 + O2 per readout row ----
       wait_bar(sm, B_OFULL, n & 1, 3);
       tc_fence_after();
+      float o[64];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t r1[32];
+        tmem_ld32(tmem_addr(tmem + TM_O, q4 * 32, hf * 32), r1);
+        if (GATED) {
+          uint32_t r2[32];
+          tmem_ld32(tmem_addr(tmem + TM_UV, q4 * 32, hf * 32), r2);
+          tmem_wait_ld_regs(r1);
+          tmem_wait_ld_regs(r2);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const int rr = hf * 32 + u;
+            const int pos = (t_lo + rr) * n_h + (n_h - 1) - e0;
+            const float gm = rr < Cp ? gam[pos] : 0.f;
+            o[rr] = fmaf(gm, __uint_as_float(r1[u]), __uint_as_float(r2[u]));
+          }
+        } else {
+          tmem_wait_ld_regs(r1);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[hf * 32 + u] = __uint_as_float(r1[u]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(sm.bar(B_OFREE));
+      // W^T of the next chunk before the stores: it gates the next chain step
+      if (n + 1 < NT) convert_w(n + 1);
+      // 8x8 transposes within groups of 8 lanes: lane k of a group then holds
+      // 8 consecutive value columns of row 8 rg + k -> one 16-byte store
       {
-        const int e0 = n * C;
-        const int t_lo = e0 / n_h;
-        int t_hi = (e0 + C - n_h) / n_h;
-        if (t_hi > p.T - 1) t_hi = p.T - 1;
-        const int Cp = t_hi - t_lo + 1;
-        __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm.base + OFF_STG);
+        const int k = lane & 7;
+        const size_t col = (size_t)q4 * 32 + (lane >> 3) * 8;
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(tmem_addr(tmem + TM_O, q4 * 32, c0), r);
-          tmem_wait_ld_regs(r);
+        for (int rg = 0; rg < 8; ++rg) {
+          float v[8];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) stg[(c0 + u) * D + L] = __float2bfloat16_rn(__uint_as_float(r[u]));
+          for (int j = 0; j < 8; ++j) v[j] = o[rg * 8 + j];
+#pragma unroll
+          for (int sh = 1; sh < 8; sh <<= 1) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (j & sh) continue;
+              const float send = (k & sh) ? v[j] : v[j | sh];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
+              if (k & sh)
+                v[j] = recv;
+              else
+                v[j | sh] = recv;
+            }
+          }
+          const int row = rg * 8 + k;
+          if (row < Cp) {
+            const uint4 pkt = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
+                                         pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+            *reinterpret_cast<uint4 *>(p.out + (((size_t)b * p.T + t_lo + row) * p.H + h) * D + col) = pkt;
+          }
         }
-        tc_fence_before();
-        mbar_arrive(sm.bar(B_OFREE));
-        // W^T of the next chunk before the copy-out: it gates the next chain step
-        if (n + 1 < NT) convert_w(n + 1);
-        if (named_sync_or(2, *sm.abort_flag() != 0)) break;
-        // rows of 256 bytes: 16 threads per row, 8 rows per pass
-        const int chunk16 = ct & 15;
-        uint4 *og = reinterpret_cast<uint4 *>(p.out);
-        const uint4 *sg = reinterpret_cast<const uint4 *>(stg);
-        for (int rr = ct >> 4; rr < Cp; rr += 8) {
-          const size_t row = ((size_t)b * p.T + t_lo + rr) * p.H + h;
-          og[row * (D / 8) + chunk16] = sg[rr * (D / 8) + chunk16];
-        }
-        named_sync(2);
       }
     }
   }
