@@ -12,37 +12,42 @@
 //   A    = strictLower(diag(beta) (Gam * K K^T)),  Gam_ij = exp(gc_i - gc_j)
 //   T    = (I + A)^{-1} diag(beta)
 //   W    = T (K * exp(gc)),  U = T V
-//   Vt   = U - W S                               (pseudo-values)
-//   O    = (Q * exp(gc)) S + (Q K^T * Gam * M) Vt   (token readout rows only)
-//   S   <- exp(gc_C) S + (K * exp(gc_C - gc))^T Vt
+//   O    = (Q * exp(gc)) S + P (U - W S),   P = Q K^T * Gam * M (M incl. diag)
+//   S   <- exp(gc_C) S + Kd^T (U - W S),    Kd = K * exp(gc_C - gc)
 //
-// Design (one CTA per (b, h) head, the 128x128 state on chip for the whole
-// sequence): everything is computed TRANSPOSED so that every tensor-core
-// product has M = 128 (the dk or dv axis) and the state S^T lives in TMEM as
-// an fp32 accumulator [dv lanes x dk columns]:
+// Everything that does not involve the state is folded into two per-chunk
+// matrices, so that the sequential state chain is ONE tensor-core product:
 //
-//   G     = [K; Q] K^T                 SS  M=128 N=64  K=128   (TMEM)
-//   U^T   = V^T T^T                    SS  M=128 N=64  K=64    (TMEM, becomes Vt^T)
-//   W^T   = K^T (T diag(exp gc))^T     SS  M=128 N=64  K=64    (TMEM -> smem bf16)
-//   Vt^T += S^T (-W^T)                 TS  M=128 N=64  K=128   (A = S^T bf16 in TMEM)
-//   S^T  += (Vt^T diag(exp(gc_C-gc))) K  TS M=128 N=128 K=64   (S^T pre-scaled by exp gc_C)
-//   O1^T  = S^T Q^T                    TS  M=128 N=64  K=128
-//   O2^T  = Vt^T P^T                   TS  M=128 N=64  K=64    (A = Vt^T bf16 in TMEM)
-//   out   = exp(gc) * O1 + O2          (epilogue; O2 accumulates into O1 when ungated)
+//   M - I = (exp(gc_C) - 1) I - Kd^T W          (dk x dk)
+//   Q'    = Q * exp(gc) - P W                    (readout rows x dk)
+//   S    <- S + (M - I) S + Kd^T U               (the chain)
+//   O     = Q' S + P U
 //
-// W and U never leave the SM.  HBM traffic is q, k, v, beta, g in and out,
-// h0/hT once per head.  The UT solve runs on the CUDA cores: 16x16 diagonal
-// blocks by forward substitution in registers (rows exchanged with warp
-// shuffles), then two block merges on the warp-level tensor cores (tf32).
+// This is an exact rewrite of the same chunk step (the state enters both
+// products once, as in U - W S).  All products are computed TRANSPOSED, so
+// that every tensor-core product has M = 128 (a d axis) and the state S^T
+// lives in TMEM as an fp32 accumulator [dv lanes x dk columns]:
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: K/Q/V tiles (128-byte swizzle, 3 stages, the
-//               next chunk prefetched into L2) + beta/log-gate rows
-//   warp 1      TMEM owner and the single MMA-issuing thread
-//   warps 2-5   "prep": G -> A, P -> UT solve -> T tiles     (S-independent)
-//   warps 6-9   "chain": Vt^T -> bf16 TMEM operands, S^T -> bf16 copy and
-//               gate decay, W^T -> smem operand, output epilogue, final state
-// The prep stage of chunk n+1 overlaps the state-dependent chain of chunk n.
+//   G     = [K; Q] K^T                  SS  N=64  K=128  (-> A, P)
+//   W^T   = K^T (T diag exp gc)^T       SS  N=64  K=64
+//   U^T   = V^T T^T                     SS  N=64  K=64
+//   (M-I)^T = -W^T Kd                   TS  N=128 K=64   (A = W^T bf16 in TMEM)
+//   Q'^T  = -W^T P^T (+ exp(gc) Q^T)    TS  N=64  K=64
+//   O^T   = U^T P^T + S^T Q'^T          TS  N=64  K=64 + K=128
+//   S^T  += S^T (M-I)^T + U^T Kd        TS  N=128 K=128 + K=64   (chain)
+//
+// W, U, T, M, Q' and P never leave the SM.  HBM traffic is q, k, v, beta, g
+// in and out, h0/hT once per head.
+//
+// Warp roles (448 threads, one CTA per (b, h) head):
+//   warp 0       TMA producer: K/Q/V tiles (128-byte swizzle, 3 stages, the
+//                chunk after them prefetched into L2) + beta / log-gate rows
+//   warp 1       TMEM owner and the single MMA-issuing thread
+//   warps 2-5    prep (chunk n+2): G -> A, P -> UT solve -> T tiles
+//   warps 6-9    feed-forward (chunk n+1): W^T, U^T -> bf16 TMEM operands,
+//                Kd, (M-I)^T -> smem operand
+//   warps 10-13  chain (chunk n): S^T -> bf16 operand, output epilogue, hT;
+//                then Q' of chunk n+1 -> smem operand
 // Every mbarrier wait is bounded; a timeout sets a device error word and the
 // kernel winds down instead of hanging.
 #include <cuda_bf16.h>
@@ -62,64 +67,68 @@ using namespace sm100;
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr int NS = 3;  // TMA stages
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLogGateFloor = -80.0f;
+// Down to this cumulative log2 gate within a chunk the decay factors are
+// formed as 2^gc_i * 2^-gc_j (no overflow); below it, exactly per entry.
+constexpr float kRatioFloor = -100.0f;
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ----
-constexpr uint32_t STAGE_BYTES = 49152;  // [K0 | Q0 | K1 | Q1] 32 KB + [V0 | V1] 16 KB
-constexpr uint32_t OFF_W = NS * STAGE_BYTES;     // W^T bf16 [128 d][64 c], MN-major
-constexpr uint32_t OFF_TU = OFF_W + 16384;       // T    bf16 [64][64], K-major
-constexpr uint32_t OFF_TW = OFF_TU + 8192;       // T diag(exp gc)
-constexpr uint32_t OFF_P = OFF_TW + 8192;        // 2 x P bf16 [64][64]
-constexpr uint32_t OFF_A = OFF_P + 16384;        // A^T fp32 [64][64] (entry (j, i) = A_ij)
-constexpr uint32_t OFF_X = OFF_A + 16384;        // X = (I + A)^{-1} fp32 [64][64]
-constexpr uint32_t SMEM_TOTAL = OFF_X + 16384;
-// A^T rows 32..63 only ever hold entries of columns 32..63 (A_ij with
-// i > j >= 32): the first 128 bytes of each of those rows are free and carry
-// the small per-chunk arrays and the barriers, one 128-byte slice per row.
-constexpr int SL_BETA = 0;    // [NS] arrays of 64 floats, 2 slices each
-constexpr int SL_LAM = SL_BETA + 2 * NS;
-constexpr int SL_GCP = SL_LAM + 2 * NS;
-constexpr int SL_DEC = SL_GCP + 2;   // [2]
-constexpr int SL_GAM = SL_DEC + 4;   // [2]
-constexpr int SL_BGC = SL_GAM + 4;
-constexpr int SL_BAR = SL_BGC + 2;   // 16 barriers per slice
-constexpr int NBARS = 2 * NS + 14;
-constexpr int SL_MISC = SL_BAR + (NBARS + 15) / 16;
-static_assert(SL_MISC < 32, "small region must fit in the free slices of A^T");
-constexpr uint32_t SMEM_ALLOC = SMEM_TOTAL + 1024;
-static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-
-// ---- TMEM columns ----
-constexpr uint32_t TM_S = 0;        // S^T fp32            [dv][dk]   128 cols
-constexpr uint32_t TM_SBF = 128;    // 2 x S^T bf16 (packed)         2x64 cols
-constexpr uint32_t TM_GW = 256;     // G, then W^T fp32                64 cols
-constexpr uint32_t TM_UV = 320;     // U^T -> Vt^T -> (gated) O2^T     64 cols
-constexpr uint32_t TM_O = 384;      // O1^T fp32                       64 cols
-constexpr uint32_t TM_VBF = 448;    // Vt^T bf16 (packed)              32 cols
-constexpr uint32_t TM_VDEC = 480;   // Vt^T diag(exp(gc_C - gc)) bf16  32 cols
-constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t STAGE_BYTES = 49152;
+constexpr uint32_t ST_K0 = 0, ST_Q0 = 8192, ST_K1 = 16384, ST_Q1 = 24576;
+constexpr uint32_t ST_V0 = 32768;  // V (64 x 128), later Kd, same layout
+constexpr uint32_t OFF_MS = NS * STAGE_BYTES;  // (M-I)^T bf16 [128 j][128 i], MN-major B
+constexpr uint32_t OFF_TU = OFF_MS + 32768;    // T bf16 [64][64], K-major
+constexpr uint32_t OFF_TW = OFF_TU + 8192;     // T diag(exp gc)
+constexpr uint32_t OFF_P = OFF_TW + 8192;      // 2 x P bf16 [64][64], K-major
+constexpr uint32_t OFF_AX = OFF_P + 16384;     // A (upper, transposed) / X (lower) fp32 [64][64]
+constexpr uint32_t OFF_SM = OFF_AX + 16384;    // small arrays and barriers
+constexpr uint32_t SM_BETA = 0;                // [NS][64]
+constexpr uint32_t SM_LAM = SM_BETA + NS * 256;  // [NS][64] log2 gate
+constexpr uint32_t SM_EG = SM_LAM + NS * 256;    // prep: 2^gc
+constexpr uint32_t SM_IEG = SM_EG + 256;         // prep: 2^-gc
+constexpr uint32_t SM_BGC = SM_IEG + 256;        // prep: beta 2^gc
+constexpr uint32_t SM_DEC = SM_BGC + 256;        // feed-forward: 2^(gc_C - gc)
+constexpr uint32_t SM_GQ = SM_DEC + 256;         // feed-forward: 2^gc at readout rows
+constexpr uint32_t SM_BAR = SM_GQ + 256;
 
 // ---- barrier indices ----
 enum {
-  B_FULL = 0,             // [NS] producer -> consumers (count 2 + tx)
-  B_EMPTY = NS,           // [NS] MMA commit -> producer
-  B_GFULL = 2 * NS,       // MMA -> prep: G ready in TMEM
-  B_TFULL,                // prep -> MMA: T, P in smem (128)
-  B_WFULL,                // MMA -> chain, prep: U, W^T ready (T tiles consumed)
-  B_WREADY,               // chain -> MMA: W in smem, TMEM GW free (128)
-  B_WFREE,                // MMA -> chain: W smem consumed
-  B_SREADY,               // chain -> MMA: S^T bf16 ready, S^T decayed (128)
-  B_VTFULL,               // MMA -> chain: Vt^T ready
-  B_VTREADY,              // chain -> MMA: Vt^T bf16 operands ready (128)
-  B_SFULL,                // MMA -> chain: S^T updated
-  B_OFULL,                // MMA -> chain: O1 (and O2) complete
-  B_OFREE,                // chain -> MMA: O1 / O2 read (128)
-  B_PQFREE0,              // MMA -> prep: P buffer 0 free
-  B_PQFREE1,              //                          1
-  B_DRAIN,                // MMA: everything issued has completed
+  B_FULL = 0,        // [NS] producer -> all: stage loaded (count 2 + tx)
+  B_EMPTY = NS,      // [NS] MMA -> producer: stage consumed
+  B_GFULL = 2 * NS,  // MMA -> prep: G in TMEM
+  B_GFREE,           // prep -> MMA: G read (one arrival per warp)
+  B_TFULL,           // prep -> MMA: T tiles and P written (per warp)
+  B_WFULL,           // MMA -> ff, prep: W^T, U^T in TMEM (T tiles consumed)
+  B_CWD,             // ff -> MMA: W^T, U^T bf16 in TMEM, Kd in smem (per warp)
+  B_MFULL,           // MMA -> ff: (M-I)^T in TMEM
+  B_MRDY,            // ff -> MMA: (M-I)^T in smem, TMEM free (per warp)
+  B_QFULL,           // MMA -> ff: -W^T P^T in TMEM
+  B_QRDY,            // ff -> MMA: Q' in smem, TMEM free (per warp)
+  B_SRDY,            // chain -> MMA: S^T bf16 in TMEM (per warp)
+  B_SFULL,           // MMA -> chain, ff: state step done
+  B_OFULL,           // MMA -> chain: O^T in TMEM
+  B_OFREE,           // chain -> MMA: O^T read (per warp)
+  B_PFREE0,          // MMA -> prep: P buffer 0 consumed
+  B_PFREE1,          //                        1
+  B_DRAIN,           // MMA: everything issued has completed
+  NBARS
 };
+constexpr uint32_t SM_MISC = SM_BAR + NBARS * 8;  // tmem slot, abort flag, gate of the chunk
+constexpr uint32_t SMEM_TOTAL = OFF_SM + SM_MISC + 16;
+constexpr uint32_t SMEM_ALLOC = 232448;
+static_assert(SMEM_TOTAL <= SMEM_ALLOC, "shared memory budget");
+
+// ---- TMEM columns ----
+constexpr uint32_t TM_S = 0;      // S^T fp32 [dv][dk]                128
+constexpr uint32_t TM_SBF = 128;  // S^T bf16 (packed)                 64
+constexpr uint32_t TM_O = 192;    // -W^T P^T, then O^T fp32           64
+constexpr uint32_t TM_X1 = 256;   // W^T | U^T fp32, then (M-I)^T     128
+constexpr uint32_t TM_G = 384;    // G fp32                            64
+constexpr uint32_t TM_WB = 448;   // W^T bf16 (packed)                 32
+constexpr uint32_t TM_UB = 480;   // U^T bf16 (packed)                 32
+constexpr uint32_t TM_COLS = 512;
 
 struct TcParams {
   const float *beta, *g, *h0;
@@ -128,36 +137,29 @@ struct TcParams {
   int H, T, L, n_h, nchunks;
 };
 
-// 64 floats split over two 128-byte slices.
-struct Arr64 {
-  uint8_t *p0, *p1;
-  __device__ float &operator[](int e) const {
-    return reinterpret_cast<float *>(e < 32 ? p0 : p1)[e & 31];
-  }
-};
-
 struct Smem {
   uint8_t *base;
   __device__ uint8_t *stage(int s) const { return base + s * STAGE_BYTES; }
-  __device__ uint8_t *slice(int k) const { return base + OFF_A + (32 + k) * 256; }
-  __device__ Arr64 arr(int k) const { return Arr64{slice(k), slice(k + 1)}; }
-  __device__ Arr64 beta(int s) const { return arr(SL_BETA + 2 * s); }
-  __device__ Arr64 lam(int s) const { return arr(SL_LAM + 2 * s); }
-  __device__ Arr64 gcp() const { return arr(SL_GCP); }
-  __device__ Arr64 dec(int b) const { return arr(SL_DEC + 2 * b); }
-  __device__ Arr64 gam(int b) const { return arr(SL_GAM + 2 * b); }
-  __device__ Arr64 bgc() const { return arr(SL_BGC); }
+  __device__ float *arr(uint32_t off) const { return reinterpret_cast<float *>(base + OFF_SM + off); }
+  __device__ float *beta(int s) const { return arr(SM_BETA + s * 256); }
+  __device__ float *lam(int s) const { return arr(SM_LAM + s * 256); }
   __device__ uint64_t *bar(int i) const {
-    return reinterpret_cast<uint64_t *>(slice(SL_BAR + (i >> 4))) + (i & 15);
+    return reinterpret_cast<uint64_t *>(base + OFF_SM + SM_BAR) + i;
   }
-  __device__ uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(slice(SL_MISC)); }
-  __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(slice(SL_MISC) + 4); }
-  __device__ float *At() const { return reinterpret_cast<float *>(base + OFF_A); }
-  __device__ float *X() const { return reinterpret_cast<float *>(base + OFF_X); }
+  __device__ uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(base + OFF_SM + SM_MISC); }
+  __device__ volatile int *abort_flag() const {
+    return reinterpret_cast<volatile int *>(base + OFF_SM + SM_MISC + 4);
+  }
+  __device__ float *gate_c() const { return reinterpret_cast<float *>(base + OFF_SM + SM_MISC + 8); }
+  __device__ float *AX() const { return reinterpret_cast<float *>(base + OFF_AX); }
 };
 
 // Bounded wait that also gives up at once when another role has aborted.
-__device__ __forceinline__ bool wait_bar(const Smem &sm, int idx, uint32_t parity, int role) {
+// The first poll is inline; the loop stays out of line (it is called from
+// many places) and takes only scalars, so nothing goes through local memory.
+__device__ __noinline__ bool wait_bar_slow(uint8_t *base, int idx, uint32_t parity, int role) {
+  Smem sm;
+  sm.base = base;
   uint64_t *b = sm.bar(idx);
   for (uint32_t i = 0; i < (1u << 22); ++i) {
     if (mbar_try_wait(b, parity)) return true;
@@ -167,12 +169,25 @@ __device__ __forceinline__ bool wait_bar(const Smem &sm, int idx, uint32_t parit
   atomicCAS(&g_tc_error, 0u, (unsigned)(1 + role) | ((unsigned)idx << 8));
   return false;
 }
+__device__ __forceinline__ bool wait_bar(const Smem &sm, int idx, uint32_t parity, int role) {
+  if (mbar_try_wait(sm.bar(idx), parity)) return true;
+  return wait_bar_slow(sm.base, idx, parity, role);
+}
 
 // fp32 64x64 matrices in shared memory are stored row-major with the column
 // XOR-swizzled by the row (bits 2..4), which keeps float4 runs along a row
 // contiguous and makes the tf32 MMA fragment loads below conflict-free.
 __device__ __forceinline__ int swz(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
 
+// The solve's 64x64 array holds A_ij (i > j) at (j, i) -- the upper triangle --
+// and X_ij = ((I + A)^{-1})_ij (i > j) at (i, j) -- the lower triangle.  The
+// diagonal holds the chunk's cumulative log gate (X_ii = 1 is implicit).
+__device__ __forceinline__ float ldA(const float *AX, int i, int j) { return AX[swz(j, i)]; }
+// X_rc of a block that touches the diagonal: 1 on it, 0 above it.
+__device__ __forceinline__ float ldXm(const float *M, int r, int c) {
+  const float v = M[swz(r, c)];
+  return r > c ? v : (r == c ? 1.f : 0.f);
+}
 
 // D(16x8) += A(16x8) B(8x8) on the warp-level tensor-core path, tf32 inputs
 // (fp32 bit patterns; the MMA ignores the low mantissa bits).
@@ -188,52 +203,59 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// One warp: D(16x8) (+)= M1[r0.., k0..k0+K) * M2[k2.., n0..n0+8) (and a second
-// tile at n0 + 8 when TWO) with both operands read from swizzled fp32 smem;
-// M1 is read through its transpose when `m1t` (A^T holds A).  The fp32 bits
-// are fed to the tf32 MMA as they are (the low mantissa bits are ignored).
-template <int K, bool TWO>
-__device__ __forceinline__ void warp_gemm(float (&d0)[4], float (&d1)[4], const float *M1, bool m1t,
-                                          int r0, int k0, const float *M2, int k2, int n0, int lane) {
+// Operand fragments of the tf32 MMA read from the solve array.  KIND 0: a
+// block of A (stored transposed in the upper triangle); KIND 1: a block of X
+// that may touch the diagonal (1 on it, 0 above it).
+template <int KIND>
+__device__ __forceinline__ uint32_t lsol(const float *AX, int r, int c) {
+  return __float_as_uint(KIND == 0 ? ldA(AX, r, c) : ldXm(AX, r, c));
+}
+template <int KIND>
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float *AX, int r0, int k0, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  uint32_t a[K / 8][4], b0[K / 8][2], b1[K / 8][2];
-#pragma unroll
-  for (int ks = 0; ks < K / 8; ++ks) {
-    const int c = k0 + 8 * ks;
-    if (m1t) {
-      a[ks][0] = __float_as_uint(M1[swz(c + t, r0 + g)]);
-      a[ks][1] = __float_as_uint(M1[swz(c + t, r0 + g + 8)]);
-      a[ks][2] = __float_as_uint(M1[swz(c + t + 4, r0 + g)]);
-      a[ks][3] = __float_as_uint(M1[swz(c + t + 4, r0 + g + 8)]);
-    } else {
-      a[ks][0] = __float_as_uint(M1[swz(r0 + g, c + t)]);
-      a[ks][1] = __float_as_uint(M1[swz(r0 + g + 8, c + t)]);
-      a[ks][2] = __float_as_uint(M1[swz(r0 + g, c + t + 4)]);
-      a[ks][3] = __float_as_uint(M1[swz(r0 + g + 8, c + t + 4)]);
-    }
-    const int kr = k2 + 8 * ks;
-    b0[ks][0] = __float_as_uint(M2[swz(kr + t, n0 + g)]);
-    b0[ks][1] = __float_as_uint(M2[swz(kr + t + 4, n0 + g)]);
-    if (TWO) {
-      b1[ks][0] = __float_as_uint(M2[swz(kr + t, n0 + 8 + g)]);
-      b1[ks][1] = __float_as_uint(M2[swz(kr + t + 4, n0 + 8 + g)]);
-    }
-  }
-#pragma unroll
-  for (int ks = 0; ks < K / 8; ++ks) {
-    mma_tf32(d0, a[ks], b0[ks]);
-    if (TWO) mma_tf32(d1, a[ks], b1[ks]);
-  }
+  a[0] = lsol<KIND>(AX, r0 + g, k0 + t);
+  a[1] = lsol<KIND>(AX, r0 + g + 8, k0 + t);
+  a[2] = lsol<KIND>(AX, r0 + g, k0 + t + 4);
+  a[3] = lsol<KIND>(AX, r0 + g + 8, k0 + t + 4);
+}
+template <int KIND>
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float *AX, int k0, int n0, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  b[0] = lsol<KIND>(AX, k0 + t, n0 + g);
+  b[1] = lsol<KIND>(AX, k0 + t + 4, n0 + g);
+}
+// B fragment for k-step ks (rows 8 ks .. 8 ks + 7) of a matrix Y held as MMA
+// results: y[h] is the 16x8 accumulator of rows 16 h .. 16 h + 15.  Row r,
+// column c of a 16x8 accumulator lives in lane (r % 8) * 4 + c / 2, element
+// (r / 8) * 2 + c % 2: two candidates are shuffled in and one is kept.
+template <int NH>
+__device__ __forceinline__ void frag_b_acc(uint32_t (&b)[2], const float (&y)[NH][4], int ks,
+                                           int lane) {
+  const int g = lane >> 2, t = lane & 3, h = ks >> 1, e = (ks & 1) * 2;
+  const int s0 = t * 4 + (g >> 1), s1 = (t + 4) * 4 + (g >> 1);
+  const float a0 = __shfl_sync(0xffffffffu, y[h][e], s0);
+  const float a1 = __shfl_sync(0xffffffffu, y[h][e + 1], s0);
+  const float c0 = __shfl_sync(0xffffffffu, y[h][e], s1);
+  const float c1 = __shfl_sync(0xffffffffu, y[h][e + 1], s1);
+  b[0] = __float_as_uint((g & 1) ? a1 : a0);
+  b[1] = __float_as_uint((g & 1) ? c1 : c0);
 }
 
-// T_U = x * beta_j and T_W = x * beta_j exp(gc_j) of a 16x8 fragment of
-// (scale * D) at rows r0.., columns n0.. of the bf16 T tiles.
+// T_U[r][c] = x beta_c and T_W[r][c] = x beta_c exp(gc_c) (bf16 tiles).
+__device__ __forceinline__ void put_t(uint8_t *tu, uint8_t *tw, int r, int c, float x, float bc,
+                                      float wc) {
+  const uint32_t off = sw128_offset(r, c, 64);
+  *reinterpret_cast<__nv_bfloat16 *>(tu + off) = __float2bfloat16_rn(x * bc);
+  *reinterpret_cast<__nv_bfloat16 *>(tw + off) = __float2bfloat16_rn(x * wc);
+}
+
+// T tiles from a 16x8 fragment of (scale * D) at rows r0.., columns n0...
 __device__ __forceinline__ void frag_to_t(uint8_t *tu, uint8_t *tw, int r0, int n0,
-                                          const float (&d)[4], float scale, const Arr64 &bcol,
-                                          const Arr64 &bgcol, int lane) {
+                                          const float (&d)[4], float scale, const float *beta,
+                                          const float *bgc, int lane) {
   const int g = lane >> 2, t = lane & 3;
   const int c = n0 + 2 * t;
-  const float b0 = bcol[c], b1 = bcol[c + 1], w0 = bgcol[c], w1 = bgcol[c + 1];
+  const float b0 = beta[c], b1 = beta[c + 1], w0 = bgc[c], w1 = bgc[c + 1];
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const float x0 = d[2 * hh] * scale, x1 = d[2 * hh + 1] * scale;
@@ -251,6 +273,142 @@ __device__ __forceinline__ void warp_store_16x8(float *M, int r0, int n0, const 
   M[swz(r0 + g, n0 + 2 * t + 1)] = d[1] * scale;
   M[swz(r0 + g + 8, n0 + 2 * t)] = d[2] * scale;
   M[swz(r0 + g + 8, n0 + 2 * t + 1)] = d[3] * scale;
+}
+
+// One warp inverts the unit lower-triangular 16x16 diagonal block at offset
+// o of (I + A): closed-form 4x4 leaves, then the merges 4 -> 8 -> 16, each
+// X21 = -X22 (A21 X11).  Every entry of A the warp needs is loaded at once;
+// the partial inverses move between lanes by shuffles, not through shared
+// memory.  X goes to the lower triangle of the solve array and, scaled, to
+// the T tiles.
+__device__ __forceinline__ void invert_diag16(float *AX, uint8_t *tu, uint8_t *tw,
+                                              const float *beta, const float *bgc, int o,
+                                              int lane) {
+  const unsigned full = 0xffffffffu;
+  // leaf lanes (0..11): leaf a, column cc;  merge-1 lanes: (hh, r4, c4);
+  // merge-2 lanes: (r8, c0 and c0 + 4)
+  const int a = lane < 12 ? lane / 3 : 0, cc = lane < 12 ? lane - 3 * (lane / 3) : 0;
+  const int b0 = o + 4 * a;
+  const int hh = lane >> 4, r4 = (lane >> 2) & 3, c4 = lane & 3, o8 = o + 8 * hh;
+  const int r8 = lane >> 2, c0 = lane & 3;
+  const float a10 = ldA(AX, b0 + 1, b0), a20 = ldA(AX, b0 + 2, b0), a21 = ldA(AX, b0 + 2, b0 + 1);
+  const float a30 = ldA(AX, b0 + 3, b0), a31 = ldA(AX, b0 + 3, b0 + 1), a32 = ldA(AX, b0 + 3, b0 + 2);
+  float am1[4], am2[8];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) am1[m] = ldA(AX, o8 + 4 + r4, o8 + m);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) am2[m] = ldA(AX, o + 8 + r8, o + m);
+
+  // ---- leaves: column cc of leaf a by forward substitution ----
+  const float x0 = cc == 0 ? 1.f : 0.f;
+  const float x1 = cc == 1 ? 1.f : (cc < 1 ? -(a10 * x0) : 0.f);
+  const float x2 = cc == 2 ? 1.f : (cc < 2 ? -fmaf(a21, x1, a20 * x0) : 0.f);
+  const float x3 = -fmaf(a32, x2, fmaf(a31, x1, a30 * x0));
+  if (lane < 12) {
+    const int col = b0 + cc;
+    const float bc = beta[col], wc = bgc[col];
+    if (cc < 1) {
+      AX[swz(b0 + 1, col)] = x1;
+      put_t(tu, tw, b0 + 1, col, x1, bc, wc);
+    }
+    if (cc < 2) {
+      AX[swz(b0 + 2, col)] = x2;
+      put_t(tu, tw, b0 + 2, col, x2, bc, wc);
+    }
+    AX[swz(b0 + 3, col)] = x3;
+    put_t(tu, tw, b0 + 3, col, x3, bc, wc);
+  }
+  if (lane < 16) put_t(tu, tw, o + lane, o + lane, 1.f, beta[o + lane], bgc[o + lane]);
+
+  // ---- 4 -> 8: X[o8+4+r4][o8+c4] ----
+  float xm1;
+  {
+    // X11 = leaf 2 hh, column c4 (lane 6 hh + c4); X11[m][c4] for m > c4
+    const int s11 = 6 * hh + c4;
+    const float u1 = __shfl_sync(full, x1, s11), u2 = __shfl_sync(full, x2, s11),
+                u3 = __shfl_sync(full, x3, s11);
+    const float xc[4] = {c4 == 0 ? 1.f : 0.f, c4 == 1 ? 1.f : (c4 < 1 ? u1 : 0.f),
+                         c4 == 2 ? 1.f : (c4 < 2 ? u2 : 0.f), c4 == 3 ? 1.f : u3};
+    float y = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) y = fmaf(am1[m], xc[m], y);
+    // Y[m][c4] from lane (hh, m, c4); X22[r4][m] = leaf 2 hh + 1, column m, row r4
+    float z = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float ym = __shfl_sync(full, y, (lane & 16) | (m << 2) | c4);
+      float xr = 1.f;
+      if (m < 3) {
+        const int s22 = 6 * hh + 3 + m;
+        const float w1 = __shfl_sync(full, x1, s22), w2 = __shfl_sync(full, x2, s22),
+                    w3 = __shfl_sync(full, x3, s22);
+        xr = r4 == 1 ? w1 : (r4 == 2 ? w2 : w3);
+      }
+      if (m < r4) z = fmaf(xr, ym, z);
+      if (m == r4) z += ym;
+    }
+    xm1 = -z;
+    AX[swz(o8 + 4 + r4, o8 + c4)] = xm1;
+    put_t(tu, tw, o8 + 4 + r4, o8 + c4, xm1, beta[o8 + c4], bgc[o8 + c4]);
+  }
+
+  // ---- 8 -> 16: X[o+8+r8][o+c0] and X[o+8+r8][o+c0+4] ----
+  {
+    // column c0 of X11 = X[o..o+8][o..o+8]: rows < 4 from leaf 0 (lane c0),
+    // rows >= 4 from the 4 -> 8 merge (lane (0, m-4, c0))
+    const float u1 = __shfl_sync(full, x1, c0), u2 = __shfl_sync(full, x2, c0),
+                u3 = __shfl_sync(full, x3, c0);
+    // column c0 + 4: rows >= 4 from leaf 1 (lane 3 + c0)
+    const float v1 = __shfl_sync(full, x1, 3 + c0), v2 = __shfl_sync(full, x2, 3 + c0),
+                v3 = __shfl_sync(full, x3, 3 + c0);
+    float y0 = 0.f, y1 = 0.f;
+    const float lo[4] = {c0 == 0 ? 1.f : 0.f, c0 == 1 ? 1.f : (c0 < 1 ? u1 : 0.f),
+                         c0 == 2 ? 1.f : (c0 < 2 ? u2 : 0.f), c0 == 3 ? 1.f : u3};
+    const float hi[4] = {c0 == 0 ? 1.f : 0.f, c0 == 1 ? 1.f : (c0 < 1 ? v1 : 0.f),
+                         c0 == 2 ? 1.f : (c0 < 2 ? v2 : 0.f), c0 == 3 ? 1.f : v3};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      y0 = fmaf(am2[m], lo[m], y0);
+      const float wm = __shfl_sync(full, xm1, (m << 2) | c0);
+      y0 = fmaf(am2[m + 4], wm, y0);
+      y1 = fmaf(am2[m + 4], hi[m], y1);
+    }
+    // X22 = X[o+8..o+16][o+8..o+16]: rows < 4 from leaf 2, rows >= 4 from
+    // leaf 3 (same columns) or, for columns < 4, from the 4 -> 8 merge (hh 1)
+    float z0 = 0.f, z1 = 0.f;
+    const int rr = r8 & 3;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float ya = __shfl_sync(full, y0, (m << 2) | c0);
+      const float yb = __shfl_sync(full, y1, (m << 2) | c0);
+      float xr;
+      if ((m & 3) < 3) {
+        // leaf 2 (r8 < 4) or leaf 3 (r8 >= 4), column m & 3, row r8 & 3
+        const int sl = (r8 < 4 ? 6 : 9) + (m & 3);
+        const float w1 = __shfl_sync(full, x1, sl), w2 = __shfl_sync(full, x2, sl),
+                    w3 = __shfl_sync(full, x3, sl);
+        xr = rr == 1 ? w1 : (rr == 2 ? w2 : w3);
+      } else {
+        xr = 0.f;
+      }
+      if (m < 4) {
+        const float xq = __shfl_sync(full, xm1, 16 | ((r8 & 3) << 2) | m);
+        if (r8 >= 4) xr = xq;
+      }
+      if (m < r8) {
+        z0 = fmaf(xr, ya, z0);
+        z1 = fmaf(xr, yb, z1);
+      }
+      if (m == r8) {
+        z0 += ya;
+        z1 += yb;
+      }
+    }
+    AX[swz(o + 8 + r8, o + c0)] = -z0;
+    AX[swz(o + 8 + r8, o + c0 + 4)] = -z1;
+    put_t(tu, tw, o + 8 + r8, o + c0, -z0, beta[o + c0], bgc[o + c0]);
+    put_t(tu, tw, o + 8 + r8, o + c0 + 4, -z1, beta[o + c0 + 4], bgc[o + c0 + 4]);
+  }
 }
 
 // 2^x on the MUFU unit (relative error ~2^-22; flushes to 0 far below 1)
@@ -280,9 +438,16 @@ __device__ __forceinline__ bool named_sync_or(int id, bool cond) {
   return r != 0;
 }
 
+// One arrival per warp once every lane's prior work (fenced by the caller) is
+// done: the warp converges, then lane 0 arrives.
+__device__ __forceinline__ void arrive_warp(uint64_t *bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 // Inclusive prefix sum over the 64 log-gate entries of a chunk, per warp:
 // lane holds entries lane and lane + 32.
-__device__ __forceinline__ void warp_scan64(const Arr64 &lam, int lane, float &lo, float &hi) {
+__device__ __forceinline__ void warp_scan64(const float *lam, int lane, float &lo, float &hi) {
   lo = lam[lane];
   hi = lam[lane + 32];
 #pragma unroll
@@ -297,20 +462,41 @@ __device__ __forceinline__ void warp_scan64(const Arr64 &lam, int lane, float &l
   hi += __shfl_sync(0xffffffffu, lo, 31);
 }
 
-// 16-byte store of 8 packed bf16 values into a swizzled tile row.
-__device__ __forceinline__ void st_chunk(uint8_t *tile, uint32_t off, const uint32_t (&p)[4]) {
-  *reinterpret_cast<uint4 *>(tile + off) = make_uint4(p[0], p[1], p[2], p[3]);
+__device__ __forceinline__ void st_chunk(uint8_t *p, const uint32_t (&v)[4]) {
+  *reinterpret_cast<uint4 *>(p) = make_uint4(v[0], v[1], v[2], v[3]);
 }
 
+// readout rows of chunk n: tokens t_lo .. t_lo + Cp - 1 (their last sub-step
+// falls in the chunk); row r reads out after extended step pos(r)
+struct Rows {
+  int e0, t_lo, Cp;
+  __device__ Rows(int n, int n_h, int T) {
+    e0 = n * C;
+    t_lo = e0 / n_h;
+    int t_hi = (e0 + C - n_h) / n_h;
+    if (t_hi > T - 1) t_hi = T - 1;
+    Cp = t_hi - t_lo + 1;
+  }
+  __device__ int pos(int r, int n_h) const { return (t_lo + r) * n_h + (n_h - 1) - e0; }
+};
+
+// 14 warps: at most 4 per SM sub-partition, so 128 registers per thread
 template <bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem sm;
-  sm.base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                        ~static_cast<uintptr_t>(1023));
+  // pointer arithmetic on the shared array (not integer casts) keeps every
+  // access below in the shared state space
+  sm.base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __builtin_assume(__isShared(sm.base));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the layout needs SMEM_TOTAL bytes after the 1024-byte alignment
+  if ((uint32_t)(sm.base - smem_raw) + SMEM_TOTAL > SMEM_ALLOC) {
+    if (tid == 0) atomicCAS(&g_tc_error, 0u, 0xFFu);
+    return;
+  }
   const int bh = blockIdx.x;
   const int b = bh / p.H, h = bh % p.H;
   const int n_h = p.n_h, NT = p.nchunks;
@@ -327,20 +513,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(sm.bar(B_FULL + s), 2);
       mbar_init(sm.bar(B_EMPTY + s), 1);
     }
-    mbar_init(sm.bar(B_GFULL), 1);
-    mbar_init(sm.bar(B_TFULL), 128);
-    mbar_init(sm.bar(B_WFULL), 1);
-    mbar_init(sm.bar(B_WREADY), 128);
-    mbar_init(sm.bar(B_WFREE), 1);
-    mbar_init(sm.bar(B_SREADY), 128);
-    mbar_init(sm.bar(B_VTFULL), 1);
-    mbar_init(sm.bar(B_VTREADY), 128);
-    mbar_init(sm.bar(B_SFULL), 1);
-    mbar_init(sm.bar(B_OFULL), 1);
-    mbar_init(sm.bar(B_OFREE), 128);
-    mbar_init(sm.bar(B_PQFREE0), 1);
-    mbar_init(sm.bar(B_PQFREE1), 1);
-    mbar_init(sm.bar(B_DRAIN), 1);
+    const int cnt[NBARS - 2 * NS] = {1, 4, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, 1};
+    for (int i = 2 * NS; i < NBARS; ++i) mbar_init(sm.bar(i), cnt[i - 2 * NS]);
     *sm.abort_flag() = 0;
     fence_mbar_init();
   }
@@ -361,6 +535,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 
   if (warp == 0) {
     // ===================================================== TMA producer
+    // beta and the log gate of a chunk are read from global memory one chunk
+    // ahead (registers), so that a stage is complete as soon as its tiles land
+    float nb[2], nl[2];
+    auto fetch = [&](int n) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int e = n * C + lane + 32 * k;
+        float bt = 0.f, lg = 0.f;
+        if (n < NT && e < p.L) {
+          bt = p.beta[((size_t)b * p.L + e) * p.H + h];
+          if (GATED && (e % n_h) == 0)
+            lg = fmaxf(logf(p.g[((size_t)b * p.T + e / n_h) * p.H + h]), kLogGateFloor) * kLog2e;
+        }
+        nb[k] = bt;
+        nl[k] = lg;
+      }
+    };
+    fetch(0);
+    int issued = 0;
     for (int n = 0; n < NT; ++n) {
       const int s = n % NS;
       int ok = 1;
@@ -382,130 +575,147 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         mbar_arrive_expect_tx(sm.bar(B_FULL + s), 2u * (8192u + 8192u + (uint32_t)QR * 128u));
         uint64_t *fb = sm.bar(B_FULL + s);
-        tma_load_4d(st + 0, &map_k, fb, 0, h, e0, b);
-        tma_load_4d(st + 16384, &map_k, fb, 64, h, e0, b);
-        tma_load_4d(st + 8192, &map_q, fb, 0, h, t_lo, b);
-        tma_load_4d(st + 24576, &map_q, fb, 64, h, t_lo, b);
-        tma_load_4d(st + 32768, &map_v, fb, 0, h, e0, b);
-        tma_load_4d(st + 40960, &map_v, fb, 64, h, e0, b);
+        tma_load_4d(st + ST_K0, &map_k, fb, 0, h, e0, b);
+        tma_load_4d(st + ST_K1, &map_k, fb, 64, h, e0, b);
+        tma_load_4d(st + ST_Q0, &map_q, fb, 0, h, t_lo, b);
+        tma_load_4d(st + ST_Q1, &map_q, fb, 64, h, t_lo, b);
+        tma_load_4d(st + ST_V0, &map_v, fb, 0, h, e0, b);
+        tma_load_4d(st + ST_V0 + 8192, &map_v, fb, 64, h, e0, b);
       }
-      const Arr64 sb = sm.beta(s), sl = sm.lam(s);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int r = lane + 32 * k;
-        const int e = e0 + r;
-        float bt = 0.f, lg = 0.f;
-        if (e < p.L) {
-          bt = p.beta[((size_t)b * p.L + e) * p.H + h];
-          if (GATED && (e % n_h) == 0)
-            lg = fmaxf(logf(p.g[((size_t)b * p.T + e / n_h) * p.H + h]), kLogGateFloor) * kLog2e;
-        }
-        sb[r] = bt;
-        sl[r] = lg;
-      }
+      issued = n + 1;
+      float *sb = sm.beta(s), *sl = sm.lam(s);
+      sb[lane] = nb[0];
+      sb[lane + 32] = nb[1];
+      sl[lane] = nl[0];
+      sl[lane + 32] = nl[1];
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(B_FULL + s));
+      fetch(n + 1);
     }
+    // copies still in flight must land before the CTA's shared memory goes
+    if (lane == 0)
+      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n)
+        wait_bar(sm, B_FULL + n % NS, (n / NS) & 1, 0);
+    __syncwarp();
   } else if (warp == 1) {
     // ===================================================== MMA issuer
     if (lane == 0) {
-      bool ok = true;
-      const uint32_t id_g = idesc_bf16(128, 64, false, false);
-      const uint32_t id_uw = idesc_bf16(128, 64, true, false);
-      const uint32_t id_vt = idesc_bf16(128, 64, false, true, true);  // B = W^T MN-major, negated
-      const uint32_t id_o = idesc_bf16(128, 64, false, false);
-      const uint32_t id_s = idesc_bf16(128, 128, false, true);
+      constexpr uint32_t id_uw = idesc_bf16(128, 64, true, false);
+      constexpr uint32_t id_m = idesc_bf16(128, 128, false, true, true);  // B = Kd, MN-major, negated
+      constexpr uint32_t id_q = idesc_bf16(128, 64, false, false, true);  // B = P, negated
+      constexpr uint32_t id_op = idesc_bf16(128, 64, false, false);       // B = P
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);        // B = (M-I)^T or Kd, MN-major
+      constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);        // B = Q' (K-major)
       const uint32_t a_tu = smem_u32(sm.base + OFF_TU), a_tw = smem_u32(sm.base + OFF_TW);
-      const uint32_t a_w = smem_u32(sm.base + OFF_W);
-
-      auto issue_g = [&](int m) -> bool {  // G(m) = [K;Q] K^T
-        const int s = m % NS;
-        if (!wait_bar(sm, B_FULL + s, (m / NS) & 1, 1)) return false;
-        tc_fence_after();
-        const uint32_t kq = smem_u32(sm.stage(s));
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tmem + TM_GW, sdesc_sw128(kq + off, 0, 1024), sdesc_sw128(kq + off, 0, 1024),
-                 id_g, k > 0);
-        }
-        mma_commit(sm.bar(B_GFULL));
-        return true;
-      };
-      auto issue_w = [&](int m) {  // W(m)^T = K^T (T diag(exp gc))^T
+      const uint32_t a_ms = smem_u32(sm.base + OFF_MS), a_p = smem_u32(sm.base + OFF_P);
+      auto rdy = [&](int idx, int k) -> bool { return mbar_test_wait(sm.bar(idx), k & 1); };
+      auto kd_desc = [&](int m, int k) -> uint64_t {  // B = Kd (gated: V slot) or K
         const uint32_t kq = smem_u32(sm.stage(m % NS));
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + TM_GW, sdesc_sw128(kq + k * 2048, 16384, 1024),
-                 sdesc_sw128(a_tw + k * 32, 0, 1024), id_uw, k > 0);
+        return GATED ? sdesc_sw128(kq + ST_V0 + k * 2048, 8192, 1024)
+                     : sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024);
       };
-      auto issue_u = [&](int m) {  // U(m)^T = V^T T^T
-        const uint32_t vv = smem_u32(sm.stage(m % NS)) + 32768;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + TM_UV, sdesc_sw128(vv + k * 2048, 8192, 1024),
-                 sdesc_sw128(a_tu + k * 32, 0, 1024), id_uw, k > 0);
-      };
-
-      ok = issue_g(0) && wait_bar(sm, B_TFULL, 0, 1);
-      if (ok) {
-        tc_fence_after();
-        issue_w(0);
-        issue_u(0);
-        mma_commit(sm.bar(B_WFULL));
-      }
-      for (int n = 0; ok && n < NT; ++n) {
-        const int s = n % NS;
-        const uint32_t kq = smem_u32(sm.stage(s));
-        const uint32_t sbf = tmem + TM_SBF + (n & 1) * 64;
-        if (!wait_bar(sm, B_WREADY, n & 1, 1)) break;
-        // G of the next chunk as soon as W^T(n) has left TMEM: its solve
-        // overlaps this chunk's state-dependent chain
-        if (n + 1 < NT && !issue_g(n + 1)) break;
-        if (!wait_bar(sm, B_SREADY, n & 1, 1)) break;
-        tc_fence_after();
-        // Vt^T = U^T - S^T W^T                                (critical chain)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + TM_UV, sbf + k * 8, sdesc_sw128(a_w + k * 2048, 8192, 1024), id_vt, true);
-        mma_commit(sm.bar(B_VTFULL));
-        mma_commit(sm.bar(B_WFREE));
-        if (!wait_bar(sm, B_VTREADY, n & 1, 1)) break;
-        tc_fence_after();
-        // S^T += Vt^T diag(dec) K                             (critical chain)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + TM_S, tmem + (GATED ? TM_VDEC : TM_VBF) + k * 8,
-                 sdesc_sw128(kq + k * 2048, 16384, 1024), id_s, true);
-        mma_commit(sm.bar(B_SFULL));
-        // O1^T = S^T Q^T ; O2^T = Vt^T P^T (into the same accumulator when ungated)
-        if (n >= 1 && !wait_bar(sm, B_OFREE, (n - 1) & 1, 1)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + TM_O, sbf + k * 8,
-                 sdesc_sw128(kq + 8192 + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024), id_o, k > 0);
-        const uint32_t pb = smem_u32(sm.base + OFF_P) + (n & 1) * 8192;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + (GATED ? TM_UV : TM_O), tmem + TM_VBF + k * 8,
-                 sdesc_sw128(pb + k * 32, 0, 1024), id_o, GATED ? (k > 0) : true);
-        mma_commit(sm.bar(B_OFULL));
-        mma_commit(sm.bar(B_EMPTY + s));
-        mma_commit(sm.bar(B_PQFREE0 + (n & 1)));
-        // W (and U) of the next chunk
-        if (n + 1 < NT) {
-          if (!wait_bar(sm, B_TFULL, (n + 1) & 1, 1)) break;
+      // Every product of chunk k is issued as soon as its inputs are ready,
+      // each kind in chunk order; the barriers are the whole dependency graph
+      // (each phase is waited for once, in order).  The tensor pipe runs in
+      // order, so background work goes in 4-MMA pieces that the critical
+      // products can overtake.  In priority order:
+      //   W(k): TFULL(k), MRDY(k-1)   U(k): after W(k)   (they release the T tiles)
+      //   G(k) halves: FULL(k), GFREE(k-1)              (the UT solve is the long pole)
+      //   m(k): CWD(k)   q(k): M(k), W/U(k) issued, OFREE(k-1)   op(k): QRDY(k)
+      //   chain(n): SRDY(n), MRDY(n), O-part(n) issued
+      constexpr uint32_t id_g = idesc_bf16(128, 64, false, false);
+      int c_ch = 0, c_op = 0, c_q = 0, c_m = 0, c_w = 0, c_u = 0, c_g2 = 0;
+      uint32_t idle = 0, nap = 16;
+      while (c_ch < NT) {
+        if (c_w < NT && c_w == c_u && rdy(B_TFULL, c_w) && (c_w == 0 || rdy(B_MRDY, c_w - 1))) {
+          // ---- W^T = K^T (T diag exp gc)^T ----
+          const int m = c_w++;
           tc_fence_after();
-          issue_w(n + 1);
-          if (GATED) {
-            // U overwrites O2(n) in TMEM: wait until the epilogue has read it
-            if (!wait_bar(sm, B_OFREE, n & 1, 1)) break;
-            tc_fence_after();
-          }
-          issue_u(n + 1);
+          const uint32_t kq = smem_u32(sm.stage(m % NS));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + TM_X1, sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024),
+                   sdesc_sw128(a_tw + k * 32, 0, 1024), id_uw, k > 0);
+        } else if (c_u < c_w) {
+          // ---- U^T = V^T T^T ----
+          const int m = c_u++;
+          const uint32_t kq = smem_u32(sm.stage(m % NS));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + TM_X1 + 64, sdesc_sw128(kq + ST_V0 + k * 2048, 8192, 1024),
+                   sdesc_sw128(a_tu + k * 32, 0, 1024), id_uw, k > 0);
           mma_commit(sm.bar(B_WFULL));
+        } else if (c_g2 < 2 * NT && ((c_g2 & 1) ||
+                                     (rdy(B_FULL + (c_g2 >> 1) % NS, (c_g2 >> 1) / NS) &&
+                                      (c_g2 == 0 || rdy(B_GFREE, (c_g2 >> 1) - 1))))) {
+          // ---- G = [K;Q] K^T, one 64-column half of the K dimension ----
+          const int m = c_g2 >> 1, hf = c_g2 & 1;
+          ++c_g2;
+          tc_fence_after();
+          const uint32_t kq = smem_u32(sm.stage(m % NS)) + hf * 16384;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + TM_G, sdesc_sw128(kq + k * 32, 0, 1024), sdesc_sw128(kq + k * 32, 0, 1024), id_g,
+                   hf > 0 || k > 0);
+          if (hf) mma_commit(sm.bar(B_GFULL));
+        } else if (c_m < c_u && rdy(B_CWD, c_m)) {
+          // ---- (M-I)^T = -W^T Kd ----
+          const int m = c_m++;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_X1, tmem + TM_WB + k * 8, kd_desc(m, k), id_m, k > 0);
+          mma_commit(sm.bar(B_MFULL));
+        } else if (c_q < c_m && (c_q == 0 || rdy(B_OFREE, c_q - 1))) {
+          // ---- -W^T P^T (the rest of Q' is added on the CUDA cores) ----
+          const int m = c_q++;
+          tc_fence_after();
+          const uint32_t pb = a_p + (m & 1) * 8192;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + TM_O, tmem + TM_WB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_q, k > 0);
+          mma_commit(sm.bar(B_QFULL));
+        } else if (c_op < c_q && rdy(B_QRDY, c_op)) {
+          // ---- O^T = U^T P^T (first part of the output) ----
+          const int m = c_op++;
+          tc_fence_after();
+          const uint32_t pb = a_p + (m & 1) * 8192;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + TM_O, tmem + TM_UB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_op, k > 0);
+          mma_commit(sm.bar(B_PFREE0 + (m & 1)));
+        } else if (c_ch < c_op && rdy(B_SRDY, c_ch) && rdy(B_MRDY, c_ch)) {
+          // ---- the state step and the rest of O(n) ----
+          const int n = c_ch++;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + TM_S, tmem + TM_SBF + k * 8, sdesc_sw128(a_ms + k * 2048, 16384, 1024), id_s, true);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_S, tmem + TM_UB + k * 8, kd_desc(n, k), id_s, true);
+          mma_commit(sm.bar(B_SFULL));
+          const uint32_t st = smem_u32(sm.stage(n % NS));
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t qa = st + (k < 4 ? ST_Q0 : ST_Q1) + (k & 3) * 32;
+            mma_ts(tmem + TM_O, tmem + TM_SBF + k * 8, sdesc_sw128(qa, 0, 1024), id_o, true);
+          }
+          mma_commit(sm.bar(B_OFULL));
+          mma_commit(sm.bar(B_EMPTY + n % NS));
+        } else {
+          // nothing ready: back off (exponentially, so that the polling
+          // leaves the issue slots of this SM sub-partition to the solve),
+          // give up after ~1 s
+          if (++idle > (1u << 22) || ((idle & 63) == 0 && *sm.abort_flag())) {
+            *sm.abort_flag() = 1;
+            atomicCAS(&g_tc_error, 0u, 2u | (0xEEu << 8));
+            break;
+          }
+          __nanosleep(nap);
+          if (nap < 256) nap <<= 1;
+          continue;
         }
+        idle = 0;
+        nap = 16;
       }
       mma_commit(sm.bar(B_DRAIN));
       wait_bar(sm, B_DRAIN, 0, 1);
@@ -517,198 +727,327 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int L = q4 * 32 + lane;         // TMEM lane of this thread
     const int pw = warp - 2;              // 0..3
     const int pt = tid - 64;              // 0..127 within the group
-    float *At = sm.At();                  // A^T: entry (j, i) holds A_ij
-    float *X = sm.X();
-    const Arr64 gcp = sm.gcp();
-    const Arr64 bgc = sm.bgc();
+    float *AX = sm.AX();
+    float *eg = sm.arr(SM_EG), *ieg = sm.arr(SM_IEG), *bgc = sm.arr(SM_BGC);
     uint8_t *tu = sm.base + OFF_TU;
     uint8_t *tw = sm.base + OFF_TW;
     for (int m = 0; m < NT; ++m) {
       const int s = m % NS;
+      // every warp of the group is done with the previous chunk (its gate
+      // factors and beta exp(gc) are rewritten below)
+      if (named_sync_or(1, *sm.abort_flag() != 0)) break;
       // a failed wait sets the abort flag; every thread still reaches the
       // next named barrier and all of them leave together after it
       wait_bar(sm, B_FULL + s, (m / NS) & 1, 2);
-      const Arr64 sb = sm.beta(s);
+      const float *sb = sm.beta(s);
       if (GATED && warp == 2) {
         float lo, hi;
         warp_scan64(sm.lam(s), lane, lo, hi);
-        gcp[lane] = lo;
-        gcp[lane + 32] = hi;
+        AX[swz(lane, lane)] = lo;
+        AX[swz(lane + 32, lane + 32)] = hi;
+        const float e0 = fast_exp2(lo), e1 = fast_exp2(hi);
+        eg[lane] = e0;
+        eg[lane + 32] = e1;
+        ieg[lane] = fast_exp2(-lo);
+        ieg[lane + 32] = fast_exp2(-hi);
+        bgc[lane] = sb[lane] * e0;
+        bgc[lane + 32] = sb[lane + 32] * e1;
       }
+      if (!GATED && pt < 64) bgc[pt] = sb[pt];
       if (named_sync_or(1, *sm.abort_flag() != 0)) break;
-      if (pt < 64) bgc[pt] = GATED ? sb[pt] * fast_exp2(gcp[pt]) : sb[pt];
-      const int e0 = m * C;
-      const int t_lo = e0 / n_h;
-      int t_hi = (e0 + C - n_h) / n_h;
-      if (t_hi > p.T - 1) t_hi = p.T - 1;
-      const int Cp = t_hi - t_lo + 1;  // readout rows of this chunk
+      const Rows rw(m, n_h, p.T);
+      // exact per-entry decay only when the chunk's gate product leaves the
+      // range of the ratio form
+      const bool ratio = !GATED || AX[swz(63, 63)] >= kRatioFloor;
 
-      // ---- one row of G = [K;Q] K^T per thread (TMEM lane L) ----
+      // the P buffer is rewritten from here on
+      if (m >= 2) wait_bar(sm, B_PFREE0 + (m & 1), ((m >> 1) - 1) & 1, 2);
+      // ---- one row of G = [K;Q] K^T per thread (TMEM lane L), 16 columns at a time:
+      //      rows 0..63 give A (upper triangle of the solve array, transposed),
+      //      rows 64..127 give P ----
       wait_bar(sm, B_GFULL, m & 1, 2);
       tc_fence_after();
-      uint32_t g[64];
-      tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&g[0]));
-      tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&g[32]));
-      tmem_wait_ld_regs(g);
-      tc_fence_before();
-
-      if (L < 64) {
-        // ---- row i of A = beta_i Gam_ij (k_i . k_j), j < i, into A^T; blocks
-        //      right of the diagonal block are never read and not stored ----
-        const int i = L, blk = i >> 4;
-        const float bi = sb[i];
-        const float gi = GATED ? gcp[i] : 0.f;
+      {
+        const int i = L, r = L - 64;
+        const float bi = L < 64 ? sb[i] : 0.f;
+        const float gi = (GATED && L < 64) ? AX[swz(i, i)] : 0.f;
+        const float bie = (GATED && L < 64) ? bi * eg[i] : bi;
+        const int pos = (L >= 64 && r < rw.Cp) ? rw.pos(r, n_h) : -1;
+        const float gp = (GATED && pos >= 0) ? AX[swz(pos, pos)] : 0.f;
+        const float ep = (GATED && pos >= 0) ? eg[pos] : 1.f;
+        uint8_t *prow = sm.base + OFF_P + (m & 1) * 8192;
+#pragma unroll 1
+        for (int jb = 0; jb < 64; jb += 16) {
+          uint32_t g[16];
+          tmem_ld16(tmem_addr(tmem + TM_G, q4 * 32, jb), g);
+          tmem_wait_ld_regs(g);
+          if (L < 64) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          if ((j >> 4) > blk) continue;
-          const float v = bi * __uint_as_float(g[j]) * (GATED ? fast_exp2(gi - gcp[j]) : 1.f);
-          At[swz(j, i)] = ((j >> 4) == blk && j >= i) ? 0.f : v;
-        }
-      } else {
-        // ---- row r of P = (q_r . k_j) Gam, j <= pos(r) ----
-        const int r = L - 64;
-        const bool valid = r < Cp;
-        const int pos = valid ? (t_lo + r) * n_h + (n_h - 1) - e0 : -1;
-        const float gp = (GATED && valid) ? gcp[pos] : 0.f;
-        if (m >= 2) wait_bar(sm, B_PQFREE0 + (m & 1), ((m >> 1) - 1) & 1, 2);
-        uint8_t *ptile = sm.base + OFF_P + (m & 1) * 8192;
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = jb + jj;
+              if (j < i) {
+                const float f = !GATED ? bi : (ratio ? bie * ieg[j] : bi * fast_exp2(gi - AX[swz(j, j)]));
+                AX[swz(j, i)] = f * __uint_as_float(g[jj]);
+              }
+            }
+          } else {
+            uint32_t pk[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint32_t pk[4];
+            for (int u = 0; u < 8; ++u) {
+              float v[2];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j0 = q * 8 + 2 * u;
-            const float v0 =
-                (j0 <= pos) ? __uint_as_float(g[j0]) * (GATED ? fast_exp2(gp - gcp[j0]) : 1.f) : 0.f;
-            const float v1 = (j0 + 1 <= pos)
-                                 ? __uint_as_float(g[j0 + 1]) * (GATED ? fast_exp2(gp - gcp[j0 + 1]) : 1.f)
-                                 : 0.f;
-            pk[u] = pack_bf16(v0, v1);
+              for (int e = 0; e < 2; ++e) {
+                const int j = jb + 2 * u + e;
+                const float f = !GATED ? 1.f : (ratio ? ep * ieg[j] : fast_exp2(gp - AX[swz(j, j)]));
+                v[e] = j <= pos ? __uint_as_float(g[2 * u + e]) * f : 0.f;
+              }
+              pk[u] = pack_bf16(v[0], v[1]);
+            }
+            st_chunk(prow + sw128_offset(r, jb, 64), {pk[0], pk[1], pk[2], pk[3]});
+            st_chunk(prow + sw128_offset(r, jb + 8, 64), {pk[4], pk[5], pk[6], pk[7]});
           }
-          st_chunk(ptile, sw128_offset(r, q * 8, 64), pk);
         }
+        tc_fence_before();
+        arrive_warp(sm.bar(B_GFREE), lane);
       }
-      // the T tiles are rewritten from here on: U/W of the previous chunk
-      // must have consumed them
+      if (named_sync_or(1, *sm.abort_flag() != 0)) break;  // A complete
+
+      // ---- X = (I + A)^{-1}: 16x16 diagonal blocks, one per warp; the T
+      //      tiles are rewritten from here on ----
       if (m >= 1) wait_bar(sm, B_WFULL, (m - 1) & 1, 2);
-      if (named_sync_or(1, *sm.abort_flag() != 0)) break;  // A^T, P, bgc ready
-
+      invert_diag16(AX, tu, tw, sb, bgc, 16 * pw, lane);
+      named_sync(1);
       {
-        // ---- 16x16 diagonal blocks of X = (I + A)^{-1}: column jj of block
-        //      blk, rows split over a lane pair, right-looking forward
-        //      substitution; X and the T tiles written as columns finish ----
-        const int blk = pt >> 5, jj = (pt >> 1) & 15, half = pt & 1, o = 16 * blk;
-        const int col = o + jj;
-        const float bcol = sb[col], wcol = bgc[col];
-        float acc[8];
+        // ---- merge 16 -> 32: X21 = -X22 (A21 X11) in each 32-row half;
+        //      warp = (half, 8-column slab), the product A21 X11 stays in registers ----
+        const int o = 32 * (pw >> 1), n0 = o + 8 * (pw & 1);
+        uint32_t fa[2][4], fx[2][2], fz[2][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        float4 n0 = *reinterpret_cast<const float4 *>(At + swz(o, o + 8 * half));
-        float4 n1 = *reinterpret_cast<const float4 *>(At + swz(o, o + 8 * half + 4));
-#pragma unroll
-        for (int mm = 0; mm < 16; ++mm) {
-          const float cur[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-          if (mm + 1 < 16) {
-            n0 = *reinterpret_cast<const float4 *>(At + swz(o + mm + 1, o + 8 * half));
-            n1 = *reinterpret_cast<const float4 *>(At + swz(o + mm + 1, o + 8 * half + 4));
-          }
-          const int owner = mm >> 3;
-          const float xo = (mm == jj) ? 1.f : ((mm > jj) ? -acc[mm & 7] : 0.f);
-          const float x = __shfl_sync(0xffffffffu, xo, (lane & ~1) | owner);
-          if (half == owner) {
-            X[swz(o + mm, col)] = x;
-            const uint32_t off = sw128_offset(o + mm, col, 64);
-            *reinterpret_cast<__nv_bfloat16 *>(tu + off) = __float2bfloat16_rn(x * bcol);
-            *reinterpret_cast<__nv_bfloat16 *>(tw + off) = __float2bfloat16_rn(x * wcol);
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (8 * half + i > mm) acc[i] = fmaf(cur[i], x, acc[i]);
+        for (int ks = 0; ks < 2; ++ks) {
+          frag_a<0>(fa[ks], AX, o + 16, o + 8 * ks, lane);
+          frag_b<1>(fx[ks], AX, o + 8 * ks, n0, lane);
+          frag_a<1>(fz[ks], AX, o + 16, o + 16 + 8 * ks, lane);
         }
+        float y[1][4] = {{0.f, 0.f, 0.f, 0.f}}, z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) mma_tf32(y[0], fa[ks], fx[ks]);
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          uint32_t bb[2];
+          frag_b_acc<1>(bb, y, ks, lane);
+          mma_tf32(z, fz[ks], bb);
+        }
+        warp_store_16x8(AX, o + 16, n0, z, -1.f, lane);
+        frag_to_t(tu, tw, o + 16, n0, z, -1.f, sb, bgc, lane);
       }
       named_sync(1);
       {
-        // ---- merge 16 -> 32: X21' = -X22' (A21' X11') in each 32-row half ----
-        const int o = (pw >> 1) * 32, nt = pw & 1;
-        float y[4] = {0.f, 0.f, 0.f, 0.f}, unused[4];
-        warp_gemm<16, false>(y, unused, At, true, o + 16, o, X, o, o + 8 * nt, lane);
-        // scratch: the unused upper-right 32x32 block of X
-        const int sr = (pw >> 1) * 16, scol = 32 + (pw >> 1) * 16 + 8 * nt;
-        warp_store_16x8(X, sr, scol, y, 1.f, lane);
-        __syncwarp();
-        float z[4] = {0.f, 0.f, 0.f, 0.f};
-        warp_gemm<16, false>(z, unused, X, false, o + 16, o + 16, X, sr, scol, lane);
-        warp_store_16x8(X, o + 16, o + 8 * nt, z, -1.f, lane);
-        frag_to_t(tu, tw, o + 16, o + 8 * nt, z, -1.f, sb, bgc, lane);
-      }
-      named_sync(1);
-      {
-        // ---- merge 32 -> 64: Y = A21 X11 into the upper-right block, then
-        //      X21 = -X22 Y straight into the T tiles ----
-        const int mr = (pw >> 1) * 16, nc = (pw & 1) * 16;
-        float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
-        warp_gemm<32, true>(y0, y1, At, true, 32 + mr, 0, X, 0, nc, lane);
-        warp_store_16x8(X, mr, 32 + nc, y0, 1.f, lane);
-        warp_store_16x8(X, mr, 32 + nc + 8, y1, 1.f, lane);
-        named_sync(1);
-        float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
-        warp_gemm<32, true>(z0, z1, X, false, 32 + mr, 32, X, 0, 32 + nc, lane);
-        frag_to_t(tu, tw, 32 + mr, nc, z0, -1.f, sb, bgc, lane);
-        frag_to_t(tu, tw, 32 + mr, nc + 8, z1, -1.f, sb, bgc, lane);
+        // ---- merge 32 -> 64: rows 32..63, columns 8 pw .. 8 pw + 7 of X,
+        //      straight into the T tiles ----
+        const int n0 = 8 * pw;
+        uint32_t fa[2][4][4], fx[4][2], fz[2][4][4];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          frag_b<1>(fx[ks], AX, 8 * ks, n0, lane);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            frag_a<0>(fa[mt][ks], AX, 32 + 16 * mt, 8 * ks, lane);
+            frag_a<1>(fz[mt][ks], AX, 32 + 16 * mt, 32 + 8 * ks, lane);
+          }
+        }
+        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) mma_tf32(y[mt], fa[mt][ks], fx[ks]);
+        float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          uint32_t bb[2];
+          frag_b_acc<2>(bb, y, ks, lane);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) mma_tf32(z[mt], fz[mt][ks], bb);
+        }
+        frag_to_t(tu, tw, 32, n0, z[0], -1.f, sb, bgc, lane);
+        frag_to_t(tu, tw, 48, n0, z[1], -1.f, sb, bgc, lane);
       }
       fence_proxy_async_smem();
-      mbar_arrive(sm.bar(B_TFULL));
+      arrive_warp(sm.bar(B_TFULL), lane);
+    }
+  } else if (warp < 10) {
+    // ===================================================== feed-forward warps
+    const int q4 = warp & 3;
+    const int L = q4 * 32 + lane;  // TMEM lane: a d index
+    const int ft = tid - 192;      // 0..127 within the group
+    float *dec = sm.arr(SM_DEC);
+    for (int c = 0; c < NT; ++c) {
+      const int s = c % NS;
+      // every warp of the group is done with the previous chunk's gate
+      // factors before they are rewritten
+      if (named_sync_or(2, *sm.abort_flag() != 0)) break;
+      if (GATED) {
+        wait_bar(sm, B_FULL + s, (c / NS) & 1, 3);
+        if (warp == 6) {
+          float lo, hi;
+          warp_scan64(sm.lam(s), lane, lo, hi);
+          const float tot = __shfl_sync(0xffffffffu, hi, 31);
+          dec[lane] = fast_exp2(tot - lo);
+          dec[lane + 32] = fast_exp2(tot - hi);
+          if (lane == 0) *sm.gate_c() = fast_exp2(tot);
+        }
+        named_sync(2);
+      }
+
+      // ---- W^T, U^T -> bf16 operands; Kd ----
+      wait_bar(sm, B_WFULL, c & 1, 3);
+      tc_fence_after();
+      uint32_t pu[32];
+      {
+        uint32_t r[64];
+        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+        tmem_wait_ld_regs(r);
+        uint32_t pw_[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          pw_[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+        tmem_st32(tmem_addr(tmem + TM_WB, q4 * 32, 0), pw_);
+        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 64), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 96), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+        tmem_wait_ld_regs(r);
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          pu[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+      }
+      if (GATED) {
+        // Kd = diag(exp(gc_C - gc)) K into the V slot (V was consumed by U)
+        const uint8_t *kt = sm.stage(s);
+        uint8_t *kd = sm.stage(s) + ST_V0;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int qi = ft + 128 * it;  // 16-byte chunk: 512 per 64-column half
+          const int half = qi >> 9, rem = qi & 511, row = rem >> 3;
+          const uint4 v = *reinterpret_cast<const uint4 *>(kt + half * 16384 + rem * 16);
+          const float dr = dec[row];
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            o4[u] = pack_bf16(__uint_as_float(in[u] << 16) * dr, __uint_as_float(in[u] & 0xFFFF0000u) * dr);
+          st_chunk(kd + half * 8192 + rem * 16, o4);
+        }
+        fence_proxy_async_smem();
+      }
+      // U^T bf16 is read by the state step of the previous chunk until it ends
+      if (c >= 1) wait_bar(sm, B_SFULL, (c - 1) & 1, 3);
+      tmem_st32(tmem_addr(tmem + TM_UB, q4 * 32, 0), pu);
+      tmem_wait_st();
+      tc_fence_before();
+      arrive_warp(sm.bar(B_CWD), lane);
+
+      // ---- (M-I)^T -> bf16 smem operand (row L = j, columns i) ----
+      wait_bar(sm, B_MFULL, c & 1, 3);
+      tc_fence_after();
+      const float gm1 = GATED ? *sm.gate_c() - 1.f : 0.f;
+#pragma unroll 1
+      for (int cb = 0; cb < 128; cb += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, cb), r);
+        tmem_wait_ld_regs(r);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            o4[u] = pack_bf16(__uint_as_float(r[q * 8 + 2 * u]), __uint_as_float(r[q * 8 + 2 * u + 1]));
+          st_chunk(sm.base + OFF_MS + sw128_offset(L, cb + q * 8, 128), o4);
+        }
+      }
+      if (GATED) {
+        // the (exp(gc_C) - 1) I term, on this thread's own diagonal entry
+        __nv_bfloat16 *dg = reinterpret_cast<__nv_bfloat16 *>(sm.base + OFF_MS + sw128_offset(L, L, 128));
+        *dg = __float2bfloat16_rn(__bfloat162float(*dg) + gm1);
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      arrive_warp(sm.bar(B_MRDY), lane);
+
     }
   } else {
     // ===================================================== chain warps
     const int q4 = warp & 3;
     const int L = q4 * 32 + lane;  // TMEM lane = value column dv
-    // gate of a chunk: 2^(sum of its log2 gates)
-    auto chunk_decay = [&](int n) -> float {
-      if (!GATED) return 1.f;
-      const Arr64 lam = sm.lam(n % NS);
-      float t = lam[lane] + lam[lane + 32];
+    float *gq = sm.arr(SM_GQ);
+    // Q'(c) = exp(gc) Q - P W, in place over the Q tile of chunk c (same
+    // K-major layout: the output product reads it as its B operand); the
+    // scan for exp(gc) at the readout rows first
+    auto qprime = [&](int c) {
+      const int s = c % NS;
+      const Rows rw(c, n_h, p.T);
+      if (GATED) wait_bar(sm, B_FULL + s, (c / NS) & 1, 4);  // the chunk's log-gate row
+      if (GATED && warp == 10) {
+        float lo, hi;
+        warp_scan64(sm.lam(s), lane, lo, hi);
+        const float elo = fast_exp2(lo), ehi = fast_exp2(hi);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-      return fast_exp2(t);
-    };
-    // W^T of chunk m (TMEM, lane = d) -> bf16 smem operand, row d
-    auto convert_w = [&](int m) {
-      wait_bar(sm, B_WFULL, m & 1, 3);
-      if (m >= 1) wait_bar(sm, B_WFREE, (m - 1) & 1, 3);
-      tc_fence_after();
-      uint8_t *wt = sm.base + OFF_W;
-      uint32_t r[64];
-      tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-      tmem_ld32(tmem_addr(tmem + TM_GW, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
-      tmem_wait_ld_regs(r);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          pk[u] = pack_bf16(__uint_as_float(r[q * 8 + 2 * u]), __uint_as_float(r[q * 8 + 2 * u + 1]));
-        st_chunk(wt, sw128_offset(L, q * 8, 128), pk);
+        for (int hf = 0; hf < 2; ++hf) {
+          const int r = lane + 32 * hf;
+          const int pos = rw.pos(r, n_h);
+          const float a = __shfl_sync(0xffffffffu, elo, pos & 31);
+          const float e = __shfl_sync(0xffffffffu, ehi, pos & 31);
+          gq[r] = r < rw.Cp ? (pos < 32 ? a : e) : 0.f;
+        }
       }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      mbar_arrive(sm.bar(B_WREADY));
-    };
-    // the whole chain group proceeds only if every thread saw chunk 0 arrive
-    const bool ok = !named_sync_or(2, !wait_bar(sm, B_FULL + 0, 0, 3));
-    // ---- initial state S^T (lane = dv, column = dk) ----
-    if (ok) {
-      const float d0 = chunk_decay(0);
-      const float *h0 = p.h0 ? p.h0 + (size_t)bh * D * D : nullptr;
+      if (GATED) named_sync(3);
+      wait_bar(sm, B_QFULL, c & 1, 4);
+      tc_fence_after();
+      {
+        // element (row, column L) of the tile: row / 8 * 1024 + off[row % 8]
+        uint8_t *qt = sm.stage(s) + ((L >> 6) ? ST_Q1 : ST_Q0);
+        const int c8 = (L & 63) >> 3, ce = (L & 7) * 2;
+        uint32_t off[8];
 #pragma unroll
+        for (int bb = 0; bb < 8; ++bb) off[bb] = bb * 128 + ((c8 ^ bb) << 4) + ce;
+        const int cp = rw.Cp;
+        // 16 rows at a time: every load of a batch issues before its stores
+#pragma unroll 1
+        for (int b16 = 0; b16 < 64; b16 += 16) {
+          uint32_t z[16];
+          tmem_ld16(tmem_addr(tmem + TM_O, q4 * 32, b16), z);
+          uint8_t *qb = qt + (b16 >> 3) * 1024;
+          __nv_bfloat16 *e[16];
+          float qv[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            e[j] = reinterpret_cast<__nv_bfloat16 *>(qb + (j >> 3) * 1024 + off[j & 7]);
+            qv[j] = __bfloat162float(*e[j]);
+          }
+          tmem_wait_ld_regs(z);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int rr = b16 + j;
+            const float v = GATED ? fmaf(gq[rr], qv[j], __uint_as_float(z[j])) : qv[j] + __uint_as_float(z[j]);
+            *e[j] = __float2bfloat16_rn(rr < cp ? v : 0.f);
+          }
+        }
+        tc_fence_before();
+      }
+      fence_proxy_async_smem();
+      arrive_warp(sm.bar(B_QRDY), lane);
+      if (GATED) named_sync(3);  // gq is rewritten for the next chunk
+    };
+    // ---- initial state S^T (lane = dv, column = dk) ----
+    {
+      const float *h0 = p.h0 ? p.h0 + (size_t)bh * D * D : nullptr;
+#pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t f[32], pk[16];
 #pragma unroll
         for (int u = 0; u < 32; u += 2) {
           const float x0 = h0 ? h0[(size_t)(c0 + u) * D + L] : 0.f;
           const float x1 = h0 ? h0[(size_t)(c0 + u + 1) * D + L] : 0.f;
-          f[u] = __float_as_uint(x0 * d0);
-          f[u + 1] = __float_as_uint(x1 * d0);
+          f[u] = __float_as_uint(x0);
+          f[u + 1] = __float_as_uint(x1);
           pk[u >> 1] = pack_bf16(x0, x1);
         }
         tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, c0), f);
@@ -716,89 +1055,38 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(sm.bar(B_SREADY));
-      convert_w(0);
+      arrive_warp(sm.bar(B_SRDY), lane);
     }
-    for (int n = 0; ok && n < NT; ++n) {
-      const int s = n % NS;
-      const int e0 = n * C;
-      const int t_lo = e0 / n_h;
-      int t_hi = (e0 + C - n_h) / n_h;
-      if (t_hi > p.T - 1) t_hi = p.T - 1;
-      const int Cp = t_hi - t_lo + 1;
-      // ---- pseudo-values: Vt^T -> bf16 operands ----
-      wait_bar(sm, B_VTFULL, n & 1, 3);
-      tc_fence_after();
-      const Arr64 dec = sm.dec(n & 1);
-      const Arr64 gam = sm.gam(n & 1);
-      if (GATED) {
-        wait_bar(sm, B_FULL + s, (n / NS) & 1, 3);
-        if (warp == 6) {
-          float lo, hi;
-          warp_scan64(sm.lam(s), lane, lo, hi);
-          const float tot = __shfl_sync(0xffffffffu, hi, 31);
-          dec[lane] = fast_exp2(tot - lo);
-          dec[lane + 32] = fast_exp2(tot - hi);
-          gam[lane] = fast_exp2(lo);
-          gam[lane + 32] = fast_exp2(hi);
-        }
-        if (named_sync_or(2, *sm.abort_flag() != 0)) break;
-      }
-      {
-        uint32_t r[64];
-        tmem_ld32(tmem_addr(tmem + TM_UV, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-        tmem_ld32(tmem_addr(tmem + TM_UV, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
-        tmem_wait_ld_regs(r);
-        uint32_t pk[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u)
-          pk[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-        tmem_st32(tmem_addr(tmem + TM_VBF, q4 * 32, 0), pk);
-        if (GATED) {
-#pragma unroll
-          for (int u = 0; u < 32; ++u)
-            pk[u] = pack_bf16(__uint_as_float(r[2 * u]) * dec[2 * u],
-                              __uint_as_float(r[2 * u + 1]) * dec[2 * u + 1]);
-          tmem_st32(tmem_addr(tmem + TM_VDEC, q4 * 32, 0), pk);
-        }
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      mbar_arrive(sm.bar(B_VTREADY));
-
-      // ---- state: S^T -> bf16 copy for the next chunk (+ its decay), or hT ----
-      wait_bar(sm, B_SFULL, n & 1, 3);
+    if (!named_sync_or(3, *sm.abort_flag() != 0)) qprime(0);
+    for (int n = 0; n < NT; ++n) {
+      if (named_sync_or(3, *sm.abort_flag() != 0)) break;
+      const Rows rw(n, n_h, p.T);
+      // ---- state: S^T -> bf16 operand for the next chunk, or hT ----
+      wait_bar(sm, B_SFULL, n & 1, 4);
       tc_fence_after();
       if (n + 1 < NT) {
-        float dn = 1.f;
-        if (GATED) {
-          wait_bar(sm, B_FULL + (n + 1) % NS, ((n + 1) / NS) & 1, 3);
-          dn = chunk_decay(n + 1);
-        }
-        const uint32_t sbf = tmem + TM_SBF + ((n + 1) & 1) * 64;
+        uint32_t pk[64];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 64) {
-          uint32_t r[64], pk[32];
-          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0 + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r[64];
+          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, hf * 64), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, hf * 64 + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
           tmem_wait_ld_regs(r);
 #pragma unroll
           for (int u = 0; u < 32; ++u)
-            pk[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-          tmem_st32(tmem_addr(sbf, q4 * 32, c0 / 2), pk);
-          if (GATED) {
-#pragma unroll
-            for (int u = 0; u < 64; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * dn);
-            tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, c0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-            tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, c0 + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
-          }
+            pk[hf * 32 + u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
         }
+        // the output products of chunk n read the bf16 copy until they end
+        wait_bar(sm, B_OFULL, n & 1, 4);
+        tc_fence_after();
+        tmem_st32(tmem_addr(tmem + TM_SBF, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&pk[0]));
+        tmem_st32(tmem_addr(tmem + TM_SBF, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&pk[32]));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(sm.bar(B_SREADY));
+        arrive_warp(sm.bar(B_SRDY), lane);
       } else if (p.hT) {
         float *hT = p.hT + (size_t)bh * D * D;
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32];
           tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0), r);
@@ -807,67 +1095,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int u = 0; u < 32; ++u) hT[(size_t)(c0 + u) * D + L] = __uint_as_float(r[u]);
         }
       }
-      // ---- outputs of this chunk: o = exp(gc) O1 + O2 per readout row ----
-      wait_bar(sm, B_OFULL, n & 1, 3);
+      // ---- outputs of this chunk: the accumulator is read at once (so that
+      //      TMEM is released early), then one bf16 per readout row: the 32
+      //      lanes of a warp write 32 consecutive value columns of the row ----
+      wait_bar(sm, B_OFULL, n & 1, 4);
       tc_fence_after();
-      float o[64];
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t r1[32];
-        tmem_ld32(tmem_addr(tmem + TM_O, q4 * 32, hf * 32), r1);
-        if (GATED) {
-          uint32_t r2[32];
-          tmem_ld32(tmem_addr(tmem + TM_UV, q4 * 32, hf * 32), r2);
-          tmem_wait_ld_regs(r1);
-          tmem_wait_ld_regs(r2);
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const int rr = hf * 32 + u;
-            const int pos = (t_lo + rr) * n_h + (n_h - 1) - e0;
-            const float gm = rr < Cp ? gam[pos] : 0.f;
-            o[rr] = fmaf(gm, __uint_as_float(r1[u]), __uint_as_float(r2[u]));
-          }
-        } else {
-          tmem_wait_ld_regs(r1);
-#pragma unroll
-          for (int u = 0; u < 32; ++u) o[hf * 32 + u] = __uint_as_float(r1[u]);
-        }
-      }
+      uint32_t o[64];
+      tmem_ld32(tmem_addr(tmem + TM_O, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&o[0]));
+      tmem_ld32(tmem_addr(tmem + TM_O, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&o[32]));
+      tmem_wait_ld_regs(o);
       tc_fence_before();
-      mbar_arrive(sm.bar(B_OFREE));
-      // W^T of the next chunk before the stores: it gates the next chain step
-      if (n + 1 < NT) convert_w(n + 1);
-      // 8x8 transposes within groups of 8 lanes: lane k of a group then holds
-      // 8 consecutive value columns of row 8 rg + k -> one 16-byte store
+      arrive_warp(sm.bar(B_OFREE), lane);
       {
-        const int k = lane & 7;
-        const size_t col = (size_t)q4 * 32 + (lane >> 3) * 8;
+        __nv_bfloat16 *orow = p.out + (((size_t)b * p.T + rw.t_lo) * p.H + h) * D + L;
+        const size_t rstride = (size_t)p.H * D;
+        const int cp = rw.Cp;
 #pragma unroll
-        for (int rg = 0; rg < 8; ++rg) {
-          float v[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = o[rg * 8 + j];
-#pragma unroll
-          for (int sh = 1; sh < 8; sh <<= 1) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (j & sh) continue;
-              const float send = (k & sh) ? v[j] : v[j | sh];
-              const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
-              if (k & sh)
-                v[j] = recv;
-              else
-                v[j | sh] = recv;
-            }
-          }
-          const int row = rg * 8 + k;
-          if (row < Cp) {
-            const uint4 pkt = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
-                                         pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
-            *reinterpret_cast<uint4 *>(p.out + (((size_t)b * p.T + t_lo + row) * p.H + h) * D + col) = pkt;
-          }
-        }
+        for (int rr = 0; rr < 64; ++rr)
+          if (rr < cp) orow[rr * rstride] = __float2bfloat16_rn(__uint_as_float(o[rr]));
       }
+      if (n + 1 < NT) qprime(n + 1);
     }
   }
 

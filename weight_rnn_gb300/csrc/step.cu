@@ -16,11 +16,15 @@
 // (expand S after each sub-step: S_j = g S0 + sum_{i<=j} beta_i k_i e_i^T, so
 // S_{j-1}^T k_j and S_{n_h}^T q are the sums above).
 //
-// The kernel is bound by HBM bandwidth: one CTA per (b, h) head, each row of
-// the state is read by float4 loads across a warp (dv/4 threads per row) and
-// held in registers between the read and the write; the reductions over the
-// key index use shared memory across row groups.  Loads and stores of the
-// state use the streaming cache hint: every byte is touched once per call.
+// The kernel is bound by HBM bandwidth.  The columns of a head's state are
+// independent given the token's keys and query (every reduction runs over the
+// key index d), so a CTA owns one head and one slab of 32 value columns: a
+// 16 KB slice of the state, read once into registers (float4 per thread, 8
+// threads per row, 16 row groups) and written once.  The key/query dot
+// products are recomputed per slab (a few hundred flops).  Small CTAs let
+// several slices per SM be in their load phase while others compute and
+// store.  Loads and stores use the streaming cache hint: every byte of the
+// state is touched once per call.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -28,10 +32,10 @@
 namespace delta {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kMaxNh = 4;
+constexpr int kThreads = 128;
+constexpr int kSlab = 32;      // value columns per CTA (fewer when dv < 32)
 constexpr int kMaxD = 128;
-constexpr int kMaxRows = 16;  // rows of the state held per thread (dk = 128, dv = 128)
+constexpr int kMaxRows = 8;    // state rows per thread at dk = 128
 
 __device__ __forceinline__ float load_io(const void *p, int64_t i, bool bf16) {
   return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i])
@@ -45,53 +49,60 @@ __device__ __forceinline__ void store_io(void *p, int64_t i, float x, bool bf16)
     static_cast<float *>(p)[i] = x;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) step_kernel(StepArgs a) {
-  __shared__ float s_k[kMaxNh][kMaxD];
+template <int NH>
+__global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
+  __shared__ float s_k[NH][kMaxD];
   __shared__ float s_q[kMaxD];
-  __shared__ float s_v[kMaxNh][kMaxD];
-  __shared__ float s_e[kMaxNh][kMaxD];
-  __shared__ float s_r[kMaxNh + 1][kMaxD];
-  __shared__ float s_beta[kMaxNh];
-  __shared__ float s_dot[kMaxNh + 1][kMaxNh];  // [i][j] = k_i.k_j (i<j); [n_h][j] = k_j.q
-  // partial sums per row group: (n_h + 1) x RG x dv floats, RG * dv == 4 * kThreads
-  __shared__ float s_part[(kMaxNh + 1) * 4 * kThreads];
+  __shared__ float s_v[NH][kSlab];
+  __shared__ float s_e[NH][kSlab];
+  __shared__ float s_r[NH + 1][kSlab];
+  __shared__ float s_beta[NH];
+  __shared__ float s_dot[NH + 1][NH];  // [i][j] = k_i.k_j (i<j); [NH][j] = k_j.q
+  // partial sums per row group: (NH + 1) x RG x SW floats, RG * SW == 4 * kThreads
+  // (written as float4: 16-byte alignment)
+  __shared__ __align__(16) float s_part[(NH + 1) * 4 * kThreads];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int dk = a.dk, dv = a.dv, n_h = a.n_h;
-  const int64_t bh = blockIdx.x;
+  const int dk = a.dk, dv = a.dv;
+  const int SW = dv < kSlab ? dv : kSlab;
+  const int nslab = dv / SW;
+  const int64_t bh = blockIdx.x / nslab;
+  const int cbase = (blockIdx.x % nslab) * SW;
   const int64_t b = bh / a.H, h = bh % a.H, H = a.H;
 
-  // ---- token inputs to shared memory ----
-  for (int i = tid; i < dk; i += kThreads) s_q[i] = load_io(a.q, bh * dk + i, a.bf16);
-  for (int i = tid; i < n_h * dk; i += kThreads) {
-    const int j = i / dk, d = i % dk;
-    s_k[j][d] = load_io(a.k, ((b * n_h + j) * H + h) * dk + d, a.bf16);
-  }
-  for (int i = tid; i < n_h * dv; i += kThreads) {
-    const int j = i / dv, c = i % dv;
-    s_v[j][c] = load_io(a.v, ((b * n_h + j) * H + h) * dv + c, a.bf16);
-  }
-  if (tid < n_h) s_beta[tid] = a.beta[(b * n_h + tid) * H + h];
-  const float gate = a.g ? a.g[bh] : 1.0f;
-
-  // ---- the state: thread owns 4 columns of rows d = rg, rg + RG, ... ----
-  const int tpr = dv / 4;          // threads per row
+  // ---- the state slice: thread owns 4 columns of rows d = rg, rg + RG, ... ----
+  const int tpr = SW / 4;          // threads per row
   const int RG = kThreads / tpr;   // row groups
   const int rg = tid / tpr;
-  const int c4 = (tid % tpr) * 4;
-  float4 *srow = reinterpret_cast<float4 *>(a.state + bh * (int64_t)dk * dv);
+  const int c4 = (tid % tpr) * 4;  // column within the slab
+  float4 *srow = reinterpret_cast<float4 *>(a.state + bh * (int64_t)dk * dv + cbase);
   float4 S[kMaxRows];
 #pragma unroll
   for (int i = 0; i < kMaxRows; ++i) {
     const int d = rg + i * RG;
     if (d < dk) S[i] = __ldcs(srow + ((int64_t)d * dv + c4) / 4);
   }
+
+  // ---- token inputs to shared memory ----
+  for (int i = tid; i < dk; i += kThreads) s_q[i] = load_io(a.q, bh * dk + i, a.bf16);
+  for (int i = tid; i < NH * dk; i += kThreads) {
+    const int j = i / dk, d = i % dk;
+    s_k[j][d] = load_io(a.k, ((b * NH + j) * H + h) * dk + d, a.bf16);
+  }
+  for (int i = tid; i < NH * SW; i += kThreads) {
+    const int j = i / SW, c = i % SW;
+    s_v[j][c] = load_io(a.v, ((b * NH + j) * H + h) * dv + cbase + c, a.bf16);
+  }
+  if (tid < NH) s_beta[tid] = a.beta[(b * NH + tid) * H + h];
+  const float gate = a.g ? a.g[bh] : 1.0f;
   __syncthreads();  // token inputs visible
 
   // ---- the small dot products k_i.k_j and k_j.q, one warp each ----
   {
     int pair = 0;
-    for (int j = 0; j < n_h; ++j) {
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+#pragma unroll
       for (int i = 0; i <= j; ++i, ++pair) {
         // i < j: k_i.k_j ; i == j: k_j.q
         if (pair % (kThreads / 32) != warp) continue;
@@ -103,24 +114,23 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepArgs a) {
           if (i < j)
             s_dot[i][j] = acc;
           else
-            s_dot[n_h][j] = acc;
+            s_dot[NH][j] = acc;
         }
       }
     }
   }
 
   // ---- partial r_j = S0^T k_j and r_q = S0^T q over this thread's rows ----
-  float4 part[kMaxNh + 1];
+  float4 part[NH + 1];
 #pragma unroll
-  for (int j = 0; j <= kMaxNh; ++j) part[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j <= NH; ++j) part[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < kMaxRows; ++i) {
     const int d = rg + i * RG;
     if (d < dk) {
 #pragma unroll
-      for (int j = 0; j <= kMaxNh; ++j) {
-        if (j > n_h) continue;
-        const float w = (j < n_h) ? s_k[j][d] : s_q[d];
+      for (int j = 0; j <= NH; ++j) {
+        const float w = (j < NH) ? s_k[j][d] : s_q[d];
         part[j].x = fmaf(S[i].x, w, part[j].x);
         part[j].y = fmaf(S[i].y, w, part[j].y);
         part[j].z = fmaf(S[i].z, w, part[j].z);
@@ -128,63 +138,55 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepArgs a) {
       }
     }
   }
-  // s_part layout: [j][rg][dv]
+  // s_part layout: [j][rg][SW]
 #pragma unroll
-  for (int j = 0; j <= kMaxNh; ++j) {
-    if (j > n_h) continue;
-    float *dst = s_part + ((size_t)j * RG + rg) * dv + c4;
-    dst[0] = part[j].x;
-    dst[1] = part[j].y;
-    dst[2] = part[j].z;
-    dst[3] = part[j].w;
-  }
+  for (int j = 0; j <= NH; ++j)
+    *reinterpret_cast<float4 *>(s_part + ((size_t)j * RG + rg) * SW + c4) = part[j];
   __syncthreads();
-  for (int i = tid; i < (n_h + 1) * dv; i += kThreads) {
-    const int j = i / dv, c = i % dv;
-    const float *src = s_part + (size_t)j * RG * dv + c;
+  for (int i = tid; i < (NH + 1) * SW; i += kThreads) {
+    const int j = i / SW, c = i % SW;
+    const float *src = s_part + (size_t)j * RG * SW + c;
     float acc = 0.0f;
     const int rows_used = dk < RG ? dk : RG;
-    for (int r = 0; r < rows_used; ++r) acc += src[(size_t)r * dv];
+    for (int r = 0; r < rows_used; ++r) acc += src[(size_t)r * SW];
     s_r[j][c] = acc;
   }
   __syncthreads();
 
   // ---- prediction errors and the output, per value column ----
-  for (int c = tid; c < dv; c += kThreads) {
-    float o = gate * s_r[n_h][c];
-    for (int j = 0; j < n_h; ++j) {
+  for (int c = tid; c < SW; c += kThreads) {
+    float o = gate * s_r[NH][c];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
       float pred = gate * s_r[j][c];
+#pragma unroll
       for (int i = 0; i < j; ++i) pred = fmaf(s_beta[i] * s_dot[i][j], s_e[i][c], pred);
       const float e = s_v[j][c] - pred;
       s_e[j][c] = e;
-      o = fmaf(s_beta[j] * s_dot[n_h][j], e, o);
+      o = fmaf(s_beta[j] * s_dot[NH][j], e, o);
     }
-    store_io(a.out, bh * dv + c, o, a.bf16);
+    store_io(a.out, bh * dv + cbase + c, o, a.bf16);
   }
   __syncthreads();
 
   // ---- S' = g S0 + sum_j beta_j k_j e_j^T, written in place ----
-  float4 be[kMaxNh];
+  float4 be[NH];
 #pragma unroll
-  for (int j = 0; j < kMaxNh; ++j) {
-    if (j < n_h)
-      be[j] = make_float4(s_beta[j] * s_e[j][c4], s_beta[j] * s_e[j][c4 + 1],
-                          s_beta[j] * s_e[j][c4 + 2], s_beta[j] * s_e[j][c4 + 3]);
-  }
+  for (int j = 0; j < NH; ++j)
+    be[j] = make_float4(s_beta[j] * s_e[j][c4], s_beta[j] * s_e[j][c4 + 1],
+                        s_beta[j] * s_e[j][c4 + 2], s_beta[j] * s_e[j][c4 + 3]);
 #pragma unroll
   for (int i = 0; i < kMaxRows; ++i) {
     const int d = rg + i * RG;
     if (d < dk) {
       float4 x = make_float4(S[i].x * gate, S[i].y * gate, S[i].z * gate, S[i].w * gate);
 #pragma unroll
-      for (int j = 0; j < kMaxNh; ++j) {
-        if (j < n_h) {
-          const float kd = s_k[j][d];
-          x.x = fmaf(kd, be[j].x, x.x);
-          x.y = fmaf(kd, be[j].y, x.y);
-          x.z = fmaf(kd, be[j].z, x.z);
-          x.w = fmaf(kd, be[j].w, x.w);
-        }
+      for (int j = 0; j < NH; ++j) {
+        const float kd = s_k[j][d];
+        x.x = fmaf(kd, be[j].x, x.x);
+        x.y = fmaf(kd, be[j].y, x.y);
+        x.z = fmaf(kd, be[j].z, x.z);
+        x.w = fmaf(kd, be[j].w, x.w);
       }
       __stcs(srow + ((int64_t)d * dv + c4) / 4, x);
     }
@@ -194,7 +196,15 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepArgs a) {
 }  // namespace
 
 cudaError_t launch_step(const StepArgs &a, cudaStream_t s) {
-  step_kernel<<<(unsigned)(a.B * a.H), kThreads, 0, s>>>(a);
+  const int sw = a.dv < kSlab ? a.dv : kSlab;
+  const unsigned grid = (unsigned)(a.B * a.H * (a.dv / sw));
+  switch (a.n_h) {
+    case 1: step_kernel<1><<<grid, kThreads, 0, s>>>(a); break;
+    case 2: step_kernel<2><<<grid, kThreads, 0, s>>>(a); break;
+    case 3: step_kernel<3><<<grid, kThreads, 0, s>>>(a); break;
+    case 4: step_kernel<4><<<grid, kThreads, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
