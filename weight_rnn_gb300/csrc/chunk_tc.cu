@@ -95,7 +95,7 @@ constexpr uint32_t SM_BAR = SM_GQ + 256;
 
 // ---- barrier indices ----
 enum {
-  B_FULL = 0,        // [NS] producer -> all: stage loaded (count 2 + tx)
+  B_FULL = 0,        // [NS] producer -> all: K, Q tiles, beta, log gate loaded (count 2 + tx)
   B_EMPTY = NS,      // [NS] MMA -> producer: stage consumed
   B_GFULL = 2 * NS,  // MMA -> prep: G in TMEM
   B_GFREE,           // prep -> MMA: G read (one arrival per warp)
@@ -113,7 +113,8 @@ enum {
   B_PFREE0,          // MMA -> prep: P buffer 0 consumed
   B_PFREE1,          //                        1
   B_DRAIN,           // MMA: everything issued has completed
-  NBARS
+  B_VFULL,           // [NS] producer -> MMA: the V tile of a stage loaded (count 1 + tx)
+  NBARS = B_VFULL + NS
 };
 constexpr uint32_t SM_MISC = SM_BAR + NBARS * 8;  // tmem slot, abort flag, gate of the chunk
 constexpr uint32_t SMEM_TOTAL = OFF_SM + SM_MISC + 16;
@@ -513,8 +514,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(sm.bar(B_FULL + s), 2);
       mbar_init(sm.bar(B_EMPTY + s), 1);
     }
-    const int cnt[NBARS - 2 * NS] = {1, 4, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, 1};
-    for (int i = 2 * NS; i < NBARS; ++i) mbar_init(sm.bar(i), cnt[i - 2 * NS]);
+    const int cnt[B_VFULL - 2 * NS] = {1, 4, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, 1};
+    for (int i = 2 * NS; i < B_VFULL; ++i) mbar_init(sm.bar(i), cnt[i - 2 * NS]);
+    for (int s = 0; s < NS; ++s) mbar_init(sm.bar(B_VFULL + s), 1);
     *sm.abort_flag() = 0;
     fence_mbar_init();
   }
@@ -573,14 +575,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           tma_prefetch_4d(&map_q, 0, h, pt, b);
           tma_prefetch_4d(&map_q, 64, h, pt, b);
         }
-        mbar_arrive_expect_tx(sm.bar(B_FULL + s), 2u * (8192u + 8192u + (uint32_t)QR * 128u));
+        // K and Q first, on their own barrier (the G product waits for them
+        // only); V, needed later, on a second one
+        mbar_arrive_expect_tx(sm.bar(B_FULL + s), 2u * (8192u + (uint32_t)QR * 128u));
         uint64_t *fb = sm.bar(B_FULL + s);
         tma_load_4d(st + ST_K0, &map_k, fb, 0, h, e0, b);
         tma_load_4d(st + ST_K1, &map_k, fb, 64, h, e0, b);
         tma_load_4d(st + ST_Q0, &map_q, fb, 0, h, t_lo, b);
         tma_load_4d(st + ST_Q1, &map_q, fb, 64, h, t_lo, b);
-        tma_load_4d(st + ST_V0, &map_v, fb, 0, h, e0, b);
-        tma_load_4d(st + ST_V0 + 8192, &map_v, fb, 64, h, e0, b);
+        uint64_t *vb = sm.bar(B_VFULL + s);
+        mbar_arrive_expect_tx(vb, 2u * 8192u);
+        tma_load_4d(st + ST_V0, &map_v, vb, 0, h, e0, b);
+        tma_load_4d(st + ST_V0 + 8192, &map_v, vb, 64, h, e0, b);
       }
       issued = n + 1;
       float *sb = sm.beta(s), *sl = sm.lam(s);
@@ -594,8 +600,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     }
     // copies still in flight must land before the CTA's shared memory goes
     if (lane == 0)
-      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n)
+      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n) {
         wait_bar(sm, B_FULL + n % NS, (n / NS) & 1, 0);
+        wait_bar(sm, B_VFULL + n % NS, (n / NS) & 1, 0);
+      }
     __syncwarp();
   } else if (warp == 1) {
     // ===================================================== MMA issuer
@@ -619,7 +627,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       // (each phase is waited for once, in order).  The tensor pipe runs in
       // order, so background work goes in 4-MMA pieces that the critical
       // products can overtake.  In priority order:
-      //   W(k): TFULL(k), MRDY(k-1)   U(k): after W(k)   (they release the T tiles)
+      //   W(k): TFULL(k), MRDY(k-1)   U(k): after W(k), VFULL(k)   (they release the T tiles)
       //   G(k) halves: FULL(k), GFREE(k-1)              (the UT solve is the long pole)
       //   m(k): CWD(k)   q(k): M(k), W/U(k) issued, OFREE(k-1)   op(k): QRDY(k)
       //   chain(n): SRDY(n), MRDY(n), O-part(n) issued
@@ -636,9 +644,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_X1, sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024),
                    sdesc_sw128(a_tw + k * 32, 0, 1024), id_uw, k > 0);
-        } else if (c_u < c_w) {
+        } else if (c_u < c_w && rdy(B_VFULL + c_u % NS, c_u / NS)) {
           // ---- U^T = V^T T^T ----
           const int m = c_u++;
+          tc_fence_after();
           const uint32_t kq = smem_u32(sm.stage(m % NS));
 #pragma unroll
           for (int k = 0; k < 4; ++k)
