@@ -854,28 +854,34 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         // ---- merge 32 -> 64: rows 32..63, columns 8 pw .. 8 pw + 7 of X,
         //      straight into the T tiles ----
         const int n0 = 8 * pw;
-        uint32_t fa[2][4][4], fx[4][2], fz[2][4][4];
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          frag_b<1>(fx[ks], AX, 8 * ks, n0, lane);
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            frag_a<0>(fa[mt][ks], AX, 32 + 16 * mt, 8 * ks, lane);
-            frag_a<1>(fz[mt][ks], AX, 32 + 16 * mt, 32 + 8 * ks, lane);
-          }
-        }
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          uint32_t fa[2][4][4], fx[4][2];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+          for (int ks = 0; ks < 4; ++ks) {
+            frag_b<1>(fx[ks], AX, 8 * ks, n0, lane);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) mma_tf32(y[mt], fa[mt][ks], fx[ks]);
+            for (int mt = 0; mt < 2; ++mt) frag_a<0>(fa[mt][ks], AX, 32 + 16 * mt, 8 * ks, lane);
+          }
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_tf32(y[mt], fa[mt][ks], fx[ks]);
+        }
         float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          uint32_t fz[2][4][4];
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          uint32_t bb[2];
-          frag_b_acc<2>(bb, y, ks, lane);
+          for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt) mma_tf32(z[mt], fz[mt][ks], bb);
+            for (int mt = 0; mt < 2; ++mt) frag_a<1>(fz[mt][ks], AX, 32 + 16 * mt, 32 + 8 * ks, lane);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            uint32_t bb[2];
+            frag_b_acc<2>(bb, y, ks, lane);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) mma_tf32(z[mt], fz[mt][ks], bb);
+          }
         }
         frag_to_t(tu, tw, 32, n0, z[0], -1.f, sb, bgc, lane);
         frag_to_t(tu, tw, 48, n0, z[1], -1.f, sb, bgc, lane);
@@ -910,23 +916,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       // ---- W^T, U^T -> bf16 operands; Kd ----
       wait_bar(sm, B_WFULL, c & 1, 3);
       tc_fence_after();
-      uint32_t pu[32];
       {
-        uint32_t r[64];
+        uint32_t r[64], pw_[32];
         tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
         tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
         tmem_wait_ld_regs(r);
-        uint32_t pw_[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u)
           pw_[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+        // W^T bf16 of the previous chunk is read by its -W^T P^T product
+        // (after its M product, whose completion was waited for already)
+        if (c >= 1) {
+          wait_bar(sm, B_QFULL, (c - 1) & 1, 3);
+          tc_fence_after();
+        }
         tmem_st32(tmem_addr(tmem + TM_WB, q4 * 32, 0), pw_);
-        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 64), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 96), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
-        tmem_wait_ld_regs(r);
-#pragma unroll
-        for (int u = 0; u < 32; ++u)
-          pu[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
       }
       if (GATED) {
         // Kd = diag(exp(gc_C - gc)) K into the V slot (V was consumed by U)
@@ -946,6 +950,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           st_chunk(kd + half * 8192 + rem * 16, o4);
         }
         fence_proxy_async_smem();
+      }
+      uint32_t pu[32];
+      {
+        uint32_t r[64];
+        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 64), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 96), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+        tmem_wait_ld_regs(r);
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          pu[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
       }
       // U^T bf16 is read by the state step of the previous chunk until it ends
       if (c >= 1) wait_bar(sm, B_SFULL, (c - 1) & 1, 3);
@@ -1076,14 +1090,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       if (n + 1 < NT) {
         uint32_t pk[64];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t r[64];
-          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, hf * 64), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, hf * 64 + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t r[32];
+          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, cb * 32), r);
           tmem_wait_ld_regs(r);
 #pragma unroll
-          for (int u = 0; u < 32; ++u)
-            pk[hf * 32 + u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+          for (int u = 0; u < 16; ++u)
+            pk[cb * 16 + u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
         }
         // the output products of chunk n read the bf16 copy until they end
         wait_bar(sm, B_OFULL, n & 1, 4);
