@@ -120,6 +120,22 @@ def test_deterministic():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
+@pytest.mark.parametrize("gated,n_h", [(False, 1), (True, 1), (True, 3)])
+def test_repeated_launches_are_bitwise_identical(gated, n_h):
+    """The tensor-core kernel hands every intermediate between warp roles
+    through barriers; a missing wait shows up as run-to-run differences.
+    Many heads (one CTA each) and many chunks, several launches, bitwise."""
+    w = small(B=4, H=16, T=1024, gated=gated, n_h=n_h, h0=0.05 if gated else 0.0,
+              seed=123 + n_h)
+    inp = synth.fwd_inputs(w)
+    o0, s0 = gpu_fwd(inp, w)
+    for _ in range(4):
+        o, s_ = gpu_fwd(inp, w)
+        assert torch.equal(o, o0) and torch.equal(s_, s0)
+    heads = [(0, 0), (1, 7), (3, 15)]
+    check_sampled(inp, w, o0, s0, heads)
+
+
 def test_misaligned_pointer_is_rejected():
     w = small(T=8)
     inp = synth.fwd_inputs(w)
