@@ -96,7 +96,7 @@ constexpr uint32_t SM_BAR = SM_GQ + 256;
 // ---- barrier indices ----
 enum {
   B_FULL = 0,        // [NS] producer -> all: K, Q tiles, beta, log gate loaded (count 2 + tx)
-  B_EMPTY = NS,      // [NS] MMA -> producer: stage consumed
+  B_EMPTY = NS,      // [NS] MMA -> producer: K, Q tiles of the stage consumed
   B_GFULL = 2 * NS,  // MMA -> prep: G in TMEM
   B_GFREE,           // prep -> MMA: G read (one arrival per warp)
   B_TFULL,           // prep -> MMA: T tiles and P written (per warp)
@@ -114,7 +114,8 @@ enum {
   B_PFREE1,          //                        1
   B_DRAIN,           // MMA: everything issued has completed
   B_VFULL,           // [NS] producer -> MMA: the V tile of a stage loaded (count 1 + tx)
-  NBARS = B_VFULL + NS
+  B_VEMPTY = B_VFULL + NS,  // [NS] chain -> producer: V slot free (per warp; it stages the outputs)
+  NBARS = B_VEMPTY + NS
 };
 constexpr uint32_t SM_MISC = SM_BAR + NBARS * 8;  // tmem slot, abort flag, gate of the chunk
 constexpr uint32_t SMEM_TOTAL = OFF_SM + SM_MISC + 16;
@@ -463,6 +464,12 @@ __device__ __forceinline__ void warp_scan64(const float *lam, int lane, float &l
   hi += __shfl_sync(0xffffffffu, lo, 31);
 }
 
+// 16-byte shared-memory load at a 32-bit shared address
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_chunk(uint8_t *p, const uint32_t (&v)[4]) {
   *reinterpret_cast<uint4 *>(p) = make_uint4(v[0], v[1], v[2], v[3]);
 }
@@ -513,6 +520,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     for (int s = 0; s < NS; ++s) {
       mbar_init(sm.bar(B_FULL + s), 2);
       mbar_init(sm.bar(B_EMPTY + s), 1);
+      mbar_init(sm.bar(B_VEMPTY + s), 4);
     }
     const int cnt[B_VFULL - 2 * NS] = {1, 4, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, 1};
     for (int i = 2 * NS; i < B_VFULL; ++i) mbar_init(sm.bar(i), cnt[i - 2 * NS]);
@@ -555,7 +563,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
     };
     fetch(0);
-    int issued = 0;
+    int issued = 0, issued_v = 0;
     for (int n = 0; n < NT; ++n) {
       const int s = n % NS;
       int ok = 1;
@@ -583,10 +591,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         tma_load_4d(st + ST_K1, &map_k, fb, 64, h, e0, b);
         tma_load_4d(st + ST_Q0, &map_q, fb, 0, h, t_lo, b);
         tma_load_4d(st + ST_Q1, &map_q, fb, 64, h, t_lo, b);
-        uint64_t *vb = sm.bar(B_VFULL + s);
-        mbar_arrive_expect_tx(vb, 2u * 8192u);
-        tma_load_4d(st + ST_V0, &map_v, vb, 0, h, e0, b);
-        tma_load_4d(st + ST_V0 + 8192, &map_v, vb, 64, h, e0, b);
       }
       issued = n + 1;
       float *sb = sm.beta(s), *sl = sm.lam(s);
@@ -596,14 +600,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       sl[lane + 32] = nl[1];
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(B_FULL + s));
+      // V on its own barrier: its slot stages the outputs of the chunk NS
+      // back, until the chain warps have written them out
+      if (n >= NS && lane == 0) ok = wait_bar(sm, B_VEMPTY + s, ((n / NS) - 1) & 1, 0);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane == 0) {
+        uint64_t *vb = sm.bar(B_VFULL + s);
+        mbar_arrive_expect_tx(vb, 2u * 8192u);
+        tma_load_4d(st + ST_V0, &map_v, vb, 0, h, e0, b);
+        tma_load_4d(st + ST_V0 + 8192, &map_v, vb, 64, h, e0, b);
+      }
+      issued_v = n + 1;
       fetch(n + 1);
     }
     // copies still in flight must land before the CTA's shared memory goes
-    if (lane == 0)
-      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n) {
-        wait_bar(sm, B_FULL + n % NS, (n / NS) & 1, 0);
+    if (lane == 0) {
+      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n) wait_bar(sm, B_FULL + n % NS, (n / NS) & 1, 0);
+      for (int n = (issued_v > NS ? issued_v - NS : 0); n < issued_v; ++n)
         wait_bar(sm, B_VFULL + n % NS, (n / NS) & 1, 0);
-      }
+    }
     __syncwarp();
   } else if (warp == 1) {
     // ===================================================== MMA issuer
@@ -625,17 +640,62 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       // Every product of chunk k is issued as soon as its inputs are ready,
       // each kind in chunk order; the barriers are the whole dependency graph
       // (each phase is waited for once, in order).  The tensor pipe runs in
-      // order, so background work goes in 4-MMA pieces that the critical
-      // products can overtake.  In priority order:
+      // order and a thread's issue blocks while it is busy, so the products
+      // on the state recurrence (chain -> outputs -> Q' -> op -> chain) go
+      // first and the look-ahead work for later chunks after them, in 4-MMA
+      // pieces.  In priority order:
+      //   op(k): QRDY(k)   chain(n): op(n) issued, SRDY(n), MRDY(n)
+      //   m(k): CWD(k)     q(k): M(k) issued, OFREE(k-1)
       //   W(k): TFULL(k), MRDY(k-1)   U(k): after W(k), VFULL(k)   (they release the T tiles)
-      //   G(k) halves: FULL(k), GFREE(k-1)              (the UT solve is the long pole)
-      //   m(k): CWD(k)   q(k): M(k), W/U(k) issued, OFREE(k-1)   op(k): QRDY(k)
-      //   chain(n): SRDY(n), MRDY(n), O-part(n) issued
+      //   G(k) halves: FULL(k), GFREE(k-1)
       constexpr uint32_t id_g = idesc_bf16(128, 64, false, false);
       int c_ch = 0, c_op = 0, c_q = 0, c_m = 0, c_w = 0, c_u = 0, c_g2 = 0;
       uint32_t idle = 0, nap = 16;
       while (c_ch < NT) {
-        if (c_w < NT && c_w == c_u && rdy(B_TFULL, c_w) && (c_w == 0 || rdy(B_MRDY, c_w - 1))) {
+        if (c_op < c_q && rdy(B_QRDY, c_op)) {
+          // ---- O^T = U^T P^T (first part of the output) ----
+          const int m = c_op++;
+          tc_fence_after();
+          const uint32_t pb = a_p + (m & 1) * 8192;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + TM_O, tmem + TM_UB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_op, k > 0);
+          mma_commit(sm.bar(B_PFREE0 + (m & 1)));
+        } else if (c_ch < c_op && rdy(B_SRDY, c_ch) && rdy(B_MRDY, c_ch)) {
+          // ---- the state step and the rest of O(n) ----
+          const int n = c_ch++;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + TM_S, tmem + TM_SBF + k * 8, sdesc_sw128(a_ms + k * 2048, 16384, 1024), id_s, true);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_S, tmem + TM_UB + k * 8, kd_desc(n, k), id_s, true);
+          mma_commit(sm.bar(B_SFULL));
+          const uint32_t st = smem_u32(sm.stage(n % NS));
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t qa = st + (k < 4 ? ST_Q0 : ST_Q1) + (k & 3) * 32;
+            mma_ts(tmem + TM_O, tmem + TM_SBF + k * 8, sdesc_sw128(qa, 0, 1024), id_o, true);
+          }
+          mma_commit(sm.bar(B_OFULL));
+          mma_commit(sm.bar(B_EMPTY + n % NS));
+        } else if (c_m < c_u && rdy(B_CWD, c_m)) {
+          // ---- (M-I)^T = -W^T Kd ----
+          const int m = c_m++;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_X1, tmem + TM_WB + k * 8, kd_desc(m, k), id_m, k > 0);
+          mma_commit(sm.bar(B_MFULL));
+        } else if (c_q < c_m && (c_q == 0 || rdy(B_OFREE, c_q - 1))) {
+          // ---- -W^T P^T (the rest of Q' is added on the CUDA cores) ----
+          const int m = c_q++;
+          tc_fence_after();
+          const uint32_t pb = a_p + (m & 1) * 8192;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + TM_O, tmem + TM_WB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_q, k > 0);
+          mma_commit(sm.bar(B_QFULL));
+        } else if (c_w < NT && c_w == c_u && rdy(B_TFULL, c_w) && (c_w == 0 || rdy(B_MRDY, c_w - 1))) {
           // ---- W^T = K^T (T diag exp gc)^T ----
           const int m = c_w++;
           tc_fence_after();
@@ -667,49 +727,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mma_ss(tmem + TM_G, sdesc_sw128(kq + k * 32, 0, 1024), sdesc_sw128(kq + k * 32, 0, 1024), id_g,
                    hf > 0 || k > 0);
           if (hf) mma_commit(sm.bar(B_GFULL));
-        } else if (c_m < c_u && rdy(B_CWD, c_m)) {
-          // ---- (M-I)^T = -W^T Kd ----
-          const int m = c_m++;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_X1, tmem + TM_WB + k * 8, kd_desc(m, k), id_m, k > 0);
-          mma_commit(sm.bar(B_MFULL));
-        } else if (c_q < c_m && (c_q == 0 || rdy(B_OFREE, c_q - 1))) {
-          // ---- -W^T P^T (the rest of Q' is added on the CUDA cores) ----
-          const int m = c_q++;
-          tc_fence_after();
-          const uint32_t pb = a_p + (m & 1) * 8192;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_O, tmem + TM_WB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_q, k > 0);
-          mma_commit(sm.bar(B_QFULL));
-        } else if (c_op < c_q && rdy(B_QRDY, c_op)) {
-          // ---- O^T = U^T P^T (first part of the output) ----
-          const int m = c_op++;
-          tc_fence_after();
-          const uint32_t pb = a_p + (m & 1) * 8192;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_O, tmem + TM_UB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_op, k > 0);
-          mma_commit(sm.bar(B_PFREE0 + (m & 1)));
-        } else if (c_ch < c_op && rdy(B_SRDY, c_ch) && rdy(B_MRDY, c_ch)) {
-          // ---- the state step and the rest of O(n) ----
-          const int n = c_ch++;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + TM_S, tmem + TM_SBF + k * 8, sdesc_sw128(a_ms + k * 2048, 16384, 1024), id_s, true);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_S, tmem + TM_UB + k * 8, kd_desc(n, k), id_s, true);
-          mma_commit(sm.bar(B_SFULL));
-          const uint32_t st = smem_u32(sm.stage(n % NS));
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t qa = st + (k < 4 ? ST_Q0 : ST_Q1) + (k & 3) * 32;
-            mma_ts(tmem + TM_O, tmem + TM_SBF + k * 8, sdesc_sw128(qa, 0, 1024), id_o, true);
-          }
-          mma_commit(sm.bar(B_OFULL));
-          mma_commit(sm.bar(B_EMPTY + n % NS));
         } else {
           // nothing ready: back off (exponentially, so that the polling
           // leaves the issue slots of this SM sub-partition to the solve),
@@ -1025,32 +1042,45 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       wait_bar(sm, B_QFULL, c & 1, 4);
       tc_fence_after();
       {
-        // element (row, column L) of the tile: row / 8 * 1024 + off[row % 8]
-        uint8_t *qt = sm.stage(s) + ((L >> 6) ? ST_Q1 : ST_Q0);
-        const int c8 = (L & 63) >> 3, ce = (L & 7) * 2;
-        uint32_t off[8];
+        // Warp-MMA fragments throughout: the tile of this warp (d = 32 q4 ..
+        // 32 q4 + 31, all 64 rows) goes in 8x8 pieces; a thread holds the
+        // pairs (d = t / 4 (+ 8), rows 8 g + 2 (t % 4), + 1) of TMEM, of Q
+        // (transposing 8x8 loads) and of Q' (transposing 8x8 stores, to the
+        // addresses the loads came from)
+        const int tq = lane & 3;
+        float2 gv[8];
 #pragma unroll
-        for (int bb = 0; bb < 8; ++bb) off[bb] = bb * 128 + ((c8 ^ bb) << 4) + ce;
+        for (int g = 0; g < 8; ++g)
+          gv[g] = GATED ? *reinterpret_cast<const float2 *>(gq + 8 * g + 2 * tq) : make_float2(1.f, 1.f);
         const int cp = rw.Cp;
-        // 16 rows at a time: every load of a batch issues before its stores
-#pragma unroll 1
-        for (int b16 = 0; b16 < 64; b16 += 16) {
-          uint32_t z[16];
-          tmem_ld16(tmem_addr(tmem + TM_O, q4 * 32, b16), z);
-          uint8_t *qb = qt + (b16 >> 3) * 1024;
-          __nv_bfloat16 *e[16];
-          float qv[16];
+        const uint32_t qh = smem_u32(sm.stage(s) + ((q4 >> 1) ? ST_Q1 : ST_Q0));
+        const int mi = lane >> 3, mr = lane & 7;  // the 8x8 piece and row this lane addresses
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            e[j] = reinterpret_cast<__nv_bfloat16 *>(qb + (j >> 3) * 1024 + off[j & 7]);
-            qv[j] = __bfloat162float(*e[j]);
+        for (int b16 = 0; b16 < 32; b16 += 16) {
+          uint32_t hreg[32];
+          tmem_ld16x256b_x8(tmem_addr(tmem + TM_O, q4 * 32 + b16, 0), hreg);
+          tmem_wait_ld_regs(hreg);
+          const int ck = (32 * (q4 & 1) + b16) / 8 + (mi & 1);  // 16-byte piece of the row
+          // all loads of this half first (the stores go to the same places)
+          uint32_t addr[4], qd[4][4];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int row = 16 * cc + 8 * (mi >> 1) + mr;
+            addr[cc] = qh + (row >> 3) * 1024 + (row & 7) * 128 + ((ck ^ (row & 7)) << 4);
+            ldsm_x4_trans(addr[cc], qd[cc]);
           }
-          tmem_wait_ld_regs(z);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int rr = b16 + j;
-            const float v = GATED ? fmaf(gq[rr], qv[j], __uint_as_float(z[j])) : qv[j] + __uint_as_float(z[j]);
-            *e[j] = __float2bfloat16_rn(rr < cp ? v : 0.f);
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int g = 2 * cc + (m >> 1), j = 4 * g + 2 * (m & 1);
+              const int r0 = 8 * g + 2 * tq;
+              const float v0 = fmaf(gv[g].x, __uint_as_float(qd[cc][m] << 16), __uint_as_float(hreg[j]));
+              const float v1 = fmaf(gv[g].y, __uint_as_float(qd[cc][m] & 0xFFFF0000u), __uint_as_float(hreg[j + 1]));
+              o4[m] = pack_bf16(r0 < cp ? v0 : 0.f, r0 + 1 < cp ? v1 : 0.f);
+            }
+            stsm_x4_trans(addr[cc], o4);
           }
         }
         tc_fence_before();
@@ -1117,24 +1147,60 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int u = 0; u < 32; ++u) hT[(size_t)(c0 + u) * D + L] = __uint_as_float(r[u]);
         }
       }
-      // ---- outputs of this chunk: the accumulator is read at once (so that
-      //      TMEM is released early), then one bf16 per readout row: the 32
-      //      lanes of a warp write 32 consecutive value columns of the row ----
+      // ---- outputs of this chunk: the accumulator is read at once (TMEM is
+      //      released early), staged as bf16 rows in the V slot of this chunk
+      //      (its last reader, the U product or, gated, the state step on Kd,
+      //      has completed) by transposing 8x8 stores, then written out in
+      //      16-byte pieces ----
       wait_bar(sm, B_OFULL, n & 1, 4);
       tc_fence_after();
-      uint32_t o[64];
-      tmem_ld32(tmem_addr(tmem + TM_O, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&o[0]));
-      tmem_ld32(tmem_addr(tmem + TM_O, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&o[32]));
-      tmem_wait_ld_regs(o);
+      uint32_t o0[32], o1[32];
+      tmem_ld16x256b_x8(tmem_addr(tmem + TM_O, q4 * 32, 0), o0);
+      tmem_ld16x256b_x8(tmem_addr(tmem + TM_O, q4 * 32 + 16, 0), o1);
+      tmem_wait_ld_regs(o0);
+      tmem_wait_ld_regs(o1);
       tc_fence_before();
       arrive_warp(sm.bar(B_OFREE), lane);
       {
-        __nv_bfloat16 *orow = p.out + (((size_t)b * p.T + rw.t_lo) * p.H + h) * D + L;
-        const size_t rstride = (size_t)p.H * D;
-        const int cp = rw.Cp;
+        // staging row r (a readout row): 256 bytes, the 16-byte piece k
+        // (values 8 k .. 8 k + 7) at (k ^ (r % 8)) * 16
+        const uint32_t sv = smem_u32(sm.stage(n % NS) + ST_V0);
+        auto srow = [&](int r) -> uint32_t { return sv + r * 256; };
+        const int mi = lane >> 3, mr = lane & 7;
 #pragma unroll
-        for (int rr = 0; rr < 64; ++rr)
-          if (rr < cp) orow[rr * rstride] = __float2bfloat16_rn(__uint_as_float(o[rr]));
+        for (int b16 = 0; b16 < 32; b16 += 16) {
+          const uint32_t(&ov)[32] = b16 ? o1 : o0;
+          const int k = (32 * q4 + b16) / 8 + (mi & 1);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int j = 4 * (2 * cc + (m >> 1)) + 2 * (m & 1);
+              o4[m] = pack_bf16(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]));
+            }
+            const int r = 16 * cc + 8 * (mi >> 1) + mr;
+            stsm_x4_trans(srow(r) + ((k ^ (r & 7)) << 4), o4);
+          }
+        }
+        named_sync(3);  // every value column of every row staged
+        const int ct = tid - 320;  // 0..127 within the group
+        const int k = ct & 15, cp = rw.Cp;
+        __nv_bfloat16 *obase = p.out + (((size_t)b * p.T + rw.t_lo) * p.H + h) * D + 8 * k;
+        const size_t rstride = (size_t)p.H * D;
+        uint4 v[8];  // every load before the first store
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int r = 8 * it + (ct >> 4);
+          v[it] = lds128(srow(r) + ((k ^ (r & 7)) << 4));
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int r = 8 * it + (ct >> 4);
+          if (r < cp) *reinterpret_cast<uint4 *>(obase + r * rstride) = v[it];
+        }
+        // the V slot is free once every warp has read its rows
+        arrive_warp(sm.bar(B_VEMPTY + n % NS), lane);
       }
       if (n + 1 < NT) qprime(n + 1);
     }

@@ -179,6 +179,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// 16 lanes x 64 columns in the warp-MMA accumulator layout (shape 16x256b,
+// 8 repeats along the columns): thread t, register 4 g + j holds lane
+// base + t / 4 + 8 (j / 2), column 8 g + 2 (t % 4) + (j % 2).  `base` (the
+// lane field of taddr) is the warp's lane quarter start or 16 past it.
+__device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32"
@@ -278,6 +296,24 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
       : "memory");
+}
+
+// ---------------------------------------------------------------- 8x8 b16 tiles
+// Four 8x8 tiles of 16-bit elements between shared memory and registers; lanes
+// 8 m .. 8 m + 7 give the addresses of the eight 16-byte rows of tile m.  In
+// registers, thread t holds of tile m the pair (row t / 4, columns 2 (t % 4),
+// 2 (t % 4) + 1) of the tile as seen in registers, lower column in the low
+// half.  The .trans forms exchange rows and columns between the two sides.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&d)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+               : "r"(saddr)
+               : "memory");
+}
+__device__ __forceinline__ void stsm_x4_trans(uint32_t saddr, const uint32_t (&s)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr),
+               "r"(s[0]), "r"(s[1]), "r"(s[2]), "r"(s[3])
+               : "memory");
 }
 
 // ---------------------------------------------------------------- misc
