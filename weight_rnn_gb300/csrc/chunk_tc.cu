@@ -795,39 +795,54 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       tc_fence_after();
       {
         const int i = L, r = L - 64;
-        const float bi = L < 64 ? sb[i] : 0.f;
-        const float gi = (GATED && L < 64) ? AX[swz(i, i)] : 0.f;
-        const float bie = (GATED && L < 64) ? bi * eg[i] : bi;
-        const int pos = (L >= 64 && r < rw.Cp) ? rw.pos(r, n_h) : -1;
+        const bool arow = L < 64;
+        const float bi = arow ? sb[i] : 0.f;
+        const float gi = (GATED && arow) ? AX[swz(i, i)] : 0.f;
+        const float bie = (GATED && arow) ? bi * eg[i] : bi;
+        const int pos = (!arow && r < rw.Cp) ? rw.pos(r, n_h) : -1;
         const float gp = (GATED && pos >= 0) ? AX[swz(pos, pos)] : 0.f;
         const float ep = (GATED && pos >= 0) ? eg[pos] : 1.f;
+        // entry (row, j) = G(row, j) * f_j: f_j = bx (ungated); rf 2^-gc_j
+        // (the ratio form, while the chunk's gate product stays in range);
+        // else bx 2^(gr - gc_j) exactly.  The branch is uniform per chunk.
+        const float bx = arow ? bi : 1.f, rf = arow ? bie : ep, gr = arow ? gi : gp;
         uint8_t *prow = sm.base + OFF_P + (m & 1) * 8192;
 #pragma unroll 1
         for (int jb = 0; jb < 64; jb += 16) {
           uint32_t g[16];
           tmem_ld16(tmem_addr(tmem + TM_G, q4 * 32, jb), g);
+          float cf[16];
+          if (!GATED) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) cf[jj] = bx;
+          } else if (ratio) {
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4) {
+              const float4 e4 = *reinterpret_cast<const float4 *>(ieg + jb + jj);
+              cf[jj] = rf * e4.x;
+              cf[jj + 1] = rf * e4.y;
+              cf[jj + 2] = rf * e4.z;
+              cf[jj + 3] = rf * e4.w;
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) cf[jj] = bx * fast_exp2(gr - AX[swz(jb + jj, jb + jj)]);
+          }
           tmem_wait_ld_regs(g);
-          if (L < 64) {
+          if (arow) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int j = jb + jj;
-              if (j < i) {
-                const float f = !GATED ? bi : (ratio ? bie * ieg[j] : bi * fast_exp2(gi - AX[swz(j, j)]));
-                AX[swz(j, i)] = f * __uint_as_float(g[jj]);
-              }
+              if (j < i) AX[swz(j, i)] = cf[jj] * __uint_as_float(g[jj]);
             }
           } else {
             uint32_t pk[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              float v[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int j = jb + 2 * u + e;
-                const float f = !GATED ? 1.f : (ratio ? ep * ieg[j] : fast_exp2(gp - AX[swz(j, j)]));
-                v[e] = j <= pos ? __uint_as_float(g[2 * u + e]) * f : 0.f;
-              }
-              pk[u] = pack_bf16(v[0], v[1]);
+              const int j = jb + 2 * u;
+              const float v0 = j <= pos ? __uint_as_float(g[2 * u]) * cf[2 * u] : 0.f;
+              const float v1 = j + 1 <= pos ? __uint_as_float(g[2 * u + 1]) * cf[2 * u + 1] : 0.f;
+              pk[u] = pack_bf16(v0, v1);
             }
             st_chunk(prow + sw128_offset(r, jb, 64), {pk[0], pk[1], pk[2], pk[3]});
             st_chunk(prow + sw128_offset(r, jb + 8, 64), {pk[4], pk[5], pk[6], pk[7]});
