@@ -46,8 +46,9 @@
 //   warps 2-5    prep (chunk n+2): G -> A, P -> UT solve -> T tiles
 //   warps 6-9    feed-forward (chunk n+1): W^T, U^T -> bf16 TMEM operands,
 //                Kd, (M-I)^T -> smem operand
-//   warps 10-13  chain (chunk n): S^T -> bf16 operand, output epilogue, hT;
-//                then Q' of chunk n+1 -> smem operand
+//   warps 10-13  chain (chunk n): S^T -> bf16 operand, the outputs (staged
+//                through the V slot by transposing 8x8 stores), hT; then Q'
+//                of chunk n+1 -> smem operand, in the same fragment layout
 // Every mbarrier wait is bounded; a timeout sets a device error word and the
 // kernel winds down instead of hanging.
 #include <cuda_bf16.h>
