@@ -123,6 +123,27 @@ int delta_check_device(void);
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int delta_version(void);
 
+/*
+ * delta_inject_failure -- test hook: the next `count` calls of delta_fwd and
+ * delta_step (together) return DELTA_ERR_CUDA, with "injected failure" in
+ * delta_last_error(), right after their arguments pass validation and before
+ * anything is enqueued.  count = 0 clears a pending injection; count < 0 is
+ * DELTA_ERR_INVALID.  The counter is process-wide.
+ */
+int delta_inject_failure(int count);
+
+/*
+ * delta_selftest_wait -- diagnostic: enqueues one warp on `stream` that
+ * waits, giving up after `polls` (1 .. 2^24) tries, on a shared-memory
+ * barrier that nothing completes -- the bounded-wait path every library
+ * kernel takes when a hand-off never arrives.  It gives up and records role
+ * 7, barrier 253 in the device error word; the next delta_check_device()
+ * returns DELTA_ERR_CUDA and clears it.  Nothing faults, and the context stays
+ * usable.  Returns DELTA_ERR_INVALID for polls out of range, DELTA_ERR_CUDA
+ * if the launch fails.
+ */
+int delta_selftest_wait(int polls, struct CUstream_st *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -131,3 +131,26 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(wr, "library_path", lambda: str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         wr.load_library()
+
+
+def test_injected_failure_returns_before_launch(lib):
+    """The host-side failure hook: after validation, before any CUDA call
+    (the fake pointers are never touched), the caller sees DELTA_ERR_CUDA."""
+    try:
+        assert lib.delta_inject_failure(-1) == wr.DELTA_ERR_INVALID
+        assert lib.delta_inject_failure(2) == wr.DELTA_OK
+        assert fwd(lib) == wr.DELTA_ERR_CUDA
+        assert "injected" in wr.delta_last_error()
+        assert step(lib) == wr.DELTA_ERR_CUDA
+        assert "injected" in wr.delta_last_error()
+        # validation comes first and does not use up an injection
+        assert lib.delta_inject_failure(1) == wr.DELTA_OK
+        assert fwd(lib, dk=48) == wr.DELTA_ERR_UNSUPPORTED
+        assert fwd(lib) == wr.DELTA_ERR_CUDA
+    finally:
+        lib.delta_inject_failure(0)
+
+
+def test_selftest_wait_rejects_bad_poll_counts(lib):
+    assert lib.delta_selftest_wait(0, None) == wr.DELTA_ERR_INVALID
+    assert lib.delta_selftest_wait((1 << 24) + 1, None) == wr.DELTA_ERR_INVALID

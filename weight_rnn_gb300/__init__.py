@@ -16,7 +16,7 @@ import threading
 import torch
 
 __all__ = ["delta_fwd", "delta_step", "delta_status_string", "delta_last_error",
-           "delta_check_device",
+           "delta_check_device", "delta_inject_failure", "delta_selftest_wait",
            "delta_version", "DeltaError", "library_path", "load_library",
            "DELTA_OK", "DELTA_ERR_INVALID", "DELTA_ERR_UNSUPPORTED",
            "DELTA_ERR_ALIGN", "DELTA_ERR_CUDA", "DELTA_F32", "DELTA_BF16",
@@ -32,7 +32,8 @@ DELTA_BF16 = 1
 
 #: every extern "C" entry point include/delta.h declares
 EXPORTED_SYMBOLS = ("delta_fwd", "delta_step", "delta_status_string",
-                    "delta_last_error", "delta_check_device", "delta_version")
+                    "delta_last_error", "delta_check_device", "delta_version",
+                    "delta_inject_failure", "delta_selftest_wait")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -76,6 +77,10 @@ def load_library():
         lib.delta_version.argtypes = []
         lib.delta_check_device.restype = i
         lib.delta_check_device.argtypes = []
+        lib.delta_inject_failure.restype = i
+        lib.delta_inject_failure.argtypes = [i]
+        lib.delta_selftest_wait.restype = i
+        lib.delta_selftest_wait.argtypes = [i, ctypes.c_void_p]
         _lib = lib
         return lib
 
@@ -96,6 +101,24 @@ def delta_check_device() -> None:
     """Synchronise the device and raise DeltaError if a library kernel gave up
     on one of its bounded internal waits since the last check."""
     st = load_library().delta_check_device()
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+
+
+def delta_inject_failure(count: int) -> None:
+    """Test hook: the next ``count`` delta_fwd / delta_step calls fail with
+    DELTA_ERR_CUDA after validating their arguments, before any launch."""
+    st = load_library().delta_inject_failure(int(count))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+
+
+def delta_selftest_wait(polls: int = 1000, stream=None, device=None) -> None:
+    """Enqueue one warp that gives up on a barrier nothing completes (after
+    ``polls`` tries) and records that in the device error word, which the
+    next delta_check_device() reports."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    st = load_library().delta_selftest_wait(int(polls), _stream(dev, stream))
     if st != DELTA_OK:
         raise DeltaError(st, delta_last_error())
 

@@ -4,6 +4,7 @@
 // stream and returns.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstdarg>
@@ -15,6 +16,16 @@
 namespace {
 
 thread_local char g_last_error[256] = "no error";
+// calls still to fail on purpose (delta_inject_failure)
+std::atomic<int> g_inject{0};
+
+// true (and one injection used up) when this call is to fail on purpose
+bool take_injection() {
+  int n = g_inject.load();
+  while (n > 0)
+    if (g_inject.compare_exchange_weak(n, n - 1)) return true;
+  return false;
+}
 
 int fail(int status, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int status, const char *fmt, ...) {
@@ -63,6 +74,18 @@ const char *delta_status_string(int status) {
 const char *delta_last_error(void) { return g_last_error; }
 
 int delta_version(void) { return 100; }
+
+int delta_inject_failure(int count) {
+  if (count < 0) return fail(DELTA_ERR_INVALID, "count=%d is negative", count);
+  g_inject.store(count);
+  return DELTA_OK;
+}
+
+int delta_selftest_wait(int polls, struct CUstream_st *stream) {
+  if (polls < 1 || polls > (1 << 24)) return fail(DELTA_ERR_INVALID, "polls=%d not in [1, 2^24]", polls);
+  const cudaError_t err = delta::launch_wait_selftest((unsigned)polls, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "wait self-test launch");
+}
 
 int delta_check_device(void) {
   unsigned int word = 0;
@@ -115,6 +138,8 @@ int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
   if (hT && h0 && (const void *)hT != (const void *)h0 && overlap(r_hT, inputs[5]))
     return fail(DELTA_ERR_INVALID, "hT partially overlaps h0");
 
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+
   delta::FwdArgs a;
   a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.h0 = h0;
   a.out = out; a.hT = hT;
@@ -165,6 +190,8 @@ int delta_step(const void *q, const void *k, const void *v, const float *beta,
     if (overlap(r_state, r)) return fail(DELTA_ERR_INVALID, "state overlaps an input");
   }
   if (overlap(r_state, r_out)) return fail(DELTA_ERR_INVALID, "state overlaps out");
+
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
 
   delta::StepArgs a;
   a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.state = state; a.out = out;

@@ -1238,6 +1238,28 @@ bool chunk_tc_supports(const FwdArgs &a) {
          a.L < (int64_t(1) << 30) && a.B * a.H < (int64_t(1) << 31);
 }
 
+namespace {
+// The bounded-wait path on its own: a barrier nobody arrives on.
+__global__ void wait_selftest_kernel(unsigned int polls) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    sm100::mbar_init(&bar, 1);
+    sm100::fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    bool done = false;
+    for (unsigned int i = 0; i < polls && !done; ++i) done = sm100::mbar_try_wait(&bar, 0);
+    if (!done) atomicCAS(&g_tc_error, 0u, (1u + 7u) | (253u << 8));
+  }
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(unsigned int polls, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(polls);
+  return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_tc_error(unsigned int *word) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return e;

@@ -43,6 +43,10 @@ bool chunk_tc_supports(const FwdArgs &a);
 // waits gives up (0 = no error).  Synchronises the device.
 cudaError_t read_and_clear_tc_error(unsigned int *word);
 
+// One warp waits, at most `polls` tries, on a barrier that nothing completes,
+// then records its giving up in the same device error word.
+cudaError_t launch_wait_selftest(unsigned int polls, cudaStream_t s);
+
 // hT <- h0 (or 0) for an empty sequence (T == 0).
 cudaError_t launch_state_passthrough(const FwdArgs &a, cudaStream_t s);
 
