@@ -39,10 +39,11 @@
 // W, U, T, M, Q' and P never leave the SM.  HBM traffic is q, k, v, beta, g
 // in and out, h0/hT once per head.
 //
-// Warp roles (448 threads, one CTA per (b, h) head):
+// Warp roles (448 threads ungated, 480 gated; one CTA per (b, h) head):
 //   warp 0       TMA producer: K/Q/V tiles (128-byte swizzle, 3 stages, the
 //                chunk after them prefetched into L2) + beta / log-gate rows
-//   warp 1       TMEM owner and the single MMA-issuing thread
+//   warp 1       TMEM owner and MMA issuer (gated: the state-recurrence
+//                products; warp 14 issues the look-ahead W, U, G products)
 //   warps 2-5    prep (chunk n+2): G -> A, P -> UT solve -> T tiles
 //   warps 6-9    feed-forward (chunk n+1): W^T, U^T -> bf16 TMEM operands,
 //                Kd, (M-I)^T -> smem operand
@@ -68,7 +69,9 @@ using namespace sm100;
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr int NS = 3;  // TMA stages
-constexpr int kThreads = 448;
+// Gated, a second MMA-issuing warp (14) takes the look-ahead products; the
+// ungated step keeps one issuer and its priority order (measured faster)
+__host__ __device__ constexpr int threads_for(bool gated) { return gated ? 480 : 448; }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLogGateFloor = -80.0f;
 // Down to this cumulative log2 gate within a chunk the decay factors are
@@ -491,7 +494,7 @@ struct Rows {
 
 // 14 warps: at most 4 per SM sub-partition, so 128 registers per thread
 template <bool GATED>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(GATED), 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -514,7 +517,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   // ---- set-up: zero shared memory, init barriers, allocate TMEM ----
   {
     uint4 *z = reinterpret_cast<uint4 *>(sm.base);
-    for (uint32_t i = tid; i < SMEM_TOTAL / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    for (uint32_t i = tid; i < SMEM_TOTAL / 16; i += threads_for(GATED)) z[i] = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   if (tid == 0) {
@@ -523,7 +526,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(sm.bar(B_EMPTY + s), 1);
       mbar_init(sm.bar(B_VEMPTY + s), 4);
     }
-    const int cnt[B_VFULL - 2 * NS] = {1, 4, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, 1};
+    const int cnt[B_VFULL - 2 * NS] = {1, 4, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, GATED ? 2 : 1};
     for (int i = 2 * NS; i < B_VFULL; ++i) mbar_init(sm.bar(i), cnt[i - 2 * NS]);
     for (int s = 0; s < NS; ++s) mbar_init(sm.bar(B_VFULL + s), 1);
     *sm.abort_flag() = 0;
@@ -621,8 +624,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         wait_bar(sm, B_VFULL + n % NS, (n / NS) & 1, 0);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ===================================================== MMA issuer
+  } else if (warp == 1 || (GATED && warp == 14)) {
+    // ===================================================== MMA issuers
+    // Gated: warp 1 issues the products on the state recurrence (op, the
+    // state step with the rest of the output, M, the Q' helper) and warp 14
+    // the look-ahead products for later chunks (W, U, G).  Each commits the
+    // barriers of its own products; the hand-offs between the two kinds are
+    // barriers already.  Ungated: warp 1 issues everything.
+    const bool crit = warp == 1, look = !GATED || warp == 14;
     if (lane == 0) {
       constexpr uint32_t id_uw = idesc_bf16(128, 64, true, false);
       constexpr uint32_t id_m = idesc_bf16(128, 128, false, true, true);  // B = Kd, MN-major, negated
@@ -652,8 +661,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       constexpr uint32_t id_g = idesc_bf16(128, 64, false, false);
       int c_ch = 0, c_op = 0, c_q = 0, c_m = 0, c_w = 0, c_u = 0, c_g2 = 0;
       uint32_t idle = 0, nap = 16;
-      while (c_ch < NT) {
-        if (c_op < c_q && rdy(B_QRDY, c_op)) {
+      while (crit ? c_ch < NT : (c_u < NT || c_g2 < 2 * NT)) {
+        if (crit && c_op < c_q && rdy(B_QRDY, c_op)) {
           // ---- O^T = U^T P^T (first part of the output) ----
           const int m = c_op++;
           tc_fence_after();
@@ -662,7 +671,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int k = 0; k < 4; ++k)
             mma_ts(tmem + TM_O, tmem + TM_UB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_op, k > 0);
           mma_commit(sm.bar(B_PFREE0 + (m & 1)));
-        } else if (c_ch < c_op && rdy(B_SRDY, c_ch) && rdy(B_MRDY, c_ch)) {
+        } else if (crit && c_ch < c_op && rdy(B_SRDY, c_ch) && rdy(B_MRDY, c_ch)) {
           // ---- the state step and the rest of O(n) ----
           const int n = c_ch++;
           tc_fence_after();
@@ -680,14 +689,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           }
           mma_commit(sm.bar(B_OFULL));
           mma_commit(sm.bar(B_EMPTY + n % NS));
-        } else if (c_m < c_u && rdy(B_CWD, c_m)) {
+        } else if (crit && (GATED ? c_m < NT : c_m < c_u) && rdy(B_CWD, c_m)) {  // CWD(m): U(m) done, converted
           // ---- (M-I)^T = -W^T Kd ----
           const int m = c_m++;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_X1, tmem + TM_WB + k * 8, kd_desc(m, k), id_m, k > 0);
           mma_commit(sm.bar(B_MFULL));
-        } else if (c_q < c_m && (c_q == 0 || rdy(B_OFREE, c_q - 1))) {
+        } else if (crit && c_q < c_m && (c_q == 0 || rdy(B_OFREE, c_q - 1))) {
           // ---- -W^T P^T (the rest of Q' is added on the CUDA cores) ----
           const int m = c_q++;
           tc_fence_after();
@@ -696,7 +705,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int k = 0; k < 4; ++k)
             mma_ts(tmem + TM_O, tmem + TM_WB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_q, k > 0);
           mma_commit(sm.bar(B_QFULL));
-        } else if (c_w < NT && c_w == c_u && rdy(B_TFULL, c_w) && (c_w == 0 || rdy(B_MRDY, c_w - 1))) {
+        } else if (look && c_w < NT && c_w == c_u && rdy(B_TFULL, c_w) && (c_w == 0 || rdy(B_MRDY, c_w - 1))) {
           // ---- W^T = K^T (T diag exp gc)^T ----
           const int m = c_w++;
           tc_fence_after();
@@ -705,7 +714,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_X1, sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024),
                    sdesc_sw128(a_tw + k * 32, 0, 1024), id_uw, k > 0);
-        } else if (c_u < c_w && rdy(B_VFULL + c_u % NS, c_u / NS)) {
+        } else if (look && c_u < c_w && rdy(B_VFULL + c_u % NS, c_u / NS)) {
           // ---- U^T = V^T T^T ----
           const int m = c_u++;
           tc_fence_after();
@@ -715,7 +724,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mma_ss(tmem + TM_X1 + 64, sdesc_sw128(kq + ST_V0 + k * 2048, 8192, 1024),
                    sdesc_sw128(a_tu + k * 32, 0, 1024), id_uw, k > 0);
           mma_commit(sm.bar(B_WFULL));
-        } else if (c_g2 < 2 * NT && ((c_g2 & 1) ||
+        } else if (look && c_g2 < 2 * NT && ((c_g2 & 1) ||
                                      (rdy(B_FULL + (c_g2 >> 1) % NS, (c_g2 >> 1) / NS) &&
                                       (c_g2 == 0 || rdy(B_GFREE, (c_g2 >> 1) - 1))))) {
           // ---- G = [K;Q] K^T, one 64-column half of the K dimension ----
@@ -744,7 +753,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         idle = 0;
         nap = 16;
       }
-      mma_commit(sm.bar(B_DRAIN));
+      mma_commit(sm.bar(B_DRAIN));  // every issuer arrives
       wait_bar(sm, B_DRAIN, 0, 1);
     }
     __syncwarp();
@@ -1291,7 +1300,7 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, cudaStream_t s) {
   auto kern = a.g ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)(a.B * a.H), kThreads, SMEM_ALLOC, s>>>(mq, mk, mv, p);
+  kern<<<(unsigned)(a.B * a.H), threads_for(a.g != nullptr), SMEM_ALLOC, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
