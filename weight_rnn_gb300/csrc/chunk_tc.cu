@@ -71,7 +71,10 @@ constexpr int D = 128;
 constexpr int NS = 3;  // TMA stages
 // Gated, a second MMA-issuing warp (14) takes the look-ahead products; the
 // ungated step keeps one issuer and its priority order (measured faster)
-__host__ __device__ constexpr int threads_for(bool gated) { return gated ? 480 : 448; }
+__host__ __device__ constexpr bool dual_issue(bool gated) { return gated; }
+__host__ __device__ constexpr bool look_wu(bool gated) { return true; }  // W, U on warp 14
+__host__ __device__ constexpr bool look_g(bool gated) { return true; }   // G on warp 14
+__host__ __device__ constexpr int threads_for(bool gated) { return dual_issue(gated) ? 480 : 448; }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLogGateFloor = -80.0f;
 // Down to this cumulative log2 gate within a chunk the decay factors are
@@ -526,7 +529,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(sm.bar(B_EMPTY + s), 1);
       mbar_init(sm.bar(B_VEMPTY + s), 4);
     }
-    const int cnt[B_VFULL - 2 * NS] = {1, 4, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, GATED ? 2 : 1};
+    const int cnt[B_VFULL - 2 * NS] = {1, 4, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, dual_issue(GATED) ? 2 : 1};
     for (int i = 2 * NS; i < B_VFULL; ++i) mbar_init(sm.bar(i), cnt[i - 2 * NS]);
     for (int s = 0; s < NS; ++s) mbar_init(sm.bar(B_VFULL + s), 1);
     *sm.abort_flag() = 0;
@@ -624,14 +627,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         wait_bar(sm, B_VFULL + n % NS, (n / NS) & 1, 0);
     }
     __syncwarp();
-  } else if (warp == 1 || (GATED && warp == 14)) {
+  } else if (warp == 1 || (dual_issue(GATED) && warp == 14)) {
     // ===================================================== MMA issuers
     // Gated: warp 1 issues the products on the state recurrence (op, the
     // state step with the rest of the output, M, the Q' helper) and warp 14
     // the look-ahead products for later chunks (W, U, G).  Each commits the
     // barriers of its own products; the hand-offs between the two kinds are
     // barriers already.  Ungated: warp 1 issues everything.
-    const bool crit = warp == 1, look = !GATED || warp == 14;
+    constexpr bool kDual = dual_issue(GATED);
+    const bool crit = warp == 1;
+    // which thread issues the look-ahead kinds
+    const bool do_wu = !kDual || (look_wu(GATED) ? warp == 14 : crit);
+    const bool do_g = !kDual || (look_g(GATED) ? warp == 14 : crit);
     if (lane == 0) {
       constexpr uint32_t id_uw = idesc_bf16(128, 64, true, false);
       constexpr uint32_t id_m = idesc_bf16(128, 128, false, true, true);  // B = Kd, MN-major, negated
@@ -661,7 +668,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       constexpr uint32_t id_g = idesc_bf16(128, 64, false, false);
       int c_ch = 0, c_op = 0, c_q = 0, c_m = 0, c_w = 0, c_u = 0, c_g2 = 0;
       uint32_t idle = 0, nap = 16;
-      while (crit ? c_ch < NT : (c_u < NT || c_g2 < 2 * NT)) {
+      while (crit ? c_ch < NT : ((do_wu && c_u < NT) || (do_g && c_g2 < 2 * NT))) {
         if (crit && c_op < c_q && rdy(B_QRDY, c_op)) {
           // ---- O^T = U^T P^T (first part of the output) ----
           const int m = c_op++;
@@ -689,7 +696,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           }
           mma_commit(sm.bar(B_OFULL));
           mma_commit(sm.bar(B_EMPTY + n % NS));
-        } else if (crit && (GATED ? c_m < NT : c_m < c_u) && rdy(B_CWD, c_m)) {  // CWD(m): U(m) done, converted
+        } else if (crit && (do_wu ? c_m < c_u : c_m < NT) && rdy(B_CWD, c_m)) {  // CWD(m): U(m) done, converted
           // ---- (M-I)^T = -W^T Kd ----
           const int m = c_m++;
           tc_fence_after();
@@ -705,7 +712,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int k = 0; k < 4; ++k)
             mma_ts(tmem + TM_O, tmem + TM_WB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_q, k > 0);
           mma_commit(sm.bar(B_QFULL));
-        } else if (look && c_w < NT && c_w == c_u && rdy(B_TFULL, c_w) && (c_w == 0 || rdy(B_MRDY, c_w - 1))) {
+        } else if (do_wu && c_w < NT && c_w == c_u && rdy(B_TFULL, c_w) && (c_w == 0 || rdy(B_MRDY, c_w - 1))) {
           // ---- W^T = K^T (T diag exp gc)^T ----
           const int m = c_w++;
           tc_fence_after();
@@ -714,7 +721,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_X1, sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024),
                    sdesc_sw128(a_tw + k * 32, 0, 1024), id_uw, k > 0);
-        } else if (look && c_u < c_w && rdy(B_VFULL + c_u % NS, c_u / NS)) {
+        } else if (do_wu && c_u < c_w && rdy(B_VFULL + c_u % NS, c_u / NS)) {
           // ---- U^T = V^T T^T ----
           const int m = c_u++;
           tc_fence_after();
@@ -724,7 +731,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mma_ss(tmem + TM_X1 + 64, sdesc_sw128(kq + ST_V0 + k * 2048, 8192, 1024),
                    sdesc_sw128(a_tu + k * 32, 0, 1024), id_uw, k > 0);
           mma_commit(sm.bar(B_WFULL));
-        } else if (look && c_g2 < 2 * NT && ((c_g2 & 1) ||
+        } else if (do_g && c_g2 < 2 * NT && ((c_g2 & 1) ||
                                      (rdy(B_FULL + (c_g2 >> 1) % NS, (c_g2 >> 1) / NS) &&
                                       (c_g2 == 0 || rdy(B_GFREE, (c_g2 >> 1) - 1))))) {
           // ---- G = [K;Q] K^T, one 64-column half of the K dimension ----
