@@ -2,22 +2,32 @@
 """Throughput of the delta-rule forward on GB300, one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 2|3|4|5]
+                    [--workload all|2|3|4|5]
 
 A step is one pass of the hot path over one batch of synthetic input: one
-``delta_fwd`` call on the DeltaNet workload B8 H16 T4096 dk=dv=128 bf16,
-chunk 64 (the default; ``--workload`` 3/4 select the gated and DeltaProduct
-workloads, 5 the B256 x H32 decode step).  Inputs are resident in HBM and
-larger than L2 (403 MB of q/k/v per step for the default workload), so no
-flush is needed between steps.
+``delta_fwd`` call over a whole workload (or one ``delta_step`` call for the
+decode workload).  By default every workload runs in one invocation, each
+with W untimed warm-up steps and K timed steps:
 
-Reported besides tokens/s: the roofline of the kernel (achieved GB/s over
-algorithmic bytes vs the measured HBM peak), the end-to-end rate through the
-public API with host buffers (copies inside the timed region), the CPU
-oracle's rate on a bounded sample of the same workload, SM clocks sampled
-during the timed region, and the number of kernels launched.
+  3  Gated DeltaNet      B4 H32 T8192 dk=dv=128 bf16, chunk 64, h0   (headline)
+  2  DeltaNet            B8 H16 T4096 dk=dv=128 bf16, chunk 64
+  4  Gated DeltaProduct  B4 H16 T4096 n_h=3 dk=dv=128 bf16, chunk 64
+  5  decode step         B256 H32 dk=dv=128 n_h=2, fp32 state 512 MiB
 
-Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+The headline (``value``, ``roofline``, ``e2e``, ``cpu_baseline``) is the
+largest dk=dv=128 forward that fits one GPU, workload 3; ``per_workload``
+carries the same figures for every workload.  Inputs are resident in HBM and
+larger than L2 (129 MB) every step, so no flush is needed between steps.
+
+Reported besides tokens/s: the roofline of the step (algorithmic bytes over
+the CUDA-event time of the step's kernels vs the measured HBM peak, and vs
+the GB300's nominal 7.9 TB/s), the spread of the per-step kernel times, the
+end-to-end rate through the public API with host buffers (copies inside the
+timed region, overlapped with compute over batch slices on two streams), the
+CPU oracle's rate on the headline workload (all cores and one core), SM
+clocks sampled during the timed regions, and the number of kernels launched.
+
+Under torchrun (N > 1) every rank runs the same per-GPU workloads on its own
 GPU with its own seed (weak scaling over independent heads, no collective on
 the data path); timing is barrier-bracketed and the max over ranks is taken.
 ``--impl reference`` times the float64 CPU oracle on the host cores instead
@@ -46,6 +56,9 @@ from weight_rnn_gb300 import synth  # noqa: E402
 
 METRIC = "delta fwd tokens/s (B·H·T/s) at dk=dv=128; % of tensor/HBM roofline"
 UNIT = "tokens/s"
+HEADLINE = 3
+ORDER = (3, 2, 4, 5)
+SPEC_HBM_GBS = 7900.0  # GB300 nominal HBM3e bandwidth
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "fwd": ["weight_rnn_gb300/csrc/chunk_tc.cu", "weight_rnn_gb300/csrc/chunk_generic.cu"],
@@ -111,6 +124,17 @@ def step_bytes(w: synth.Workload) -> int:
     return n + 2 * BH * w.dk * w.dv * 4
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples while the timed region runs."""
 
@@ -149,14 +173,14 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
-                    "samples": 0}
+                    "samples": 0, "samples_under_load": 0}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
         for line in self.lines:
@@ -166,14 +190,18 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 smax.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for name, val in zip(names[1:], parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
+        # samples under load: power well above the idle floor
+        loaded = [s for s, p in zip(sm, power) if power and p > min(power) + 100.0]
+        return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "samples_under_load": len(loaded)}
 
 
 # --------------------------------------------------------------------------- dist
@@ -230,12 +258,28 @@ def oracle_sample_rate(w: synth.Workload, inp, heads: int, threads: int):
     return len(pairs) * w.T / dt, dt, len(pairs)
 
 
-def run_reference(args, w, dist):
+def cpu_baseline(w, host):
+    """The oracle on the host cores: every head with all cores, and two heads
+    on one core (extrapolated to the whole workload by head count)."""
+    threads = os.cpu_count() or 1
+    rate, dt, n = oracle_sample_rate(w, host, w.B * w.H, threads)
+    rate1, dt1, n1 = oracle_sample_rate(w, host, 2, 1)
+    return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": f"{n} of {w.B * w.H} heads x {w.T} tokens of {w.name} "
+                      f"({dt:.1f} s wall, float64, {threads} threads)",
+            "single_core": {"value": rate1, "unit": UNIT, "cores": 1,
+                            "sample": f"{n1} heads x {w.T} tokens ({dt1:.2f} s)",
+                            "whole_workload_s": w.tokens / rate1}}
+
+
+def run_reference(args, dist):
     if dist.rank != 0:
         return 0
+    w = synth.WORKLOADS[HEADLINE if args.workload == "all" else int(args.workload)]
     threads = os.cpu_count() or 1
-    inp = synth.fwd_inputs(w.with_(B=1, H=min(w.H, max(1, threads))), seed=w.seed)
     wsmall = w.with_(B=1, H=min(w.H, max(1, threads)))
+    inp = synth.fwd_inputs(wsmall, seed=w.seed)
     heads = wsmall.H
     for _ in range(args.warmup):
         oracle_sample_rate(wsmall, inp, heads, threads)
@@ -254,7 +298,7 @@ def run_reference(args, w, dist):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, args),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -281,23 +325,21 @@ def read_traffic(kind, workload_name):
         return None
     with open(path) as f:
         rec = json.load(f)
-    ent = rec.get(kind)
-    if not ent or ent.get("source_sha") != source_sha(kind):
-        return None
-    if ent.get("workload") != workload_name:
-        return None
-    return ent.get("dram_bytes_per_launch")
+    for ent in rec.get("records", []):
+        if (ent.get("kind") == kind and ent.get("workload") == workload_name
+                and ent.get("source_sha") == source_sha(kind)):
+            return ent.get("dram_bytes_per_launch")
+    return None
 
 
-def run_ours(args, w, dist):
-    import weight_rnn_gb300 as wr
+def _spread(xs):
+    xs = sorted(xs)
+    return {"min": xs[0], "median": statistics.median(xs), "max": xs[-1]}
 
-    wr.load_library()
-    dev = torch.device("cuda", dist.local)
-    torch.cuda.set_device(dev)
-    dist.init("nccl")
+
+def measure(w, wr, dist, dev, args, peaks, peak_src, clocks_on):
+    """Time one workload; returns its record (rank-max times)."""
     stream = torch.cuda.current_stream(dev)
-    peaks, peak_src = load_peaks()
     decode = bool(w.calls)
 
     # ---- inputs (per-rank seed: each GPU owns its own heads) ----
@@ -312,34 +354,37 @@ def run_ours(args, w, dist):
         state = torch.zeros(w.B, w.H, w.dk, w.dv, device=dev)
         out = torch.empty(w.B, w.H, w.dv, dtype=synth.torch_dtype(w.dtype), device=dev)
 
-        def step():
-            wr.delta_step(d["q"], d["k"], d["v"], d["beta"], d["g"], state, out,
-                          n_h=w.n_h)
+        def step(dd=d, o=out, st=state, s=None):
+            wr.delta_step(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], st, o,
+                          n_h=w.n_h, stream=s)
         tokens = w.B * w.H
         kbytes = step_bytes(w)
         kflops = None
         kind = "step"
+        launches = 1
     else:
         out = torch.empty(w.B, w.T, w.H, w.dv, dtype=synth.torch_dtype(w.dtype), device=dev)
         hT = torch.empty(w.B, w.H, w.dk, w.dv, device=dev)
 
-        def step():
-            wr.delta_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], out, hT,
-                         n_h=w.n_h, chunk=w.chunk)
+        def step(dd=d, o=out, st=hT, s=None):
+            wr.delta_fwd(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["h0"], o, st,
+                         n_h=w.n_h, chunk=w.chunk, stream=s)
         tokens = w.tokens
         kbytes = algorithmic_bytes(w)
         kflops = algorithmic_flops(w)
         kind = "fwd"
+        launches = wr.fwd_launches(w.B, w.H, w.T, w.dk, w.dv, w.n_h, w.chunk,
+                                   synth.torch_dtype(w.dtype))
 
+    clocks = ClockSampler(dev) if clocks_on else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
 
     # ---- device-resident timed region ----
-    clocks = ClockSampler(dev) if dist.local == 0 else None
-    if clocks:
-        clocks.start()
-        time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
@@ -355,55 +400,74 @@ def run_ours(args, w, dist):
     torch.cuda.synchronize(dev)
     dist.barrier()
     clock_rec = clocks.stop() if clocks else None
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    kernel_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / args.steps
-    elapsed = dist.max(elapsed, dev)
-    kernel_s = dist.max(kernel_s, dev)
+    elapsed = dist.max(t_start.elapsed_time(t_end) / 1e3, dev)
+    per_step = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    kernel_s = dist.max(sum(per_step) / args.steps, dev)
     ms_per_step = 1e3 * elapsed / args.steps
     value = tokens * dist.world * args.steps / elapsed
 
-    # ---- end to end through the public API with pinned host buffers ----
+    # ---- end to end through the public API with pinned host buffers:
+    #      batch slices on two streams, so that the copies of one slice
+    #      overlap the kernels of another ----
     pinned = {n: (None if host[n] is None else host[n].pin_memory()) for n in names}
     h2d = sum(t.numel() * t.element_size() for t in pinned.values() if t is not None)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     if decode:
-        state_h = torch.empty(state.shape, dtype=state.dtype).pin_memory()
         d2h = out_h.numel() * out_h.element_size()
+        nsl = 1
     else:
         hT_h = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
-        d2h = (out_h.numel() * out_h.element_size() + hT_h.numel() * hT_h.element_size())
+        d2h = out_h.numel() * out_h.element_size() + hT_h.numel() * hT_h.element_size()
+        nsl = min(w.B, 4)
+    streams = [stream, torch.cuda.Stream(dev)]
+    bounds = [(i * w.B // nsl, (i + 1) * w.B // nsl) for i in range(nsl)]
 
     def e2e_step():
-        for n in names:
-            if pinned[n] is not None:
-                d[n].copy_(pinned[n], non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-        if not decode:
-            hT_h.copy_(hT, non_blocking=True)
+        for i, (lo, hi) in enumerate(bounds):
+            s = streams[i % 2]
+            with torch.cuda.stream(s):
+                dd = {n: None if d[n] is None else d[n][lo:hi] for n in names}
+                for n in names:
+                    if pinned[n] is not None:
+                        dd[n].copy_(pinned[n][lo:hi], non_blocking=True)
+                if decode:
+                    step(s=s)
+                    out_h.copy_(out, non_blocking=True)
+                else:
+                    step(dd, out[lo:hi], hT[lo:hi], s)
+                    out_h[lo:hi].copy_(out[lo:hi], non_blocking=True)
+                    hT_h[lo:hi].copy_(hT[lo:hi], non_blocking=True)
 
-    for _ in range(min(3, args.warmup)):
-        e2e_step()
+    def e2e_run(n):
+        # the second stream starts after the first's previous work, and the
+        # first waits for the second at the end of the step
+        for _ in range(n):
+            streams[1].wait_stream(streams[0])
+            e2e_step()
+            streams[0].wait_stream(streams[1])
+
+    e2e_run(min(3, args.warmup))
     torch.cuda.synchronize(dev)
     dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_s = dist.max(e0.elapsed_time(e1) / 1e3, dev)
     e2e_value = tokens * dist.world * args.steps / e2e_s
 
-    # ---- roofline of the (only) kernel of a step ----
+    # ---- roofline of the step's kernels ----
     hbm = float(peaks["hbm_gbs"])
     achieved = kbytes / kernel_s / 1e9
     t_hbm = kbytes / (hbm * 1e9)
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm, "traffic": read_traffic(kind, w.name),
-            "algorithmic_bytes_per_launch": kbytes,
-            "kernel_us": kernel_s * 1e6, "peak_source": f"hbm_gbs of {peak_src}"}
+            "algorithmic_bytes_per_launch": kbytes, "kernel_us": kernel_s * 1e6,
+            "kernels_per_step": launches,
+            "peak_source": f"hbm_gbs of {peak_src}",
+            "spec_peak": SPEC_HBM_GBS, "frac_of_spec_peak": achieved / SPEC_HBM_GBS}
     if kflops is not None:
         tc = float(peaks["bf16_tflops"])
         t_tc = kflops / (tc * 1e12)
@@ -415,28 +479,66 @@ def run_ours(args, w, dist):
             roof.update({"bound": "tensor", "achieved": kflops / kernel_s / 1e12,
                          "peak": tc, "unit": "TFLOP/s", "frac": roof["tensor_frac"],
                          "peak_source": f"bf16_tflops of {peak_src}"})
+    rec = {"workload": w.name, "value": value, "unit": UNIT, "ms_per_step": ms_per_step,
+           "step_ms": {k: 1e3 * v for k, v in _spread(per_step).items()},
+           "roofline": roof, "config": config_of(w, args),
+           "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "slices": nsl, "streams": 2,
+                   "host_link_gbs": (h2d + d2h) / (e2e_s / args.steps) / 1e9},
+           "clocks": clock_rec, "gpu_launches": launches * args.steps,
+           "dtype": "bf16" if w.dtype == "bf16" else "f32"}
+    return rec, host
 
-    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only) ----
+
+def run_ours(args, dist):
+    import weight_rnn_gb300 as wr
+
+    wr.load_library()
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    dist.init("nccl")
+    peaks, peak_src = load_peaks()
+    ids = ORDER if args.workload == "all" else (int(args.workload),)
+    recs, hosts = {}, {}
+    for wid in ids:
+        w = synth.WORKLOADS[wid]
+        recs[wid], host = measure(w, wr, dist, dev, args, peaks, peak_src,
+                                  clocks_on=dist.local == 0)
+        if wid == ids[0]:
+            hosts[wid] = host
+        torch.cuda.empty_cache()
+    head_id = ids[0]
+    head = recs[head_id]
+    w = synth.WORKLOADS[head_id]
+
+    # ---- CPU oracle on the headline workload (rank 0, N = 1 only) ----
     cpu = None
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not decode:
-        threads = os.cpu_count() or 1
-        # every head of the workload: ~13 s of CPU work at B8 H16 T4096
-        heads = w.B * w.H
-        rate, dt, n = oracle_sample_rate(w, host, heads, threads)
-        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{n} of {w.B * w.H} heads x {w.T} tokens of {w.name} "
-                         f"({dt:.1f} s wall, float64)"}
+    if (dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline
+            and not w.calls):
+        cpu = cpu_baseline(w, hosts[head_id])
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": config_of(w, args), "roofline": roof, "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "clocks": clock_rec, "gpu_launches": args.steps,
+        "dtype": head["dtype"], "data": "synthetic",
+        "config": head["config"], "roofline": head["roofline"], "cpu_baseline": cpu,
+        "e2e": head["e2e"], "clocks": head["clocks"], "step_ms": head["step_ms"],
+        "gpu_launches": head["gpu_launches"],
         "gpu": torch.cuda.get_device_name(dev),
+        "per_workload": {
+            recs[i]["workload"]: {
+                "value": recs[i]["value"], "unit": UNIT,
+                "ms_per_step": recs[i]["ms_per_step"], "step_ms": recs[i]["step_ms"],
+                "roofline_frac": recs[i]["roofline"]["frac"],
+                "frac_of_spec_peak": recs[i]["roofline"]["frac_of_spec_peak"],
+                "kernel_us": recs[i]["roofline"]["kernel_us"],
+                "traffic": recs[i]["roofline"]["traffic"],
+                "algorithmic_bytes_per_launch":
+                    recs[i]["roofline"]["algorithmic_bytes_per_launch"],
+                "e2e_value": recs[i]["e2e"]["value"],
+                "gpu_launches": recs[i]["gpu_launches"], "clocks": recs[i]["clocks"]}
+            for i in ids},
     }
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
@@ -447,19 +549,18 @@ def run_ours(args, w, dist):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--workload", default="all", choices=["all", "2", "3", "4", "5"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     # at least 3 untimed warm-up steps, whatever is asked
     args.warmup = max(args.warmup, 3)
-    w = synth.WORKLOADS[args.workload]
     dist = Dist()
     if args.impl == "reference":
-        return run_reference(args, w, dist)
-    return run_ours(args, w, dist)
+        return run_reference(args, dist)
+    return run_ours(args, dist)
 
 
 if __name__ == "__main__":

@@ -38,6 +38,14 @@
  * Supported set: dk, dv in {16, 32, 64, 128}; chunk in {16, 32, 64};
  * 1 <= n_h <= 4; B, H, T >= 0 with B*H < 2^31.  Anything else returns
  * DELTA_ERR_UNSUPPORTED.  Empty problems (B*H*T == 0) are valid.
+ *
+ * Fast path.  Only DELTA_BF16 with dk = dv = 128 and chunk = 64 (any n_h,
+ * gated or not, any T with n_h*T < 2^30) runs on the tensor cores (tcgen05,
+ * TMEM, TMA).  Every other shape in the supported set -- all DELTA_F32 I/O,
+ * head dims below 128, chunk 16 or 32 -- runs a float32 CUDA-core kernel
+ * meant for correctness checks, several hundred times slower (about 0.1 % of
+ * the HBM roofline at B8 H16 T4096).  delta_step has one kernel for every
+ * supported shape (HBM-bound at dk = dv = 128).
  */
 #ifndef DELTA_H_
 #define DELTA_H_
@@ -99,6 +107,14 @@ int delta_step(const void *q, const void *k, const void *v, const float *beta,
                const float *g, float *state, void *out,
                int B, int H, int dk, int dv, int n_h,
                delta_dtype dtype, struct CUstream_st *stream);
+
+/*
+ * delta_fwd_kernel_count -- how many kernels one delta_fwd call with these
+ * sizes enqueues (0 for an empty batch), or -1 if delta_fwd would reject
+ * them.  Pure host function; nothing is enqueued.
+ */
+int delta_fwd_kernel_count(int B, int H, int T, int dk, int dv, int n_h, int chunk,
+                           delta_dtype dtype);
 
 /* Static English text for a delta_status value. */
 const char *delta_status_string(int status);

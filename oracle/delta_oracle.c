@@ -37,7 +37,8 @@
  * Layouts (row-major, contiguous):
  *   q    [B, T, H, dk]          k    [B, T, n_h, H, dk]
  *   v    [B, T, n_h, H, dv]     beta [B, T, n_h, H]
- *   g    [B, T, H] or NULL      h0   [B, H, dk, dv] or NULL (=> zero state)
+ *   g    [B, T, H] or NULL      h0   [B, H, dk, dv] or NULL (=> zero state;
+ *                                float32, or float64 for the decode carry)
  *   out  [B, T, H, dv] (f64)    hT   [B, H, dk, dv] (f64) or NULL
  */
 #include <pthread.h>
@@ -47,6 +48,7 @@
 
 typedef struct {
     const float *q, *k, *v, *beta, *g, *h0;
+    const double *h0d;      /* float64 initial state (decode carry), or NULL */
     double *out, *hT;
     int64_t B, H, T, dk, dv, n_h;
     int64_t next;           /* next (b,h) pair to process */
@@ -62,6 +64,8 @@ static int run_head(job_t *J, int64_t b, int64_t h, double *S, double *e)
     if (J->h0) {
         const float *src = J->h0 + (b * H + h) * dk * dv;
         for (int64_t i = 0; i < dk * dv; ++i) S[i] = (double)src[i];
+    } else if (J->h0d) {
+        memcpy(S, J->h0d + (b * H + h) * dk * dv, sizeof(double) * (size_t)(dk * dv));
     } else {
         memset(S, 0, sizeof(double) * (size_t)(dk * dv));
     }
@@ -132,21 +136,17 @@ static void *worker(void *arg)
     return NULL;
 }
 
-/*
- * delta_oracle_fwd: returns 0 on success, -1 on bad arguments, -2 if a worker
- * could not allocate its scratch state.  nthreads <= 0 means one thread.
- */
-int delta_oracle_fwd(const float *q, const float *k, const float *v,
-                     const float *beta, const float *g, const float *h0,
-                     double *out, double *hT,
-                     int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv,
-                     int64_t n_h, int nthreads)
+static int run_all(const float *q, const float *k, const float *v,
+                   const float *beta, const float *g, const float *h0,
+                   const double *h0d, double *out, double *hT,
+                   int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv,
+                   int64_t n_h, int nthreads)
 {
     if (!q || !k || !v || !beta || !out) return -1;
     if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0 || n_h <= 0) return -1;
 
     job_t J;
-    J.q = q; J.k = k; J.v = v; J.beta = beta; J.g = g; J.h0 = h0;
+    J.q = q; J.k = k; J.v = v; J.beta = beta; J.g = g; J.h0 = h0; J.h0d = h0d;
     J.out = out; J.hT = hT;
     J.B = B; J.H = H; J.T = T; J.dk = dk; J.dv = dv; J.n_h = n_h;
     J.next = 0;
@@ -176,4 +176,31 @@ int delta_oracle_fwd(const float *q, const float *k, const float *v,
     }
     pthread_mutex_destroy(&J.lock);
     return J.failed ? -2 : 0;
+}
+
+/*
+ * delta_oracle_fwd: returns 0 on success, -1 on bad arguments, -2 if a worker
+ * could not allocate its scratch state.  nthreads <= 0 means one thread.
+ */
+int delta_oracle_fwd(const float *q, const float *k, const float *v,
+                     const float *beta, const float *g, const float *h0,
+                     double *out, double *hT,
+                     int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv,
+                     int64_t n_h, int nthreads)
+{
+    return run_all(q, k, v, beta, g, h0, NULL, out, hT, B, H, T, dk, dv, n_h, nthreads);
+}
+
+/*
+ * delta_oracle_fwd_state64: the same, with the initial state given in
+ * float64 (NULL => zero), so that a state carried from one call to the next
+ * (the decode path) is never rounded.
+ */
+int delta_oracle_fwd_state64(const float *q, const float *k, const float *v,
+                             const float *beta, const float *g, const double *h0,
+                             double *out, double *hT,
+                             int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv,
+                             int64_t n_h, int nthreads)
+{
+    return run_all(q, k, v, beta, g, NULL, h0, out, hT, B, H, T, dk, dv, n_h, nthreads);
 }

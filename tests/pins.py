@@ -410,3 +410,90 @@ ALL_CHECKS = [
     check_continuation,
     check_extended_sequence,
 ]
+
+
+# ---------------------------------------------------------------------------
+# The comparison metric and the decode entry point.  These take the function
+# under test (``oracle.rel_l2`` / ``oracle.step``) so that planted mistakes in
+# copies of them can be run through the same checks.
+
+def check_rel_l2(rel):
+    """The metric every parity tolerance rests on (global relative L2, the
+    reading of the pages' "rel err"), against values computed by hand:
+    ||(3, 4.5) - (3, 4)|| / ||(3, 4)|| = 0.5 / 5; the reference is the second
+    argument (||(6, 8) - (3, 4)|| / 5 = 1, the other way round 5 / 10); an
+    all-zero reference gives the plain norm ||(3, 4)|| = 5; a 2x2 and a
+    2x2x2 array are measured over every element, not per row."""
+    assert abs(rel([3.0, 4.5], [3.0, 4.0]) - 0.1) <= 1e-15
+    assert abs(rel([6.0, 8.0], [3.0, 4.0]) - 1.0) <= 1e-15
+    assert abs(rel([3.0, 4.0], [6.0, 8.0]) - 0.5) <= 1e-15
+    assert abs(rel([3.0, 4.0], [0.0, 0.0]) - 5.0) <= 1e-15
+    assert rel([1.0, -2.0], [1.0, -2.0]) == 0.0
+    ref = np.array([[1.0, 2.0], [2.0, 4.0]])                  # norm 5
+    x = ref + np.array([[0.3, 0.0], [0.0, 0.4]])              # error norm 0.5
+    assert abs(rel(x, ref) - 0.1) <= 1e-15
+    ref3 = np.ones((2, 2, 2))                                 # norm sqrt(8)
+    x3 = ref3.copy()
+    x3[1, 1, 1] = 1.0 + np.sqrt(8.0) * 0.25                   # error sqrt(8) / 4
+    assert abs(rel(x3, ref3) - 0.25) <= 1e-15
+
+
+# exactly representable, unit norm and mutually orthogonal in float32
+_K1 = np.array([0.5, 0.5, 0.5, 0.5])
+_K2 = np.array([0.5, -0.5, 0.5, -0.5])
+
+
+def check_step_recall(step, rng):
+    """One decode step ([DR] §2.3, the recurrent form; [DP] §2.6, gate then
+    n_h sub-steps).  With beta = 1 and orthogonal unit keys k1, k2 the step
+    writes both values so that S^T k1 = v1 and S^T k2 = v2 exactly, whatever
+    the gate and the previous state ([DR] §1.2, exact recall); the readout
+    with q = k1 returns v1.  The part of the state orthogonal to both keys is
+    only scaled by g, and g = 0 erases it ([DP] §3.3, the reset)."""
+    dk, dv, B, H = 4, 3, 1, 2
+    S0 = rng.standard_normal((B, H, dk, dv))
+    v = f32(rng.standard_normal((B, 2, H, dv)))
+    k = np.broadcast_to(np.stack([_K1, _K2])[None, :, None, :], (B, 2, H, dk)).copy()
+    q = np.broadcast_to(_K1, (B, H, dk)).copy()
+    beta = np.ones((B, 2, H))
+    proj = np.eye(dk) - np.outer(_K1, _K1) - np.outer(_K2, _K2)
+    for gval in (0.0, 0.5, 1.0):
+        g = np.full((B, H), gval)
+        out, S = step(q, k, v, beta, g, S0, n_h=2)
+        for h in range(H):
+            assert np.allclose(S[0, h].T @ _K1, v[0, 0, h], atol=1e-12, rtol=0)
+            assert np.allclose(S[0, h].T @ _K2, v[0, 1, h], atol=1e-12, rtol=0)
+            assert np.allclose(out[0, h], v[0, 0, h], atol=1e-12, rtol=0)
+            assert np.allclose(proj @ S[0, h], gval * (proj @ S0[0, h]), atol=1e-12, rtol=0)
+
+
+def check_step_chain(step, fwd, rng):
+    """Decode calls chained through the carried state equal one forward over
+    the same tokens: the state is carried in float64, never rounded, so the
+    two agree to the last bit (allowed: 1e-15 relative).  Starts from a
+    float64 state that float32 cannot represent."""
+    B, H, dk, dv, n_h, calls = 2, 2, 5, 4, 2, 3
+    S = rng.standard_normal((B, H, dk, dv)) * (1.0 + 2.0 ** -40)
+    toks = []
+    for _ in range(calls):
+        q = f32(rng.standard_normal((B, H, dk)))
+        k = f32(unit(rng.standard_normal((B, n_h, H, dk))))
+        v = f32(rng.standard_normal((B, n_h, H, dv)))
+        beta = f32(rng.uniform(0.0, 2.0, (B, n_h, H)))
+        g = f32(rng.uniform(0.5, 1.0, (B, H)))
+        toks.append((q, k, v, beta, g))
+    S0 = S.copy()
+    outs = []
+    for (q, k, v, beta, g) in toks:
+        o, S = step(q, k, v, beta, g, S, n_h=n_h)
+        outs.append(o)
+    Q, K, V, Bt, G = (np.stack([t[i] for t in toks], 1) for i in range(5))
+    # the forward is given the carried-in state by one step with a zero
+    # write (beta = 0, g = 1), which leaves it exactly unchanged
+    z = np.zeros
+    _, S0c = step(z((B, H, dk)), z((B, 1, H, dk)), z((B, 1, H, dv)), z((B, 1, H)),
+                  None, S0, n_h=1)
+    assert np.array_equal(S0c, S0)
+    O, ST = fwd(Q, K, V, Bt, G, S0, n_h=n_h, state64=True)
+    assert rel_l2(np.stack(outs, 1), O) <= 1e-15
+    assert rel_l2(S, ST) <= 1e-15

@@ -149,21 +149,12 @@ def test_misaligned_pointer_is_rejected():
 
 
 # --- full-size workloads, in the launch configuration the bench times --------
-def sample_heads(w, n=3):
-    heads = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 3)]
-    return heads[:n]
-
-
 @pytest.mark.parametrize("wid", [2, 3, 4])
 def test_full_size_workload(wid):
+    """Every head of the full-size workload against the oracle (threaded over
+    the host cores), element by element."""
     w = W[wid]
     inp = synth.fwd_inputs(w)
     out, hT = gpu_fwd(inp, w)
-    heads = sample_heads(w)
-    check_sampled(inp, w, out, hT, heads)
-    o = out.float()
-    assert torch.isfinite(o).all() and torch.isfinite(hT).all()
-    # properties that hold at any size: the state norm is bounded by the
-    # stability of the transitions plus the writes -- here simply finite and
-    # of the scale of the oracle's on the sampled heads
     assert out.shape == (w.B, w.T, w.H, w.dv) and hT.shape == (w.B, w.H, w.dk, w.dv)
+    check_full(inp, w, out, hT)

@@ -123,3 +123,81 @@ def test_unmutated_copy_passes(tmp_path):
     fwd = functools.partial(oracle.fwd, lib=oracle.load_library(lpath))
     for check in ALL_CHECKS:
         check(fwd, np.random.default_rng(20261202))
+
+
+# --- the comparison metric and the decode entry point -----------------------
+def _rel_squared(x, ref):
+    x, ref = np.asarray(x, float), np.asarray(ref, float)
+    den = np.sum(ref * ref)
+    return float(np.sum((x - ref) ** 2) / den) if den else float(np.sum((x - ref) ** 2))
+
+
+def _rel_unnormalised(x, ref):
+    return float(np.linalg.norm((np.asarray(x, float) - np.asarray(ref, float)).ravel()))
+
+
+def _rel_swapped(x, ref):
+    return oracle.rel_l2(ref, x)
+
+
+def _rel_maxabs(x, ref):
+    x, ref = np.asarray(x, float), np.asarray(ref, float)
+    den = np.abs(ref).max()
+    return float(np.abs(x - ref).max() / den) if den else float(np.abs(x - ref).max())
+
+
+def _rel_per_row_mean(x, ref):
+    x, ref = np.atleast_2d(np.asarray(x, float)), np.atleast_2d(np.asarray(ref, float))
+    rows = [oracle.rel_l2(a, b) for a, b in zip(x.reshape(x.shape[0], -1),
+                                                 ref.reshape(ref.shape[0], -1))]
+    return float(np.mean(rows))
+
+
+REL_MUTANTS = {"squared_norms": _rel_squared, "unnormalised": _rel_unnormalised,
+               "arguments_swapped": _rel_swapped, "max_abs": _rel_maxabs,
+               "per_row_mean": _rel_per_row_mean}
+
+
+@pytest.mark.parametrize("name", sorted(REL_MUTANTS))
+def test_rel_l2_mutant_is_caught(name):
+    from pins import check_rel_l2
+    with pytest.raises(AssertionError):
+        check_rel_l2(REL_MUTANTS[name])
+
+
+def _step_state_f32(q, k, v, beta, g, state, *, n_h=1, **kw):
+    # the carried state rounded to float32 before every call
+    st = None if state is None else np.asarray(state, np.float32).astype(np.float64)
+    return oracle.step(q, k, v, beta, g, st, n_h=n_h, **kw)
+
+
+def _step_no_gate(q, k, v, beta, g, state, *, n_h=1, **kw):
+    return oracle.step(q, k, v, beta, None, state, n_h=n_h, **kw)
+
+
+def _step_no_carry(q, k, v, beta, g, state, *, n_h=1, **kw):
+    return oracle.step(q, k, v, beta, g, None, n_h=n_h, **kw)
+
+
+def _step_last_substep_only(q, k, v, beta, g, state, *, n_h=1, **kw):
+    k, v, beta = np.asarray(k), np.asarray(v), np.asarray(beta)
+    return oracle.step(q, k[:, -1:], v[:, -1:], beta[:, -1:], g, state, n_h=1, **kw)
+
+
+STEP_MUTANTS = {"state_rounded_to_f32": _step_state_f32, "gate_dropped": _step_no_gate,
+                "state_not_carried": _step_no_carry,
+                "last_substep_only": _step_last_substep_only}
+
+
+@pytest.mark.parametrize("name", sorted(STEP_MUTANTS))
+def test_step_mutant_is_caught(name):
+    from pins import check_step_chain, check_step_recall
+    bad = STEP_MUTANTS[name]
+    caught = []
+    for check in (lambda: check_step_recall(bad, np.random.default_rng(20261203)),
+                  lambda: check_step_chain(bad, oracle.fwd, np.random.default_rng(20261204))):
+        try:
+            check()
+        except AssertionError:
+            caught.append(True)
+    assert caught, f"no pin catches the planted mistake '{name}' in the decode step"

@@ -109,7 +109,8 @@ def test_prefill_then_decode_matches_forward():
 
 def test_full_size_decode_1024_calls():
     """B256 x H32, dk = dv = 128, n_h = 2, gated, 512 MiB state, 1024 calls;
-    the oracle replays a sample of heads through all 1024 tokens."""
+    the oracle replays every head of four batch rows (128 heads) through all
+    1024 tokens."""
     w = synth.WORKLOADS[5]
-    heads = [(0, 0), (w.B - 1, w.H - 1), (97, 13), (200, 5)]
+    heads = [(b, h) for b in (0, 97, 200, w.B - 1) for h in range(w.H)]
     run_steps(w, calls=w.calls, heads=heads)

@@ -15,7 +15,7 @@ import threading
 
 import torch
 
-__all__ = ["delta_fwd", "delta_step", "delta_status_string", "delta_last_error",
+__all__ = ["delta_fwd", "delta_step", "fwd_launches", "delta_status_string", "delta_last_error",
            "delta_check_device", "delta_inject_failure", "delta_selftest_wait",
            "delta_version", "DeltaError", "library_path", "load_library",
            "DELTA_OK", "DELTA_ERR_INVALID", "DELTA_ERR_UNSUPPORTED",
@@ -31,7 +31,7 @@ DELTA_F32 = 0
 DELTA_BF16 = 1
 
 #: every extern "C" entry point include/delta.h declares
-EXPORTED_SYMBOLS = ("delta_fwd", "delta_step", "delta_status_string",
+EXPORTED_SYMBOLS = ("delta_fwd", "delta_fwd_kernel_count", "delta_step", "delta_status_string",
                     "delta_last_error", "delta_check_device", "delta_version",
                     "delta_inject_failure", "delta_selftest_wait")
 
@@ -67,6 +67,8 @@ def load_library():
         p, i = ctypes.c_void_p, ctypes.c_int
         lib.delta_fwd.restype = i
         lib.delta_fwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.delta_fwd_kernel_count.restype = i
+        lib.delta_fwd_kernel_count.argtypes = [i, i, i, i, i, i, i, i]
         lib.delta_step.restype = i
         lib.delta_step.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, p]
         lib.delta_status_string.restype = ctypes.c_char_p
@@ -197,6 +199,15 @@ def delta_fwd(q, k, v, beta, g=None, h0=None, out=None, hT=None, *, n_h=1,
     if st != DELTA_OK:
         raise DeltaError(st, delta_last_error())
     return out, hT
+
+
+def fwd_launches(B, H, T, dk, dv, n_h, chunk, dtype) -> int:
+    """Kernels one ``delta_fwd`` call with these sizes enqueues
+    (``delta_fwd_kernel_count``); raises if the sizes are rejected."""
+    n = load_library().delta_fwd_kernel_count(B, H, T, dk, dv, n_h, chunk, _dtype_code(dtype))
+    if n < 0:
+        raise DeltaError(DELTA_ERR_UNSUPPORTED, "sizes rejected by delta_fwd")
+    return n
 
 
 def delta_step(q, k, v, beta, g, state, out=None, *, n_h=1, stream=None):

@@ -161,6 +161,21 @@ int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
   return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "generic chunk kernel launch");
 }
 
+int delta_fwd_kernel_count(int B, int H, int T, int dk, int dv, int n_h, int chunk,
+                           delta_dtype dtype) {
+  if (B < 0 || H < 0 || T < 0 || (dtype != DELTA_F32 && dtype != DELTA_BF16) ||
+      !supported_dim(dk) || !supported_dim(dv) || !supported_chunk(chunk) || n_h < 1 ||
+      n_h > 4 || (int64_t)B * H >= (int64_t(1) << 31))
+    return -1;
+  if ((int64_t)B * H == 0) return 0;
+  delta::FwdArgs a{};
+  a.B = B; a.H = H; a.T = T; a.L = (int64_t)T * n_h;
+  a.dk = dk; a.dv = dv; a.n_h = n_h; a.chunk = chunk;
+  a.bf16 = dtype == DELTA_BF16;
+  if (T == 0) return 1;
+  return delta::chunk_tc_supports(a) ? delta::kChunkTcKernels : 1;
+}
+
 int delta_step(const void *q, const void *k, const void *v, const float *beta,
                const float *g, float *state, void *out, int B, int H, int dk, int dv,
                int n_h, delta_dtype dtype, struct CUstream_st *stream) {
@@ -174,6 +189,11 @@ int delta_step(const void *q, const void *k, const void *v, const float *beta,
     return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
   const int64_t BH = (int64_t)B * H;
   if (BH == 0) return DELTA_OK;
+  // one CTA per (b, h) and 32-column slab of the state: the grid must fit
+  // gridDim.x
+  if (BH * (dv < 32 ? 1 : dv / 32) > INT32_MAX)
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H*(dv/32)=%lld blocks exceed 2^31-1",
+                (long long)(BH * (dv < 32 ? 1 : dv / 32)));
   if (!q || !k || !v || !beta || !state || !out)
     return fail(DELTA_ERR_INVALID, "q, k, v, beta, state and out must be non-NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) ||

@@ -160,6 +160,10 @@ struct Smem {
     return reinterpret_cast<volatile int *>(base + OFF_SM + SM_MISC + 4);
   }
   __device__ float *gate_c() const { return reinterpret_cast<float *>(base + OFF_SM + SM_MISC + 8); }
+  // set when a drain wait ran out: TMEM is then not freed at exit
+  __device__ volatile int *keep_tmem() const {
+    return reinterpret_cast<volatile int *>(base + OFF_SM + SM_MISC + 12);
+  }
   __device__ float *AX() const { return reinterpret_cast<float *>(base + OFF_AX); }
 };
 
@@ -181,6 +185,24 @@ __device__ __noinline__ bool wait_bar_slow(uint8_t *base, int idx, uint32_t pari
 __device__ __forceinline__ bool wait_bar(const Smem &sm, int idx, uint32_t parity, int role) {
   if (mbar_try_wait(sm.bar(idx), parity)) return true;
   return wait_bar_slow(sm.base, idx, parity, role);
+}
+
+// Wait for the completion of TMA copies or tensor-core products that were
+// already issued.  They complete on their own, so this wait does NOT give up
+// when another role has aborted (shared memory and TMEM must not be released
+// under them); it is still bounded.  If it runs out, the error word records
+// it and the CTA keeps its TMEM columns at exit instead of freeing them
+// under work that may still be writing them.
+__device__ __noinline__ bool wait_bar_drain(uint8_t *base, int idx, uint32_t parity, int role) {
+  Smem sm;
+  sm.base = base;
+  uint64_t *b = sm.bar(idx);
+  for (uint32_t i = 0; i < (1u << 24); ++i)
+    if (mbar_try_wait(b, parity)) return true;
+  *sm.abort_flag() = 1;
+  *sm.keep_tmem() = 1;
+  atomicCAS(&g_tc_error, 0u, (unsigned)(1 + role) | ((unsigned)idx << 8));
+  return false;
 }
 
 // fp32 64x64 matrices in shared memory are stored row-major with the column
@@ -622,9 +644,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     }
     // copies still in flight must land before the CTA's shared memory goes
     if (lane == 0) {
-      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n) wait_bar(sm, B_FULL + n % NS, (n / NS) & 1, 0);
+      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n)
+        wait_bar_drain(sm.base, B_FULL + n % NS, (n / NS) & 1, 0);
       for (int n = (issued_v > NS ? issued_v - NS : 0); n < issued_v; ++n)
-        wait_bar(sm, B_VFULL + n % NS, (n / NS) & 1, 0);
+        wait_bar_drain(sm.base, B_VFULL + n % NS, (n / NS) & 1, 0);
     }
     __syncwarp();
   } else if (warp == 1 || (dual_issue(GATED) && warp == 14)) {
@@ -761,7 +784,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         nap = 16;
       }
       mma_commit(sm.bar(B_DRAIN));  // every issuer arrives
-      wait_bar(sm, B_DRAIN, 0, 1);
+      wait_bar_drain(sm.base, B_DRAIN, 0, 1);
     }
     __syncwarp();
   } else if (warp < 6) {
@@ -1241,7 +1264,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   // ---- teardown ----
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 1 && !*sm.keep_tmem()) {
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
   }

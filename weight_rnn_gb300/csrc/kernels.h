@@ -38,6 +38,8 @@ cudaError_t launch_chunk_generic(const FwdArgs &a, cudaStream_t s);
 // shape is outside that set.
 cudaError_t launch_chunk_tc(const FwdArgs &a, cudaStream_t s);
 bool chunk_tc_supports(const FwdArgs &a);
+// kernels one tensor-core forward launches
+constexpr int kChunkTcKernels = 1;
 
 // Read and clear the word the tensor-core kernel sets when one of its bounded
 // waits gives up (0 = no error).  Synchronises the device.
