@@ -149,6 +149,35 @@ def wy_chunk(q, k, v, beta, S0=None, C=16):
     return o, S
 
 
+def ut_transform(k, beta, log_g=None, C=16):
+    """[DR] §2.2 (the UT transform) with the gated decay of §3, for every
+    chunk of one sequence: with gc the inclusive cumulative log gate of the
+    chunk and Gam_ij = exp(gc_i - gc_j) (i > j),
+        A = strictLower(diag(beta) (Gam * K K^T)),  T = (I + A)^{-1} diag(beta)
+    solved as a unit lower triangular system.  A ragged tail is padded with
+    identity steps (k = 0, beta = 0, log g = 0).  k [L,dk], beta [L],
+    log_g [L] or None.  Returns T [NT, C, C] (float64)."""
+    L, dk = k.shape
+    if log_g is None:
+        log_g = np.zeros(L)
+    NT = -(-L // C)
+    pad = NT * C - L
+    K = np.concatenate([k, np.zeros((pad, dk))]) if pad else np.asarray(k, float)
+    bt = np.concatenate([np.asarray(beta, float), np.zeros(pad)])
+    lg = np.concatenate([np.asarray(log_g, float), np.zeros(pad)])
+    strict = np.tril(np.ones((C, C), dtype=bool), -1)
+    out = np.zeros((NT, C, C))
+    for n in range(NT):
+        sl = slice(n * C, (n + 1) * C)
+        Kc, bc = K[sl], bt[sl]
+        gc = np.cumsum(lg[sl])
+        diff = np.where(strict, gc[:, None] - gc[None, :], -np.inf)  # mask before exp
+        A = np.where(strict, bc[:, None] * (Kc @ Kc.T) * np.exp(diff), 0.0)
+        out[n] = solve_triangular(np.eye(C) + A, np.diag(bc), lower=True,
+                                  unit_diagonal=True)
+    return out
+
+
 def ut_chunk(q, k, v, beta, log_g=None, S0=None, C=16):
     """[DR] §2.2-§2.3 (UT transform + chunkwise algorithm) and §3 (the gated
     chunkwise form with the within-chunk cumulative decay).  Per chunk:
@@ -178,16 +207,14 @@ def ut_chunk(q, k, v, beta, log_g=None, S0=None, C=16):
     S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
     o = np.zeros((Lp, dv))
     incl = np.tril(np.ones((C, C), dtype=bool))
-    strict = np.tril(np.ones((C, C), dtype=bool), -1)
+    Ts = ut_transform(K, bt, lg, C)
     for n in range(NT):
         sl = slice(n * C, (n + 1) * C)
-        Kc, Vc, Qc, bc = K[sl], V[sl], Q[sl], bt[sl]
+        Kc, Vc, Qc = K[sl], V[sl], Q[sl]
         gc = np.cumsum(lg[sl])
         diff = np.where(incl, gc[:, None] - gc[None, :], -np.inf)
         Gam = np.exp(diff)
-        A = np.where(strict, bc[:, None] * (Kc @ Kc.T) * Gam, 0.0)
-        Tm = solve_triangular(np.eye(C) + A, np.diag(bc), lower=True,
-                              unit_diagonal=True)
+        Tm = Ts[n]
         W = Tm @ (Kc * np.exp(gc)[:, None])
         U = Tm @ Vc
         Vt = U - W @ S

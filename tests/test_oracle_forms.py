@@ -154,3 +154,49 @@ def test_batched_heads_are_independent():
                                 threads=1)
             assert np.array_equal(o1[0, :, 0], o[b, :, h])
             assert np.array_equal(s1[0, 0], s[b, h])
+
+
+@pytest.mark.parametrize("C", [4, 16, 64])
+def test_ut_transform_gives_the_wy_vectors(C):
+    """[DR] §2.1 vs §2.2: the UT transform T = (I + A)^{-1} diag(beta) of a
+    chunk produces the WY vectors that the row-by-row recursion
+    w_r = beta_r (k_r - sum_{i<r} w_i (k_i^T k_r)) (and the same for u with v)
+    builds, W = T K and U = T V (ungated).  L is not a multiple of C: the
+    padded rows of the last chunk are identity steps (T = 0 there)."""
+    rng = np.random.default_rng(C)
+    L, dk, dv = 2 * C + 3, 8, 5
+    k = rng.standard_normal((L, dk))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    v = rng.standard_normal((L, dv))
+    beta = rng.uniform(0.0, 2.0, L)
+    Ts = forms.ut_transform(k, beta, None, C)
+    assert Ts.shape == (-(-L // C), C, C)
+    for n in range(Ts.shape[0]):
+        s, e = n * C, min(n * C + C, L)
+        w = np.zeros((e - s, dk))
+        u = np.zeros((e - s, dv))
+        for r in range(e - s):
+            w[r] = beta[s + r] * (k[s + r] - sum(w[i] * (k[s + i] @ k[s + r]) for i in range(r)))
+            u[r] = beta[s + r] * (v[s + r] - sum(u[i] * (k[s + i] @ k[s + r]) for i in range(r)))
+        T = Ts[n][: e - s, : e - s]
+        assert np.allclose(T @ k[s:e], w, atol=1e-12, rtol=0)
+        assert np.allclose(T @ v[s:e], u, atol=1e-12, rtol=0)
+        assert not Ts[n][e - s:].any() and not Ts[n][:, e - s:].any()
+
+
+def test_ut_transform_special_cases():
+    """Orthogonal keys give A = 0, so T = diag(beta); beta = 0 gives T = 0;
+    a gate of 0 at row r ([DP] §3.3) cuts every coupling across r
+    (Gam_ij = 0 for j < r <= i), so T is block diagonal there."""
+    C, dk = 8, 8
+    k = np.eye(dk)
+    beta = np.linspace(0.1, 1.9, C)
+    assert np.array_equal(forms.ut_transform(k, beta, None, C)[0], np.diag(beta))
+    assert not forms.ut_transform(k, np.zeros(C), None, C).any()
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal((C, dk))
+    lg = np.zeros(C)
+    lg[5] = -1e4  # log g far below where exp underflows to 0 (g = 0)
+    T = forms.ut_transform(k, np.ones(C), lg, C)[0]
+    assert not T[5:, :5].any()
+    assert np.allclose(T[:5, :5], forms.ut_transform(k[:5], np.ones(5), None, 5)[0])
