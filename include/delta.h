@@ -26,9 +26,10 @@
  *     clamped (||k|| = 1 and beta in [0, 2] keep the recurrence stable).
  *   - g is the LINEAR gate in [0, 1]; g = 0 resets the state.  NULL means 1.
  *   - Every pointer is device memory owned by the caller, contiguous in the
- *     layout given, and 16-byte aligned.  The library allocates no device
- *     memory per call and keeps no state between calls; it is thread-safe.
- *   - Both calls only enqueue work on `stream` and return; they never
+ *     layout given, and 16-byte aligned.  The library keeps no state between
+ *     calls and is thread-safe.  The one device allocation it makes is the
+ *     scratch of delta_fwd's tensor-core path (below).
+ *   - The calls only enqueue work on `stream` and return; they never
  *     synchronise.  Argument errors are returned before anything is enqueued.
  *     A failed launch returns DELTA_ERR_CUDA.  NaN/Inf inputs propagate and
  *     are not detected.
@@ -40,12 +41,15 @@
  * DELTA_ERR_UNSUPPORTED.  Empty problems (B*H*T == 0) are valid.
  *
  * Fast path.  Only DELTA_BF16 with dk = dv = 128 and chunk = 64 (any n_h,
- * gated or not, any T with n_h*T < 2^30) runs on the tensor cores (tcgen05,
- * TMEM, TMA).  Every other shape in the supported set -- all DELTA_F32 I/O,
- * head dims below 128, chunk 16 or 32 -- runs a float32 CUDA-core kernel
- * meant for correctness checks, several hundred times slower (about 0.1 % of
- * the HBM roofline at B8 H16 T4096).  delta_step has one kernel for every
- * supported shape (HBM-bound at dk = dv = 128).
+ * gated or not, any T with n_h*T < 2^30 and B*H*ceil(n_h*T/64) < 2^31) runs
+ * on the tensor cores (tcgen05, TMEM, TMA), in two kernels: the UT pass
+ * (delta_ut_transform) over every chunk at once, then the state pass
+ * (delta_fwd_with_ut), one CTA per (b, h).  Every other shape in the
+ * supported set -- all DELTA_F32 I/O, head dims below 128, chunk 16 or 32 --
+ * runs a float32 CUDA-core kernel meant for correctness checks, several
+ * hundred times slower (about 0.1 % of the HBM roofline at B8 H16 T4096).
+ * delta_step has one kernel for every supported shape (HBM-bound at
+ * dk = dv = 128).
  */
 #ifndef DELTA_H_
 #define DELTA_H_
@@ -83,11 +87,59 @@ typedef enum {
  *   chunk                      rows of the extended sequence per chunk
  *
  * For n_h == 1 the sub-step axis has extent 1, i.e. k is [B, T, H, dk].
+ *
+ * Scratch.  On the tensor-core path the call takes B*H*ceil(n_h*T/64) * 8 KiB
+ * of device memory (the T tiles of every chunk, see delta_ut_transform) as a
+ * stream-ordered allocation from a memory pool the library creates once per
+ * device, on the current device, and releases it, stream-ordered, before
+ * returning; the pool keeps the memory for the next call until the process
+ * exits.  Concurrent calls on different streams each get their own block.
+ * Callers that manage this memory themselves call delta_ut_transform and
+ * delta_fwd_with_ut instead.  An allocation failure returns DELTA_ERR_CUDA
+ * with nothing enqueued.
  */
 int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
               const float *g, const float *h0, void *out, float *hT,
               int B, int H, int T, int dk, int dv, int n_h, int chunk,
               delta_dtype dtype, struct CUstream_st *stream);
+
+/*
+ * delta_ut_transform -- the intra-chunk pass of delta_fwd on its own: the UT
+ * transform of "08 · linear 路线（三）" §2.2 with the gated decay of §3, for
+ * every chunk n of 64 steps of the extended sequence (length L = n_h*T,
+ * "DeltaProduct" §4.1) of every (b, h):
+ *
+ *   gc_r   = sum_{e <= r} log g_e      (within the chunk; log g_e = log g_t at
+ *                                       each token's first sub-step, else 0)
+ *   A      = strictLower(diag(beta) (Gam * K K^T)),  Gam_ij = exp(gc_i - gc_j)
+ *   T      = (I + A)^{-1} diag(beta)
+ *
+ *   k, beta, g     as in delta_fwd (bf16 keys, dk = 128)
+ *   t_mat [B, H, NT, 64, 64]  bfloat16, row-major, NT = ceil(L / 64); T of
+ *                              chunk n; rows past L are identity steps
+ *                              (k = 0, beta = 0), i.e. zero rows and columns
+ *
+ * Only bf16 with dk = 128 and chunk = 64 is supported (DELTA_ERR_UNSUPPORTED
+ * otherwise).  t_mat is caller-owned device memory of B*H*NT*8192 bytes,
+ * 16-byte aligned, overlapping no input.  The entries are rounded to bf16
+ * (nearest even) from a float32 / tf32 solve.
+ */
+int delta_ut_transform(const void *k, const float *beta, const float *g, void *t_mat,
+                       int B, int H, int T, int dk, int n_h, int chunk,
+                       delta_dtype dtype, struct CUstream_st *stream);
+
+/*
+ * delta_fwd_with_ut -- the state pass of delta_fwd on its own, given the
+ * t_mat that delta_ut_transform wrote for the same k, beta and g: W = T (K *
+ * exp(gc)), U = T V, the outputs and the state update of "08 · linear 路线
+ * （三）" §2.3 and §3, chunk after chunk.  Arguments as in delta_fwd plus
+ * t_mat (read only; it must overlap no other argument).  Only bf16 with
+ * dk = dv = 128 and chunk = 64 is supported.  Allocates nothing.
+ */
+int delta_fwd_with_ut(const void *q, const void *k, const void *v, const float *beta,
+                      const float *g, const float *h0, const void *t_mat, void *out,
+                      float *hT, int B, int H, int T, int dk, int dv, int n_h, int chunk,
+                      delta_dtype dtype, struct CUstream_st *stream);
 
 /*
  * delta_step -- one decode token for every (b, h): the recurrent form of
@@ -140,8 +192,8 @@ int delta_check_device(void);
 int delta_version(void);
 
 /*
- * delta_inject_failure -- test hook: the next `count` calls of delta_fwd and
- * delta_step (together) return DELTA_ERR_CUDA, with "injected failure" in
+ * delta_inject_failure -- test hook: the next `count` calls of delta_fwd,
+ * delta_ut_transform, delta_fwd_with_ut and delta_step (together) return DELTA_ERR_CUDA, with "injected failure" in
  * delta_last_error(), right after their arguments pass validation and before
  * anything is enqueued.  count = 0 clears a pending injection; count < 0 is
  * DELTA_ERR_INVALID.  The counter is process-wide.

@@ -154,3 +154,64 @@ def test_injected_failure_returns_before_launch(lib):
 def test_selftest_wait_rejects_bad_poll_counts(lib):
     assert lib.delta_selftest_wait(0, None) == wr.DELTA_ERR_INVALID
     assert lib.delta_selftest_wait((1 << 24) + 1, None) == wr.DELTA_ERR_INVALID
+
+
+def ut(lib, **kw):
+    a = dict(k=FAKE * 2, beta=FAKE * 4, g=None, t=FAKE * 64, B=1, H=1, T=4, dk=128, n_h=1,
+             chunk=64, dtype=wr.DELTA_BF16)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_ut_transform(vp(a["k"]), vp(a["beta"]), vp(a["g"]), vp(a["t"]), a["B"],
+                                  a["H"], a["T"], a["dk"], a["n_h"], a["chunk"], a["dtype"], None)
+
+
+def fwd_ut(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, beta=FAKE * 4, g=None, h0=None, t=FAKE * 64,
+             out=FAKE * 5, hT=None, B=1, H=1, T=4, dk=128, dv=128, n_h=1, chunk=64,
+             dtype=wr.DELTA_BF16)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_fwd_with_ut(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["beta"]), vp(a["g"]),
+                                 vp(a["h0"]), vp(a["t"]), vp(a["out"]), vp(a["hT"]), a["B"],
+                                 a["H"], a["T"], a["dk"], a["dv"], a["n_h"], a["chunk"],
+                                 a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=64), wr.DELTA_ERR_UNSUPPORTED),           # the UT pass is the tensor-core shape only
+    (dict(chunk=32), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(dtype=wr.DELTA_F32), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(dtype=9), wr.DELTA_ERR_INVALID),
+    (dict(n_h=5), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(T=-1), wr.DELTA_ERR_INVALID),
+    (dict(k=None), wr.DELTA_ERR_INVALID),
+    (dict(t=None), wr.DELTA_ERR_INVALID),
+    (dict(t=FAKE * 64 + 8), wr.DELTA_ERR_ALIGN),
+    (dict(t=FAKE * 2 + 16), wr.DELTA_ERR_INVALID),      # t_mat overlaps k
+])
+def test_ut_transform_rejects_before_launch(lib, kw, status):
+    assert ut(lib, **kw) == status
+
+
+def test_ut_transform_empty_is_ok_without_gpu(lib):
+    assert ut(lib, B=0) == wr.DELTA_OK
+    assert ut(lib, T=0, k=None, t=None) == wr.DELTA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=64, dv=64), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(dtype=wr.DELTA_F32), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(t=None), wr.DELTA_ERR_INVALID),
+    (dict(t=FAKE * 5), wr.DELTA_ERR_INVALID),           # t_mat overlaps out
+    (dict(t=FAKE * 64 + 4), wr.DELTA_ERR_ALIGN),
+    (dict(q=None), wr.DELTA_ERR_INVALID),
+])
+def test_fwd_with_ut_rejects_before_launch(lib, kw, status):
+    assert fwd_ut(lib, **kw) == status
+
+
+def test_kernel_count(lib):
+    assert lib.delta_fwd_kernel_count(4, 32, 8192, 128, 128, 1, 64, wr.DELTA_BF16) == 2
+    assert lib.delta_fwd_kernel_count(1, 1, 64, 16, 16, 1, 16, wr.DELTA_F32) == 1
+    assert lib.delta_fwd_kernel_count(0, 1, 64, 128, 128, 1, 64, wr.DELTA_BF16) == 0
+    assert lib.delta_fwd_kernel_count(1, 1, 64, 48, 16, 1, 16, wr.DELTA_F32) == -1

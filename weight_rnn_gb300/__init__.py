@@ -15,7 +15,8 @@ import threading
 
 import torch
 
-__all__ = ["delta_fwd", "delta_step", "fwd_launches", "delta_status_string", "delta_last_error",
+__all__ = ["delta_fwd", "delta_ut_transform", "delta_fwd_with_ut", "delta_step",
+           "fwd_launches", "delta_status_string", "delta_last_error",
            "delta_check_device", "delta_inject_failure", "delta_selftest_wait",
            "delta_version", "DeltaError", "library_path", "load_library",
            "DELTA_OK", "DELTA_ERR_INVALID", "DELTA_ERR_UNSUPPORTED",
@@ -31,7 +32,8 @@ DELTA_F32 = 0
 DELTA_BF16 = 1
 
 #: every extern "C" entry point include/delta.h declares
-EXPORTED_SYMBOLS = ("delta_fwd", "delta_fwd_kernel_count", "delta_step", "delta_status_string",
+EXPORTED_SYMBOLS = ("delta_fwd", "delta_ut_transform", "delta_fwd_with_ut",
+                    "delta_fwd_kernel_count", "delta_step", "delta_status_string",
                     "delta_last_error", "delta_check_device", "delta_version",
                     "delta_inject_failure", "delta_selftest_wait")
 
@@ -67,6 +69,10 @@ def load_library():
         p, i = ctypes.c_void_p, ctypes.c_int
         lib.delta_fwd.restype = i
         lib.delta_fwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.delta_ut_transform.restype = i
+        lib.delta_ut_transform.argtypes = [p, p, p, p, i, i, i, i, i, i, i, p]
+        lib.delta_fwd_with_ut.restype = i
+        lib.delta_fwd_with_ut.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
         lib.delta_fwd_kernel_count.restype = i
         lib.delta_fwd_kernel_count.argtypes = [i, i, i, i, i, i, i, i]
         lib.delta_step.restype = i
@@ -196,6 +202,79 @@ def delta_fwd(q, k, v, beta, g=None, h0=None, out=None, hT=None, *, n_h=1,
     st = lib.delta_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
                        _ptr(out), _ptr(hT), B, H, T, dk, dv, n_h, chunk, code,
                        _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return out, hT
+
+
+def _kvb_shapes(k, v, beta, B, T, H, dk, n_h):
+    if n_h == 1 and k.dim() == 4:
+        return (B, T, H, dk), (B, T, H, v.shape[-1] if v is not None else dk), (B, T, H)
+    return ((B, T, n_h, H, dk), (B, T, n_h, H, v.shape[-1] if v is not None else dk),
+            (B, T, n_h, H))
+
+
+def delta_ut_transform(k, beta, g=None, t_mat=None, *, n_h=1, chunk=64, stream=None):
+    """The intra-chunk UT transform of every chunk (``delta_ut_transform``):
+    T = (I + A)^{-1} diag(beta) per 64-step chunk of the extended sequence.
+
+    k [B,T,n_h,H,128] (or [B,T,H,128]) bfloat16; beta [B,T,n_h,H] (or
+    [B,T,H]) float32; g [B,T,H] float32 or None.  Returns ``t_mat``
+    [B,H,NT,64,64] bfloat16, NT = ceil(n_h * T / 64).
+    """
+    lib = load_library()
+    B, T = k.shape[0], k.shape[1]
+    H, dk = k.shape[-2], k.shape[-1]
+    dev = k.device
+    if dev.type != "cuda":
+        raise ValueError("delta_ut_transform needs CUDA tensors")
+    code = _dtype_code(k.dtype)
+    kshape, _, bshape = _kvb_shapes(k, None, beta, B, T, H, dk, n_h)
+    _check(k, "k", kshape, k.dtype, dev)
+    _check(beta, "beta", bshape, torch.float32, dev)
+    _check(g, "g", (B, T, H), torch.float32, dev)
+    nt = -(-(n_h * T) // chunk)
+    if t_mat is None:
+        t_mat = torch.empty((B, H, nt, chunk, chunk), dtype=torch.bfloat16, device=dev)
+    _check(t_mat, "t_mat", (B, H, nt, chunk, chunk), torch.bfloat16, dev)
+    st = lib.delta_ut_transform(_ptr(k), _ptr(beta), _ptr(g), _ptr(t_mat), B, H, T, dk, n_h,
+                                chunk, code, _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return t_mat
+
+
+def delta_fwd_with_ut(q, k, v, beta, g, h0, t_mat, out=None, hT=None, *, n_h=1, chunk=64,
+                      want_state=True, stream=None):
+    """The state pass alone (``delta_fwd_with_ut``), given the ``t_mat`` that
+    ``delta_ut_transform`` returned for the same k, beta and g.  Arguments and
+    results as in ``delta_fwd``."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("delta_fwd_with_ut needs CUDA tensors")
+    dt = q.dtype
+    code = _dtype_code(dt)
+    dv = v.shape[-1]
+    kshape, vshape, bshape = _kvb_shapes(k, v, beta, B, T, H, dk, n_h)
+    _check(q, "q", (B, T, H, dk), dt, dev)
+    _check(k, "k", kshape, dt, dev)
+    _check(v, "v", vshape, dt, dev)
+    _check(beta, "beta", bshape, torch.float32, dev)
+    _check(g, "g", (B, T, H), torch.float32, dev)
+    _check(h0, "h0", (B, H, dk, dv), torch.float32, dev)
+    nt = -(-(n_h * T) // chunk)
+    _check(t_mat, "t_mat", (B, H, nt, chunk, chunk), torch.bfloat16, dev)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=dt, device=dev)
+    _check(out, "out", (B, T, H, dv), dt, dev)
+    if hT is None and want_state:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(hT, "hT", (B, H, dk, dv), torch.float32, dev)
+    st = lib.delta_fwd_with_ut(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                               _ptr(t_mat), _ptr(out), _ptr(hT), B, H, T, dk, dv, n_h, chunk,
+                               code, _stream(dev, stream))
     if st != DELTA_OK:
         raise DeltaError(st, delta_last_error())
     return out, hT

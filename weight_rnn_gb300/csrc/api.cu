@@ -1,7 +1,7 @@
 // api.cu -- the C ABI declared in include/delta.h: argument validation,
-// kernel selection and error reporting.  No device memory is allocated here
-// and nothing is synchronised: each call enqueues kernels on the caller's
-// stream and returns.
+// kernel selection, scratch memory for the tensor-core forward and error
+// reporting.  Nothing is synchronised: each call enqueues work on the
+// caller's stream and returns.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdarg>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/delta.h"
 #include "kernels.h"
@@ -56,6 +57,107 @@ bool overlap(Range a, Range b) {
   return a.lo != 0 && b.lo != 0 && a.hi > a.lo && b.hi > b.lo && a.lo < b.hi && b.lo < a.hi;
 }
 
+// Scratch for the T tiles handed from the UT pass to the state pass: stream-
+// ordered allocations from one memory pool per device, owned by the library,
+// that keeps freed memory for reuse (release threshold: unlimited), so calls
+// after the first reuse it without reaching the driver.
+constexpr int kMaxDevices = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+cudaError_t scratch_pool(cudaMemPool_t *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  if (!g_pool[dev]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool;
+    if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return e;
+    uint64_t keep = UINT64_MAX;
+    if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return e;
+    }
+    g_pool[dev] = pool;
+  }
+  *out = g_pool[dev];
+  return cudaSuccess;
+}
+
+// Checks shared by the forward entry points; fills `a` on success.
+int validate_fwd(const void *q, const void *k, const void *v, const float *beta,
+                 const float *g, const float *h0, void *out, float *hT, int B, int H,
+                 int T, int dk, int dv, int n_h, int chunk, delta_dtype dtype,
+                 delta::FwdArgs &a) {
+  if (B < 0 || H < 0 || T < 0)
+    return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d T=%d", B, H, T);
+  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
+    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (!supported_dim(dk) || !supported_dim(dv))
+    return fail(DELTA_ERR_UNSUPPORTED, "dk=%d dv=%d not in {16,32,64,128}", dk, dv);
+  if (!supported_chunk(chunk))
+    return fail(DELTA_ERR_UNSUPPORTED, "chunk=%d not in {16,32,64}", chunk);
+  if (n_h < 1 || n_h > 4) return fail(DELTA_ERR_UNSUPPORTED, "n_h=%d not in [1,4]", n_h);
+  if ((int64_t)B * H >= (int64_t(1) << 31))
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
+
+  const int64_t esz = dtype == DELTA_BF16 ? 2 : 4;
+  const int64_t BH = (int64_t)B * H;
+  const int64_t L = (int64_t)T * n_h;
+  const int64_t state_bytes = BH * dk * dv * 4;
+  a = delta::FwdArgs{};
+  a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.h0 = h0;
+  a.out = out; a.hT = hT;
+  a.B = B; a.H = H; a.T = T; a.L = L;
+  a.dk = dk; a.dv = dv; a.n_h = n_h; a.chunk = chunk;
+  a.bf16 = dtype == DELTA_BF16;
+  if (BH == 0) return DELTA_OK;
+  if (T > 0 && (!q || !k || !v || !beta || !out))
+    return fail(DELTA_ERR_INVALID, "q, k, v, beta and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) ||
+      !aligned16(g) || !aligned16(h0) || !aligned16(out) || !aligned16(hT))
+    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+
+  const Range r_out = range(out, BH * T * dv * esz);
+  const Range r_hT = range(hT, state_bytes);
+  const Range inputs[] = {range(q, BH * T * dk * esz), range(k, BH * L * dk * esz),
+                          range(v, BH * L * dv * esz),  range(beta, BH * L * 4),
+                          range(g, g ? BH * T * 4 : 0), range(h0, h0 ? state_bytes : 0)};
+  for (const Range &r : inputs)
+    if (overlap(r_out, r)) return fail(DELTA_ERR_INVALID, "out overlaps an input");
+  for (int i = 0; i < 5; ++i)
+    if (overlap(r_hT, inputs[i])) return fail(DELTA_ERR_INVALID, "hT overlaps an input");
+  if (overlap(r_hT, r_out)) return fail(DELTA_ERR_INVALID, "hT overlaps out");
+  if (hT && h0 && (const void *)hT != (const void *)h0 && overlap(r_hT, inputs[5]))
+    return fail(DELTA_ERR_INVALID, "hT partially overlaps h0");
+  return DELTA_OK;
+}
+
+// t_mat of the tensor-core shape: present, aligned and clear of the rest.
+int validate_t_mat(const delta::FwdArgs &a, const void *t_mat, bool with_outputs) {
+  if (!t_mat) return fail(DELTA_ERR_INVALID, "t_mat must be non-NULL");
+  if (!aligned16(t_mat)) return fail(DELTA_ERR_ALIGN, "t_mat must be 16-byte aligned");
+  const int64_t BH = a.B * a.H;
+  const Range r_t = range(t_mat, delta::ut_workspace_bytes(a));
+  const Range others[] = {range(a.k, BH * a.L * a.dk * 2), range(a.beta, BH * a.L * 4),
+                          range(a.g, a.g ? BH * a.T * 4 : 0),
+                          range(with_outputs ? a.q : nullptr, BH * a.T * a.dk * 2),
+                          range(with_outputs ? a.v : nullptr, BH * a.L * a.dv * 2),
+                          range(with_outputs ? a.h0 : nullptr, a.h0 ? BH * a.dk * a.dv * 4 : 0),
+                          range(with_outputs ? a.out : nullptr, BH * a.T * a.dv * 2),
+                          range(with_outputs ? a.hT : nullptr, BH * a.dk * a.dv * 4)};
+  for (const Range &r : others)
+    if (overlap(r_t, r)) return fail(DELTA_ERR_INVALID, "t_mat overlaps another argument");
+  return DELTA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -88,13 +190,18 @@ int delta_selftest_wait(int polls, struct CUstream_st *stream) {
 }
 
 int delta_check_device(void) {
-  unsigned int word = 0;
-  const cudaError_t err = delta::read_and_clear_tc_error(&word);
+  unsigned int word = 0, ut_word = 0;
+  cudaError_t err = delta::read_and_clear_tc_error(&word);
+  if (err == cudaSuccess) err = delta::read_and_clear_ut_error(&ut_word);
   if (err != cudaSuccess) return cuda_fail(err, "device check");
   if (word != 0)
     return fail(DELTA_ERR_CUDA,
                 "a kernel wait gave up (role %u, barrier %u): results of that call are invalid",
                 (word & 0xffu) - 1, word >> 8);
+  if (ut_word != 0)
+    return fail(DELTA_ERR_CUDA,
+                "a UT-pass wait gave up (role %u, barrier %u): results of that call are invalid",
+                (ut_word & 0xffu) - 1, ut_word >> 8);
   return DELTA_OK;
 }
 
@@ -102,50 +209,10 @@ int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
               const float *g, const float *h0, void *out, float *hT, int B, int H,
               int T, int dk, int dv, int n_h, int chunk, delta_dtype dtype,
               struct CUstream_st *stream) {
-  if (B < 0 || H < 0 || T < 0)
-    return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d T=%d", B, H, T);
-  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
-    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
-  if (!supported_dim(dk) || !supported_dim(dv))
-    return fail(DELTA_ERR_UNSUPPORTED, "dk=%d dv=%d not in {16,32,64,128}", dk, dv);
-  if (!supported_chunk(chunk))
-    return fail(DELTA_ERR_UNSUPPORTED, "chunk=%d not in {16,32,64}", chunk);
-  if (n_h < 1 || n_h > 4) return fail(DELTA_ERR_UNSUPPORTED, "n_h=%d not in [1,4]", n_h);
-  if ((int64_t)B * H >= (int64_t(1) << 31))
-    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
-
-  const int64_t esz = dtype == DELTA_BF16 ? 2 : 4;
-  const int64_t BH = (int64_t)B * H;
-  const int64_t L = (int64_t)T * n_h;
-  const int64_t state_bytes = BH * dk * dv * 4;
-  if (BH == 0) return DELTA_OK;
-  if (T > 0 && (!q || !k || !v || !beta || !out))
-    return fail(DELTA_ERR_INVALID, "q, k, v, beta and out must be non-NULL");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) ||
-      !aligned16(g) || !aligned16(h0) || !aligned16(out) || !aligned16(hT))
-    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
-
-  const Range r_out = range(out, BH * T * dv * esz);
-  const Range r_hT = range(hT, state_bytes);
-  const Range inputs[] = {range(q, BH * T * dk * esz), range(k, BH * L * dk * esz),
-                          range(v, BH * L * dv * esz),  range(beta, BH * L * 4),
-                          range(g, g ? BH * T * 4 : 0), range(h0, h0 ? state_bytes : 0)};
-  for (const Range &r : inputs)
-    if (overlap(r_out, r)) return fail(DELTA_ERR_INVALID, "out overlaps an input");
-  for (int i = 0; i < 5; ++i)
-    if (overlap(r_hT, inputs[i])) return fail(DELTA_ERR_INVALID, "hT overlaps an input");
-  if (overlap(r_hT, r_out)) return fail(DELTA_ERR_INVALID, "hT overlaps out");
-  if (hT && h0 && (const void *)hT != (const void *)h0 && overlap(r_hT, inputs[5]))
-    return fail(DELTA_ERR_INVALID, "hT partially overlaps h0");
-
-  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
-
   delta::FwdArgs a;
-  a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.h0 = h0;
-  a.out = out; a.hT = hT;
-  a.B = B; a.H = H; a.T = T; a.L = L;
-  a.dk = dk; a.dv = dv; a.n_h = n_h; a.chunk = chunk;
-  a.bf16 = dtype == DELTA_BF16;
+  const int st = validate_fwd(q, k, v, beta, g, h0, out, hT, B, H, T, dk, dv, n_h, chunk, dtype, a);
+  if (st != DELTA_OK || a.B * a.H == 0) return st;
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   cudaError_t err;
@@ -154,11 +221,70 @@ int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
     return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "state passthrough launch");
   }
   if (delta::chunk_tc_supports(a)) {
-    err = delta::launch_chunk_tc(a, s);
-    return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "tensor-core chunk kernel launch");
+    // the T tiles of every chunk live in stream-ordered scratch between the
+    // two passes and are released (stream-ordered) after the second
+    cudaMemPool_t pool;
+    if ((err = scratch_pool(&pool)) != cudaSuccess) return cuda_fail(err, "scratch pool");
+    void *t_mat = nullptr;
+    err = cudaMallocFromPoolAsync(&t_mat, (size_t)delta::ut_workspace_bytes(a), pool, s);
+    if (err != cudaSuccess) return cuda_fail(err, "scratch allocation");
+    err = delta::launch_ut(a, t_mat, s);
+    const char *what = "UT-pass kernel launch";
+    if (err == cudaSuccess) {
+      err = delta::launch_chunk_tc(a, t_mat, s);
+      what = "tensor-core chunk kernel launch";
+    }
+    const cudaError_t ef = cudaFreeAsync(t_mat, s);
+    if (err != cudaSuccess) return cuda_fail(err, what);
+    return ef == cudaSuccess ? DELTA_OK : cuda_fail(ef, "scratch release");
   }
   err = delta::launch_chunk_generic(a, s);
   return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "generic chunk kernel launch");
+}
+
+int delta_ut_transform(const void *k, const float *beta, const float *g, void *t_mat, int B,
+                       int H, int T, int dk, int n_h, int chunk, delta_dtype dtype,
+                       struct CUstream_st *stream) {
+  if (B < 0 || H < 0 || T < 0)
+    return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d T=%d", B, H, T);
+  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
+    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (n_h < 1 || n_h > 4) return fail(DELTA_ERR_UNSUPPORTED, "n_h=%d not in [1,4]", n_h);
+  if ((int64_t)B * H >= (int64_t(1) << 31))
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
+  delta::FwdArgs a{};
+  a.k = k; a.beta = beta; a.g = g;
+  a.B = B; a.H = H; a.T = T; a.L = (int64_t)T * n_h;
+  a.dk = dk; a.dv = dk; a.n_h = n_h; a.chunk = chunk;
+  a.bf16 = dtype == DELTA_BF16;
+  if (a.B * a.H == 0 || T == 0) return DELTA_OK;
+  if (!delta::ut_supports(a))
+    return fail(DELTA_ERR_UNSUPPORTED,
+                "the UT pass runs for bf16 keys with dk = 128 and chunk = 64 only");
+  if (!k || !beta) return fail(DELTA_ERR_INVALID, "k and beta must be non-NULL");
+  if (!aligned16(k) || !aligned16(beta) || !aligned16(g))
+    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+  int st;
+  if ((st = validate_t_mat(a, t_mat, false)) != DELTA_OK) return st;
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+  const cudaError_t err = delta::launch_ut(a, t_mat, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "UT-pass kernel launch");
+}
+
+int delta_fwd_with_ut(const void *q, const void *k, const void *v, const float *beta,
+                      const float *g, const float *h0, const void *t_mat, void *out, float *hT,
+                      int B, int H, int T, int dk, int dv, int n_h, int chunk, delta_dtype dtype,
+                      struct CUstream_st *stream) {
+  delta::FwdArgs a;
+  int st = validate_fwd(q, k, v, beta, g, h0, out, hT, B, H, T, dk, dv, n_h, chunk, dtype, a);
+  if (st != DELTA_OK || a.B * a.H == 0 || T == 0) return st;
+  if (!delta::chunk_tc_supports(a))
+    return fail(DELTA_ERR_UNSUPPORTED,
+                "the state pass runs for bf16 with dk = dv = 128 and chunk = 64 only");
+  if ((st = validate_t_mat(a, t_mat, true)) != DELTA_OK) return st;
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+  const cudaError_t err = delta::launch_chunk_tc(a, t_mat, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "tensor-core chunk kernel launch");
 }
 
 int delta_fwd_kernel_count(int B, int H, int T, int dk, int dv, int n_h, int chunk,

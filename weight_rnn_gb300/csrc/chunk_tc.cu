@@ -56,6 +56,7 @@
 
 #include "kernels.h"
 #include "sm100.cuh"
+#include "tc_common.cuh"
 #include "tma_host.h"
 
 namespace delta {
@@ -65,6 +66,7 @@ __device__ unsigned int g_tc_error = 0;
 
 namespace {
 using namespace sm100;
+using namespace tc;
 
 constexpr int C = 64;
 constexpr int D = 128;
@@ -75,28 +77,22 @@ __host__ __device__ constexpr bool dual_issue(bool gated) { return gated; }
 __host__ __device__ constexpr bool look_wu(bool gated) { return true; }  // W, U on warp 14
 __host__ __device__ constexpr bool look_g(bool gated) { return true; }   // G on warp 14
 __host__ __device__ constexpr int threads_for(bool gated) { return dual_issue(gated) ? 480 : 448; }
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLogGateFloor = -80.0f;
-// Down to this cumulative log2 gate within a chunk the decay factors are
-// formed as 2^gc_i * 2^-gc_j (no overflow); below it, exactly per entry.
-constexpr float kRatioFloor = -100.0f;
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ----
 constexpr uint32_t STAGE_BYTES = 49152;
 constexpr uint32_t ST_K0 = 0, ST_Q0 = 8192, ST_K1 = 16384, ST_Q1 = 24576;
 constexpr uint32_t ST_V0 = 32768;  // V (64 x 128), later Kd, same layout
 constexpr uint32_t OFF_MS = NS * STAGE_BYTES;  // (M-I)^T bf16 [128 j][128 i], MN-major B
-constexpr uint32_t OFF_TU = OFF_MS + 32768;    // T bf16 [64][64], K-major
-constexpr uint32_t OFF_TW = OFF_TU + 8192;     // T diag(exp gc)
+constexpr uint32_t OFF_TW = OFF_MS + 32768;    // T diag(exp gc) bf16 [64][64], K-major
 constexpr uint32_t OFF_P = OFF_TW + 8192;      // 2 x P bf16 [64][64], K-major
-constexpr uint32_t OFF_AX = OFF_P + 16384;     // A (upper, transposed) / X (lower) fp32 [64][64]
-constexpr uint32_t OFF_SM = OFF_AX + 16384;    // small arrays and barriers
+constexpr uint32_t OFF_TR = OFF_P + 16384;     // 2 x T bf16 [64][64] (TMA ring), K-major
+constexpr uint32_t OFF_SM = OFF_TR + 16384;    // small arrays and barriers
 constexpr uint32_t SM_BETA = 0;                // [NS][64]
 constexpr uint32_t SM_LAM = SM_BETA + NS * 256;  // [NS][64] log2 gate
 constexpr uint32_t SM_EG = SM_LAM + NS * 256;    // prep: 2^gc
 constexpr uint32_t SM_IEG = SM_EG + 256;         // prep: 2^-gc
-constexpr uint32_t SM_BGC = SM_IEG + 256;        // prep: beta 2^gc
-constexpr uint32_t SM_DEC = SM_BGC + 256;        // feed-forward: 2^(gc_C - gc)
+constexpr uint32_t SM_GC = SM_IEG + 256;         // prep: gc (cumulative log2 gate)
+constexpr uint32_t SM_DEC = SM_GC + 256;         // feed-forward: 2^(gc_C - gc)
 constexpr uint32_t SM_GQ = SM_DEC + 256;         // feed-forward: 2^gc at readout rows
 constexpr uint32_t SM_BAR = SM_GQ + 256;
 
@@ -105,9 +101,9 @@ enum {
   B_FULL = 0,        // [NS] producer -> all: K, Q tiles, beta, log gate loaded (count 2 + tx)
   B_EMPTY = NS,      // [NS] MMA -> producer: K, Q tiles of the stage consumed
   B_GFULL = 2 * NS,  // MMA -> prep: G in TMEM
-  B_GFREE,           // prep -> MMA: G read (one arrival per warp)
-  B_TFULL,           // prep -> MMA: T tiles and P written (per warp)
-  B_WFULL,           // MMA -> ff, prep: W^T, U^T in TMEM (T tiles consumed)
+  B_GFREE,           // prep -> MMA: G read (per P warp, 2)
+  B_TFULL,           // prep -> MMA: T diag(exp gc) and P written (per warp)
+  B_WFULL,           // MMA -> ff, prep: W^T, U^T in TMEM (T diag(exp gc) consumed)
   B_CWD,             // ff -> MMA: W^T, U^T bf16 in TMEM, Kd in smem (per warp)
   B_MFULL,           // MMA -> ff: (M-I)^T in TMEM
   B_MRDY,            // ff -> MMA: (M-I)^T in smem, TMEM free (per warp)
@@ -122,7 +118,9 @@ enum {
   B_DRAIN,           // MMA: everything issued has completed
   B_VFULL,           // [NS] producer -> MMA: the V tile of a stage loaded (count 1 + tx)
   B_VEMPTY = B_VFULL + NS,  // [NS] chain -> producer: V slot free (per warp; it stages the outputs)
-  NBARS = B_VEMPTY + NS
+  B_TRFULL = B_VEMPTY + NS,  // [2] producer -> prep: the chunk's T tile loaded (count 1 + tx)
+  B_TREMPTY = B_TRFULL + 2,  // [2] MMA -> producer: the T tile consumed (by the U product)
+  NBARS = B_TREMPTY + 2
 };
 constexpr uint32_t SM_MISC = SM_BAR + NBARS * 8;  // tmem slot, abort flag, gate of the chunk
 constexpr uint32_t SMEM_TOTAL = OFF_SM + SM_MISC + 16;
@@ -164,7 +162,6 @@ struct Smem {
   __device__ volatile int *keep_tmem() const {
     return reinterpret_cast<volatile int *>(base + OFF_SM + SM_MISC + 12);
   }
-  __device__ float *AX() const { return reinterpret_cast<float *>(base + OFF_AX); }
 };
 
 // Bounded wait that also gives up at once when another role has aborted.
@@ -205,294 +202,6 @@ __device__ __noinline__ bool wait_bar_drain(uint8_t *base, int idx, uint32_t par
   return false;
 }
 
-// fp32 64x64 matrices in shared memory are stored row-major with the column
-// XOR-swizzled by the row (bits 2..4), which keeps float4 runs along a row
-// contiguous and makes the tf32 MMA fragment loads below conflict-free.
-__device__ __forceinline__ int swz(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
-
-// The solve's 64x64 array holds A_ij (i > j) at (j, i) -- the upper triangle --
-// and X_ij = ((I + A)^{-1})_ij (i > j) at (i, j) -- the lower triangle.  The
-// diagonal holds the chunk's cumulative log gate (X_ii = 1 is implicit).
-__device__ __forceinline__ float ldA(const float *AX, int i, int j) { return AX[swz(j, i)]; }
-// X_rc of a block that touches the diagonal: 1 on it, 0 above it.
-__device__ __forceinline__ float ldXm(const float *M, int r, int c) {
-  const float v = M[swz(r, c)];
-  return r > c ? v : (r == c ? 1.f : 0.f);
-}
-
-// D(16x8) += A(16x8) B(8x8) on the warp-level tensor-core path, tf32 inputs
-// (fp32 bit patterns; the MMA ignores the low mantissa bits).
-// Fragments: a = {A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]},
-// b = {B[t][g], B[t+4][g]}, d = {D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1]}
-// with g = lane / 4, t = lane % 4.
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
-                                         const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// Operand fragments of the tf32 MMA read from the solve array.  KIND 0: a
-// block of A (stored transposed in the upper triangle); KIND 1: a block of X
-// that may touch the diagonal (1 on it, 0 above it).
-template <int KIND>
-__device__ __forceinline__ uint32_t lsol(const float *AX, int r, int c) {
-  return __float_as_uint(KIND == 0 ? ldA(AX, r, c) : ldXm(AX, r, c));
-}
-template <int KIND>
-__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float *AX, int r0, int k0, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  a[0] = lsol<KIND>(AX, r0 + g, k0 + t);
-  a[1] = lsol<KIND>(AX, r0 + g + 8, k0 + t);
-  a[2] = lsol<KIND>(AX, r0 + g, k0 + t + 4);
-  a[3] = lsol<KIND>(AX, r0 + g + 8, k0 + t + 4);
-}
-template <int KIND>
-__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float *AX, int k0, int n0, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  b[0] = lsol<KIND>(AX, k0 + t, n0 + g);
-  b[1] = lsol<KIND>(AX, k0 + t + 4, n0 + g);
-}
-// B fragment for k-step ks (rows 8 ks .. 8 ks + 7) of a matrix Y held as MMA
-// results: y[h] is the 16x8 accumulator of rows 16 h .. 16 h + 15.  Row r,
-// column c of a 16x8 accumulator lives in lane (r % 8) * 4 + c / 2, element
-// (r / 8) * 2 + c % 2: two candidates are shuffled in and one is kept.
-template <int NH>
-__device__ __forceinline__ void frag_b_acc(uint32_t (&b)[2], const float (&y)[NH][4], int ks,
-                                           int lane) {
-  const int g = lane >> 2, t = lane & 3, h = ks >> 1, e = (ks & 1) * 2;
-  const int s0 = t * 4 + (g >> 1), s1 = (t + 4) * 4 + (g >> 1);
-  const float a0 = __shfl_sync(0xffffffffu, y[h][e], s0);
-  const float a1 = __shfl_sync(0xffffffffu, y[h][e + 1], s0);
-  const float c0 = __shfl_sync(0xffffffffu, y[h][e], s1);
-  const float c1 = __shfl_sync(0xffffffffu, y[h][e + 1], s1);
-  b[0] = __float_as_uint((g & 1) ? a1 : a0);
-  b[1] = __float_as_uint((g & 1) ? c1 : c0);
-}
-
-// T_U[r][c] = x beta_c and T_W[r][c] = x beta_c exp(gc_c) (bf16 tiles).
-__device__ __forceinline__ void put_t(uint8_t *tu, uint8_t *tw, int r, int c, float x, float bc,
-                                      float wc) {
-  const uint32_t off = sw128_offset(r, c, 64);
-  *reinterpret_cast<__nv_bfloat16 *>(tu + off) = __float2bfloat16_rn(x * bc);
-  *reinterpret_cast<__nv_bfloat16 *>(tw + off) = __float2bfloat16_rn(x * wc);
-}
-
-// T tiles from a 16x8 fragment of (scale * D) at rows r0.., columns n0...
-__device__ __forceinline__ void frag_to_t(uint8_t *tu, uint8_t *tw, int r0, int n0,
-                                          const float (&d)[4], float scale, const float *beta,
-                                          const float *bgc, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  const int c = n0 + 2 * t;
-  const float b0 = beta[c], b1 = beta[c + 1], w0 = bgc[c], w1 = bgc[c + 1];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const float x0 = d[2 * hh] * scale, x1 = d[2 * hh + 1] * scale;
-    const int r = r0 + g + 8 * hh;
-    *reinterpret_cast<uint32_t *>(tu + sw128_offset(r, c, 64)) = pack_bf16(x0 * b0, x1 * b1);
-    *reinterpret_cast<uint32_t *>(tw + sw128_offset(r, c, 64)) = pack_bf16(x0 * w0, x1 * w1);
-  }
-}
-
-// Store a 16x8 fragment (scaled) into swizzled fp32 smem at (r0, n0).
-__device__ __forceinline__ void warp_store_16x8(float *M, int r0, int n0, const float (&d)[4],
-                                                float scale, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  M[swz(r0 + g, n0 + 2 * t)] = d[0] * scale;
-  M[swz(r0 + g, n0 + 2 * t + 1)] = d[1] * scale;
-  M[swz(r0 + g + 8, n0 + 2 * t)] = d[2] * scale;
-  M[swz(r0 + g + 8, n0 + 2 * t + 1)] = d[3] * scale;
-}
-
-// One warp inverts the unit lower-triangular 16x16 diagonal block at offset
-// o of (I + A): closed-form 4x4 leaves, then the merges 4 -> 8 -> 16, each
-// X21 = -X22 (A21 X11).  Every entry of A the warp needs is loaded at once;
-// the partial inverses move between lanes by shuffles, not through shared
-// memory.  X goes to the lower triangle of the solve array and, scaled, to
-// the T tiles.
-__device__ __forceinline__ void invert_diag16(float *AX, uint8_t *tu, uint8_t *tw,
-                                              const float *beta, const float *bgc, int o,
-                                              int lane) {
-  const unsigned full = 0xffffffffu;
-  // leaf lanes (0..11): leaf a, column cc;  merge-1 lanes: (hh, r4, c4);
-  // merge-2 lanes: (r8, c0 and c0 + 4)
-  const int a = lane < 12 ? lane / 3 : 0, cc = lane < 12 ? lane - 3 * (lane / 3) : 0;
-  const int b0 = o + 4 * a;
-  const int hh = lane >> 4, r4 = (lane >> 2) & 3, c4 = lane & 3, o8 = o + 8 * hh;
-  const int r8 = lane >> 2, c0 = lane & 3;
-  const float a10 = ldA(AX, b0 + 1, b0), a20 = ldA(AX, b0 + 2, b0), a21 = ldA(AX, b0 + 2, b0 + 1);
-  const float a30 = ldA(AX, b0 + 3, b0), a31 = ldA(AX, b0 + 3, b0 + 1), a32 = ldA(AX, b0 + 3, b0 + 2);
-  float am1[4], am2[8];
-#pragma unroll
-  for (int m = 0; m < 4; ++m) am1[m] = ldA(AX, o8 + 4 + r4, o8 + m);
-#pragma unroll
-  for (int m = 0; m < 8; ++m) am2[m] = ldA(AX, o + 8 + r8, o + m);
-
-  // ---- leaves: column cc of leaf a by forward substitution ----
-  const float x0 = cc == 0 ? 1.f : 0.f;
-  const float x1 = cc == 1 ? 1.f : (cc < 1 ? -(a10 * x0) : 0.f);
-  const float x2 = cc == 2 ? 1.f : (cc < 2 ? -fmaf(a21, x1, a20 * x0) : 0.f);
-  const float x3 = -fmaf(a32, x2, fmaf(a31, x1, a30 * x0));
-  if (lane < 12) {
-    const int col = b0 + cc;
-    const float bc = beta[col], wc = bgc[col];
-    if (cc < 1) {
-      AX[swz(b0 + 1, col)] = x1;
-      put_t(tu, tw, b0 + 1, col, x1, bc, wc);
-    }
-    if (cc < 2) {
-      AX[swz(b0 + 2, col)] = x2;
-      put_t(tu, tw, b0 + 2, col, x2, bc, wc);
-    }
-    AX[swz(b0 + 3, col)] = x3;
-    put_t(tu, tw, b0 + 3, col, x3, bc, wc);
-  }
-  if (lane < 16) put_t(tu, tw, o + lane, o + lane, 1.f, beta[o + lane], bgc[o + lane]);
-
-  // ---- 4 -> 8: X[o8+4+r4][o8+c4] ----
-  float xm1;
-  {
-    // X11 = leaf 2 hh, column c4 (lane 6 hh + c4); X11[m][c4] for m > c4
-    const int s11 = 6 * hh + c4;
-    const float u1 = __shfl_sync(full, x1, s11), u2 = __shfl_sync(full, x2, s11),
-                u3 = __shfl_sync(full, x3, s11);
-    const float xc[4] = {c4 == 0 ? 1.f : 0.f, c4 == 1 ? 1.f : (c4 < 1 ? u1 : 0.f),
-                         c4 == 2 ? 1.f : (c4 < 2 ? u2 : 0.f), c4 == 3 ? 1.f : u3};
-    float y = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) y = fmaf(am1[m], xc[m], y);
-    // Y[m][c4] from lane (hh, m, c4); X22[r4][m] = leaf 2 hh + 1, column m, row r4
-    float z = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const float ym = __shfl_sync(full, y, (lane & 16) | (m << 2) | c4);
-      float xr = 1.f;
-      if (m < 3) {
-        const int s22 = 6 * hh + 3 + m;
-        const float w1 = __shfl_sync(full, x1, s22), w2 = __shfl_sync(full, x2, s22),
-                    w3 = __shfl_sync(full, x3, s22);
-        xr = r4 == 1 ? w1 : (r4 == 2 ? w2 : w3);
-      }
-      if (m < r4) z = fmaf(xr, ym, z);
-      if (m == r4) z += ym;
-    }
-    xm1 = -z;
-    AX[swz(o8 + 4 + r4, o8 + c4)] = xm1;
-    put_t(tu, tw, o8 + 4 + r4, o8 + c4, xm1, beta[o8 + c4], bgc[o8 + c4]);
-  }
-
-  // ---- 8 -> 16: X[o+8+r8][o+c0] and X[o+8+r8][o+c0+4] ----
-  {
-    // column c0 of X11 = X[o..o+8][o..o+8]: rows < 4 from leaf 0 (lane c0),
-    // rows >= 4 from the 4 -> 8 merge (lane (0, m-4, c0))
-    const float u1 = __shfl_sync(full, x1, c0), u2 = __shfl_sync(full, x2, c0),
-                u3 = __shfl_sync(full, x3, c0);
-    // column c0 + 4: rows >= 4 from leaf 1 (lane 3 + c0)
-    const float v1 = __shfl_sync(full, x1, 3 + c0), v2 = __shfl_sync(full, x2, 3 + c0),
-                v3 = __shfl_sync(full, x3, 3 + c0);
-    float y0 = 0.f, y1 = 0.f;
-    const float lo[4] = {c0 == 0 ? 1.f : 0.f, c0 == 1 ? 1.f : (c0 < 1 ? u1 : 0.f),
-                         c0 == 2 ? 1.f : (c0 < 2 ? u2 : 0.f), c0 == 3 ? 1.f : u3};
-    const float hi[4] = {c0 == 0 ? 1.f : 0.f, c0 == 1 ? 1.f : (c0 < 1 ? v1 : 0.f),
-                         c0 == 2 ? 1.f : (c0 < 2 ? v2 : 0.f), c0 == 3 ? 1.f : v3};
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      y0 = fmaf(am2[m], lo[m], y0);
-      const float wm = __shfl_sync(full, xm1, (m << 2) | c0);
-      y0 = fmaf(am2[m + 4], wm, y0);
-      y1 = fmaf(am2[m + 4], hi[m], y1);
-    }
-    // X22 = X[o+8..o+16][o+8..o+16]: rows < 4 from leaf 2, rows >= 4 from
-    // leaf 3 (same columns) or, for columns < 4, from the 4 -> 8 merge (hh 1)
-    float z0 = 0.f, z1 = 0.f;
-    const int rr = r8 & 3;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float ya = __shfl_sync(full, y0, (m << 2) | c0);
-      const float yb = __shfl_sync(full, y1, (m << 2) | c0);
-      float xr;
-      if ((m & 3) < 3) {
-        // leaf 2 (r8 < 4) or leaf 3 (r8 >= 4), column m & 3, row r8 & 3
-        const int sl = (r8 < 4 ? 6 : 9) + (m & 3);
-        const float w1 = __shfl_sync(full, x1, sl), w2 = __shfl_sync(full, x2, sl),
-                    w3 = __shfl_sync(full, x3, sl);
-        xr = rr == 1 ? w1 : (rr == 2 ? w2 : w3);
-      } else {
-        xr = 0.f;
-      }
-      if (m < 4) {
-        const float xq = __shfl_sync(full, xm1, 16 | ((r8 & 3) << 2) | m);
-        if (r8 >= 4) xr = xq;
-      }
-      if (m < r8) {
-        z0 = fmaf(xr, ya, z0);
-        z1 = fmaf(xr, yb, z1);
-      }
-      if (m == r8) {
-        z0 += ya;
-        z1 += yb;
-      }
-    }
-    AX[swz(o + 8 + r8, o + c0)] = -z0;
-    AX[swz(o + 8 + r8, o + c0 + 4)] = -z1;
-    put_t(tu, tw, o + 8 + r8, o + c0, -z0, beta[o + c0], bgc[o + c0]);
-    put_t(tu, tw, o + 8 + r8, o + c0 + 4, -z1, beta[o + c0 + 4], bgc[o + c0 + 4]);
-  }
-}
-
-// 2^x on the MUFU unit (relative error ~2^-22; flushes to 0 far below 1)
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ void named_sync(int id) {
-  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
-}
-
-// Named barrier over 128 threads that also ORs `cond` across them, so that
-// every participant takes the same decision (used to leave a loop together
-// once any role has aborted).
-__device__ __forceinline__ bool named_sync_or(int id, bool cond) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %2, 0;\n\t"
-      "bar.red.or.pred q, %1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(id), "r"((uint32_t)cond)
-      : "memory");
-  return r != 0;
-}
-
-// One arrival per warp once every lane's prior work (fenced by the caller) is
-// done: the warp converges, then lane 0 arrives.
-__device__ __forceinline__ void arrive_warp(uint64_t *bar, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
-}
-
-// Inclusive prefix sum over the 64 log-gate entries of a chunk, per warp:
-// lane holds entries lane and lane + 32.
-__device__ __forceinline__ void warp_scan64(const float *lam, int lane, float &lo, float &hi) {
-  lo = lam[lane];
-  hi = lam[lane + 32];
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float a = __shfl_up_sync(0xffffffffu, lo, o);
-    const float c = __shfl_up_sync(0xffffffffu, hi, o);
-    if (lane >= o) {
-      lo += a;
-      hi += c;
-    }
-  }
-  hi += __shfl_sync(0xffffffffu, lo, 31);
-}
-
 // 16-byte shared-memory load at a 32-bit shared address
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
@@ -521,7 +230,8 @@ struct Rows {
 template <bool GATED>
 __global__ void __launch_bounds__(threads_for(GATED), 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                const __grid_constant__ CUtensorMap map_v, TcParams p) {
+                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_t,
+                TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem sm;
   // pointer arithmetic on the shared array (not integer casts) keeps every
@@ -551,9 +261,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(sm.bar(B_EMPTY + s), 1);
       mbar_init(sm.bar(B_VEMPTY + s), 4);
     }
-    const int cnt[B_VFULL - 2 * NS] = {1, 4, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, dual_issue(GATED) ? 2 : 1};
+    const int cnt[B_VFULL - 2 * NS] = {1, 2, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, dual_issue(GATED) ? 2 : 1};
     for (int i = 2 * NS; i < B_VFULL; ++i) mbar_init(sm.bar(i), cnt[i - 2 * NS]);
     for (int s = 0; s < NS; ++s) mbar_init(sm.bar(B_VFULL + s), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sm.bar(B_TRFULL + s), 1);
+      mbar_init(sm.bar(B_TREMPTY + s), 1);
+    }
     *sm.abort_flag() = 0;
     fence_mbar_init();
   }
@@ -565,6 +279,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(&map_t);
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -592,7 +307,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
     };
     fetch(0);
-    int issued = 0, issued_v = 0;
+    int issued = 0, issued_v = 0, issued_t = 0;
+    const int tc0 = bh * NT;  // this head's first chunk in the T tensor
     for (int n = 0; n < NT; ++n) {
       const int s = n % NS;
       int ok = 1;
@@ -611,6 +327,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           tma_prefetch_4d(&map_v, 64, h, pe, b);
           tma_prefetch_4d(&map_q, 0, h, pt, b);
           tma_prefetch_4d(&map_q, 64, h, pt, b);
+          tma_prefetch_3d(&map_t, 0, 0, tc0 + pf);
         }
         // K and Q first, on their own barrier (the G product waits for them
         // only); V, needed later, on a second one
@@ -640,6 +357,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         tma_load_4d(st + ST_V0 + 8192, &map_v, vb, 64, h, e0, b);
       }
       issued_v = n + 1;
+      // T of the chunk (written by the UT pass) into its 2-slot ring; the U
+      // product of the chunk two back is its last reader
+      if (n >= 2 && lane == 0) ok = wait_bar(sm, B_TREMPTY + (n & 1), ((n >> 1) - 1) & 1, 0);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane == 0) {
+        uint64_t *tb = sm.bar(B_TRFULL + (n & 1));
+        mbar_arrive_expect_tx(tb, 8192u);
+        tma_load_3d(sm.base + OFF_TR + (n & 1) * 8192, &map_t, tb, 0, 0, tc0 + n);
+      }
+      issued_t = n + 1;
       fetch(n + 1);
     }
     // copies still in flight must land before the CTA's shared memory goes
@@ -648,6 +375,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         wait_bar_drain(sm.base, B_FULL + n % NS, (n / NS) & 1, 0);
       for (int n = (issued_v > NS ? issued_v - NS : 0); n < issued_v; ++n)
         wait_bar_drain(sm.base, B_VFULL + n % NS, (n / NS) & 1, 0);
+      for (int n = (issued_t > 2 ? issued_t - 2 : 0); n < issued_t; ++n)
+        wait_bar_drain(sm.base, B_TRFULL + (n & 1), (n >> 1) & 1, 0);
     }
     __syncwarp();
   } else if (warp == 1 || (dual_issue(GATED) && warp == 14)) {
@@ -669,7 +398,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       constexpr uint32_t id_op = idesc_bf16(128, 64, false, false);       // B = P
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);        // B = (M-I)^T or Kd, MN-major
       constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);        // B = Q' (K-major)
-      const uint32_t a_tu = smem_u32(sm.base + OFF_TU), a_tw = smem_u32(sm.base + OFF_TW);
+      const uint32_t a_tr = smem_u32(sm.base + OFF_TR), a_tw = smem_u32(sm.base + OFF_TW);
       const uint32_t a_ms = smem_u32(sm.base + OFF_MS), a_p = smem_u32(sm.base + OFF_P);
       auto rdy = [&](int idx, int k) -> bool { return mbar_test_wait(sm.bar(idx), k & 1); };
       auto kd_desc = [&](int m, int k) -> uint64_t {  // B = Kd (gated: V slot) or K
@@ -736,24 +465,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mma_ts(tmem + TM_O, tmem + TM_WB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_q, k > 0);
           mma_commit(sm.bar(B_QFULL));
         } else if (do_wu && c_w < NT && c_w == c_u && rdy(B_TFULL, c_w) && (c_w == 0 || rdy(B_MRDY, c_w - 1))) {
-          // ---- W^T = K^T (T diag exp gc)^T ----
+          // ---- W^T = K^T (T diag exp gc)^T (ungated: T itself) ----
           const int m = c_w++;
           tc_fence_after();
           const uint32_t kq = smem_u32(sm.stage(m % NS));
+          const uint32_t wb = GATED ? a_tw : a_tr + (m & 1) * 8192;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_X1, sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024),
-                   sdesc_sw128(a_tw + k * 32, 0, 1024), id_uw, k > 0);
+                   sdesc_sw128(wb + k * 32, 0, 1024), id_uw, k > 0);
         } else if (do_wu && c_u < c_w && rdy(B_VFULL + c_u % NS, c_u / NS)) {
           // ---- U^T = V^T T^T ----
           const int m = c_u++;
           tc_fence_after();
           const uint32_t kq = smem_u32(sm.stage(m % NS));
+          const uint32_t tb = a_tr + (m & 1) * 8192;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_X1 + 64, sdesc_sw128(kq + ST_V0 + k * 2048, 8192, 1024),
-                   sdesc_sw128(a_tu + k * 32, 0, 1024), id_uw, k > 0);
+                   sdesc_sw128(tb + k * 32, 0, 1024), id_uw, k > 0);
           mma_commit(sm.bar(B_WFULL));
+          mma_commit(sm.bar(B_TREMPTY + (m & 1)));
         } else if (do_g && c_g2 < 2 * NT && ((c_g2 & 1) ||
                                      (rdy(B_FULL + (c_g2 >> 1) % NS, (c_g2 >> 1) / NS) &&
                                       (c_g2 == 0 || rdy(B_GFREE, (c_g2 >> 1) - 1))))) {
@@ -789,63 +521,45 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncwarp();
   } else if (warp < 6) {
     // ===================================================== prep warps
+    // warps 2, 3 (TMEM lanes 64..127): P from rows 64..127 of G;
+    // warps 4, 5: the T tile of the UT pass, scaled to T diag(exp gc) for the
+    // W product (gated; ungated the W product reads T itself)
     const int q4 = warp & 3;              // TMEM lane quarter
     const int L = q4 * 32 + lane;         // TMEM lane of this thread
-    const int pw = warp - 2;              // 0..3
-    const int pt = tid - 64;              // 0..127 within the group
-    float *AX = sm.AX();
-    float *eg = sm.arr(SM_EG), *ieg = sm.arr(SM_IEG), *bgc = sm.arr(SM_BGC);
-    uint8_t *tu = sm.base + OFF_TU;
-    uint8_t *tw = sm.base + OFF_TW;
+    float *eg = sm.arr(SM_EG), *ieg = sm.arr(SM_IEG), *gcs = sm.arr(SM_GC);
     for (int m = 0; m < NT; ++m) {
       const int s = m % NS;
-      // every warp of the group is done with the previous chunk (its gate
-      // factors and beta exp(gc) are rewritten below)
+      // every warp of the group is done with the previous chunk's gate
+      // factors (they are rewritten below)
       if (named_sync_or(1, *sm.abort_flag() != 0)) break;
       // a failed wait sets the abort flag; every thread still reaches the
       // next named barrier and all of them leave together after it
       wait_bar(sm, B_FULL + s, (m / NS) & 1, 2);
-      const float *sb = sm.beta(s);
       if (GATED && warp == 2) {
         float lo, hi;
         warp_scan64(sm.lam(s), lane, lo, hi);
-        AX[swz(lane, lane)] = lo;
-        AX[swz(lane + 32, lane + 32)] = hi;
-        const float e0 = fast_exp2(lo), e1 = fast_exp2(hi);
-        eg[lane] = e0;
-        eg[lane + 32] = e1;
+        gcs[lane] = lo;
+        gcs[lane + 32] = hi;
+        eg[lane] = fast_exp2(lo);
+        eg[lane + 32] = fast_exp2(hi);
         ieg[lane] = fast_exp2(-lo);
         ieg[lane + 32] = fast_exp2(-hi);
-        bgc[lane] = sb[lane] * e0;
-        bgc[lane + 32] = sb[lane + 32] * e1;
       }
-      if (!GATED && pt < 64) bgc[pt] = sb[pt];
       if (named_sync_or(1, *sm.abort_flag() != 0)) break;
-      const Rows rw(m, n_h, p.T);
-      // exact per-entry decay only when the chunk's gate product leaves the
-      // range of the ratio form
-      const bool ratio = !GATED || AX[swz(63, 63)] >= kRatioFloor;
-
-      // the P buffer is rewritten from here on
-      if (m >= 2) wait_bar(sm, B_PFREE0 + (m & 1), ((m >> 1) - 1) & 1, 2);
-      // ---- one row of G = [K;Q] K^T per thread (TMEM lane L), 16 columns at a time:
-      //      rows 0..63 give A (upper triangle of the solve array, transposed),
-      //      rows 64..127 give P ----
-      wait_bar(sm, B_GFULL, m & 1, 2);
-      tc_fence_after();
-      {
-        const int i = L, r = L - 64;
-        const bool arow = L < 64;
-        const float bi = arow ? sb[i] : 0.f;
-        const float gi = (GATED && arow) ? AX[swz(i, i)] : 0.f;
-        const float bie = (GATED && arow) ? bi * eg[i] : bi;
-        const int pos = (!arow && r < rw.Cp) ? rw.pos(r, n_h) : -1;
-        const float gp = (GATED && pos >= 0) ? AX[swz(pos, pos)] : 0.f;
+      if (warp < 4) {
+        // ---- P = Q K^T * Gam * M: one readout row per thread, 16 columns
+        //      at a time, into the P buffer of this chunk ----
+        const Rows rw(m, n_h, p.T);
+        // exact per-entry decay only when the chunk's gate product leaves
+        // the range of the ratio form (uniform per chunk)
+        const bool ratio = !GATED || gcs[63] >= kRatioFloor;
+        if (m >= 2) wait_bar(sm, B_PFREE0 + (m & 1), ((m >> 1) - 1) & 1, 2);
+        wait_bar(sm, B_GFULL, m & 1, 2);
+        tc_fence_after();
+        const int r = L - 64;
+        const int pos = r < rw.Cp ? rw.pos(r, n_h) : -1;
+        const float gp = (GATED && pos >= 0) ? gcs[pos] : 0.f;
         const float ep = (GATED && pos >= 0) ? eg[pos] : 1.f;
-        // entry (row, j) = G(row, j) * f_j: f_j = bx (ungated); rf 2^-gc_j
-        // (the ratio form, while the chunk's gate product stays in range);
-        // else bx 2^(gr - gc_j) exactly.  The branch is uniform per chunk.
-        const float bx = arow ? bi : 1.f, rf = arow ? bie : ep, gr = arow ? gi : gp;
         uint8_t *prow = sm.base + OFF_P + (m & 1) * 8192;
 #pragma unroll 1
         for (int jb = 0; jb < 64; jb += 16) {
@@ -854,109 +568,62 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           float cf[16];
           if (!GATED) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) cf[jj] = bx;
+            for (int jj = 0; jj < 16; ++jj) cf[jj] = 1.f;
           } else if (ratio) {
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {
               const float4 e4 = *reinterpret_cast<const float4 *>(ieg + jb + jj);
-              cf[jj] = rf * e4.x;
-              cf[jj + 1] = rf * e4.y;
-              cf[jj + 2] = rf * e4.z;
-              cf[jj + 3] = rf * e4.w;
+              cf[jj] = ep * e4.x;
+              cf[jj + 1] = ep * e4.y;
+              cf[jj + 2] = ep * e4.z;
+              cf[jj + 3] = ep * e4.w;
             }
           } else {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) cf[jj] = bx * fast_exp2(gr - AX[swz(jb + jj, jb + jj)]);
+            for (int jj = 0; jj < 16; ++jj) cf[jj] = fast_exp2(gp - gcs[jb + jj]);
           }
           tmem_wait_ld_regs(g);
-          if (arow) {
+          uint32_t pk[8];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int j = jb + jj;
-              if (j < i) AX[swz(j, i)] = cf[jj] * __uint_as_float(g[jj]);
-            }
-          } else {
-            uint32_t pk[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int j = jb + 2 * u;
-              const float v0 = j <= pos ? __uint_as_float(g[2 * u]) * cf[2 * u] : 0.f;
-              const float v1 = j + 1 <= pos ? __uint_as_float(g[2 * u + 1]) * cf[2 * u + 1] : 0.f;
-              pk[u] = pack_bf16(v0, v1);
-            }
-            st_chunk(prow + sw128_offset(r, jb, 64), {pk[0], pk[1], pk[2], pk[3]});
-            st_chunk(prow + sw128_offset(r, jb + 8, 64), {pk[4], pk[5], pk[6], pk[7]});
+          for (int u = 0; u < 8; ++u) {
+            const int j = jb + 2 * u;
+            const float v0 = j <= pos ? __uint_as_float(g[2 * u]) * cf[2 * u] : 0.f;
+            const float v1 = j + 1 <= pos ? __uint_as_float(g[2 * u + 1]) * cf[2 * u + 1] : 0.f;
+            pk[u] = pack_bf16(v0, v1);
           }
+          st_chunk(prow + sw128_offset(r, jb, 64), {pk[0], pk[1], pk[2], pk[3]});
+          st_chunk(prow + sw128_offset(r, jb + 8, 64), {pk[4], pk[5], pk[6], pk[7]});
         }
         tc_fence_before();
         arrive_warp(sm.bar(B_GFREE), lane);
-      }
-      if (named_sync_or(1, *sm.abort_flag() != 0)) break;  // A complete
-
-      // ---- X = (I + A)^{-1}: 16x16 diagonal blocks, one per warp; the T
-      //      tiles are rewritten from here on ----
-      if (m >= 1) wait_bar(sm, B_WFULL, (m - 1) & 1, 2);
-      invert_diag16(AX, tu, tw, sb, bgc, 16 * pw, lane);
-      named_sync(1);
-      {
-        // ---- merge 16 -> 32: X21 = -X22 (A21 X11) in each 32-row half;
-        //      warp = (half, 8-column slab), the product A21 X11 stays in registers ----
-        const int o = 32 * (pw >> 1), n0 = o + 8 * (pw & 1);
-        uint32_t fa[2][4], fx[2][2], fz[2][4];
+      } else {
+        // ---- the T tile of this chunk (UT pass) has landed; gated, T diag(exp gc)
+        //      into its own buffer, free once the previous chunk's W and U ended ----
+        wait_bar(sm, B_TRFULL + (m & 1), (m >> 1) & 1, 2);
+        if (GATED) {
+          if (m >= 1) wait_bar(sm, B_WFULL, (m - 1) & 1, 2);
+          const uint8_t *tt = sm.base + OFF_TR + (m & 1) * 8192;
+          uint8_t *tw = sm.base + OFF_TW;
+          const int ft = tid - 128;  // 0..63
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          frag_a<0>(fa[ks], AX, o + 16, o + 8 * ks, lane);
-          frag_b<1>(fx[ks], AX, o + 8 * ks, n0, lane);
-          frag_a<1>(fz[ks], AX, o + 16, o + 16 + 8 * ks, lane);
-        }
-        float y[1][4] = {{0.f, 0.f, 0.f, 0.f}}, z[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int it = 0; it < 8; ++it) {
+            // 16-byte piece qi of the swizzled tile: row qi / 8, columns
+            // 8 ((qi % 8) ^ (row % 8)) .. + 7
+            const int qi = ft + 64 * it, row = qi >> 3;
+            const int c0 = 8 * ((qi & 7) ^ (row & 7));
+            const uint4 v = *reinterpret_cast<const uint4 *>(tt + qi * 16);
+            const float4 e0 = *reinterpret_cast<const float4 *>(eg + c0);
+            const float4 e1 = *reinterpret_cast<const float4 *>(eg + c0 + 4);
+            const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o4[4];
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) mma_tf32(y[0], fa[ks], fx[ks]);
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          uint32_t bb[2];
-          frag_b_acc<1>(bb, y, ks, lane);
-          mma_tf32(z, fz[ks], bb);
-        }
-        warp_store_16x8(AX, o + 16, n0, z, -1.f, lane);
-        frag_to_t(tu, tw, o + 16, n0, z, -1.f, sb, bgc, lane);
-      }
-      named_sync(1);
-      {
-        // ---- merge 32 -> 64: rows 32..63, columns 8 pw .. 8 pw + 7 of X,
-        //      straight into the T tiles ----
-        const int n0 = 8 * pw;
-        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-          uint32_t fa[2][4][4], fx[4][2];
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            frag_b<1>(fx[ks], AX, 8 * ks, n0, lane);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) frag_a<0>(fa[mt][ks], AX, 32 + 16 * mt, 8 * ks, lane);
-          }
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) mma_tf32(y[mt], fa[mt][ks], fx[ks]);
-        }
-        float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-          uint32_t fz[2][4][4];
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) frag_a<1>(fz[mt][ks], AX, 32 + 16 * mt, 32 + 8 * ks, lane);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            uint32_t bb[2];
-            frag_b_acc<2>(bb, y, ks, lane);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) mma_tf32(z[mt], fz[mt][ks], bb);
+            for (int u = 0; u < 4; ++u)
+              o4[u] = pack_bf16(__uint_as_float(in[u] << 16) * ev[2 * u],
+                                __uint_as_float(in[u] & 0xFFFF0000u) * ev[2 * u + 1]);
+            st_chunk(tw + qi * 16, o4);
           }
         }
-        frag_to_t(tu, tw, 32, n0, z[0], -1.f, sb, bgc, lane);
-        frag_to_t(tu, tw, 48, n0, z[1], -1.f, sb, bgc, lane);
       }
       fence_proxy_async_smem();
       arrive_warp(sm.bar(B_TFULL), lane);
@@ -1273,8 +940,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 }  // namespace
 
 bool chunk_tc_supports(const FwdArgs &a) {
-  return a.bf16 && a.dk == D && a.dv == D && a.chunk == C && a.T > 0 &&
-         a.L < (int64_t(1) << 30) && a.B * a.H < (int64_t(1) << 31);
+  return a.bf16 && a.dk == D && a.dv == D && a.chunk == C && a.T > 0 && ut_supports(a);
 }
 
 namespace {
@@ -1308,14 +974,17 @@ cudaError_t read_and_clear_tc_error(unsigned int *word) {
   return cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(unsigned int));
 }
 
-cudaError_t launch_chunk_tc(const FwdArgs &a, cudaStream_t s) {
+cudaError_t launch_chunk_tc(const FwdArgs &a, const void *t_mat, cudaStream_t s) {
   if (!chunk_tc_supports(a)) return cudaErrorNotSupported;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mt;
   const uint32_t qr = a.n_h == 1 ? 64 : 32;
+  const int nt = (int)((a.L + C - 1) / C);
   cudaError_t e;
   if ((e = make_map_4d_bf16(&mq, a.q, D, a.H, a.T, a.B, 64, 1, qr, 1, true)) != cudaSuccess) return e;
   if ((e = make_map_4d_bf16(&mk, a.k, D, a.H, a.L, a.B, 64, 1, 64, 1, true)) != cudaSuccess) return e;
   if ((e = make_map_4d_bf16(&mv, a.v, D, a.H, a.L, a.B, 64, 1, 64, 1, true)) != cudaSuccess) return e;
+  if ((e = make_map_3d_bf16_sw128(&mt, t_mat, C, C, (uint64_t)(a.B * a.H * nt), C, C, 1)) != cudaSuccess)
+    return e;
   TcParams p;
   p.beta = a.beta;
   p.g = a.g;
@@ -1326,11 +995,11 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, cudaStream_t s) {
   p.T = (int)a.T;
   p.L = (int)a.L;
   p.n_h = a.n_h;
-  p.nchunks = (int)((a.L + C - 1) / C);
+  p.nchunks = nt;
   auto kern = a.g ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)(a.B * a.H), threads_for(a.g != nullptr), SMEM_ALLOC, s>>>(mq, mk, mv, p);
+  kern<<<(unsigned)(a.B * a.H), threads_for(a.g != nullptr), SMEM_ALLOC, s>>>(mq, mk, mv, mt, p);
   return cudaGetLastError();
 }
 

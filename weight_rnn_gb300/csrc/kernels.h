@@ -34,16 +34,25 @@ struct StepArgs {
 cudaError_t launch_chunk_generic(const FwdArgs &a, cudaStream_t s);
 
 // Tensor-core chunked forward (tcgen05 + TMEM + TMA) for bf16 I/O with
-// dk = dv = 128 and chunk = 64.  Returns cudaErrorNotSupported when the
-// shape is outside that set.
-cudaError_t launch_chunk_tc(const FwdArgs &a, cudaStream_t s);
+// dk = dv = 128 and chunk = 64: the state pass, given the T tiles the UT pass
+// (launch_ut) wrote to t_mat.  Returns cudaErrorNotSupported when the shape
+// is outside that set.
+cudaError_t launch_chunk_tc(const FwdArgs &a, const void *t_mat, cudaStream_t s);
 bool chunk_tc_supports(const FwdArgs &a);
-// kernels one tensor-core forward launches
-constexpr int kChunkTcKernels = 1;
+// kernels one tensor-core forward launches (UT pass + state pass)
+constexpr int kChunkTcKernels = 2;
 
-// Read and clear the word the tensor-core kernel sets when one of its bounded
-// waits gives up (0 = no error).  Synchronises the device.
+// The intra-chunk UT transform T = (I + A)^{-1} diag(beta) of every chunk,
+// bf16 [B*H*NT][64][64] row-major (tensor cores; bf16 keys, dk = 128,
+// chunk = 64).  t_mat must hold ut_workspace_bytes(a) bytes, 16-byte aligned.
+bool ut_supports(const FwdArgs &a);
+int64_t ut_workspace_bytes(const FwdArgs &a);
+cudaError_t launch_ut(const FwdArgs &a, void *t_mat, cudaStream_t s);
+
+// Read and clear the word the tensor-core kernels set when one of their
+// bounded waits gives up (0 = no error).  Synchronises the device.
 cudaError_t read_and_clear_tc_error(unsigned int *word);
+cudaError_t read_and_clear_ut_error(unsigned int *word);
 
 // One warp waits, at most `polls` tries, on a barrier that nothing completes,
 // then records its giving up in the same device error word.

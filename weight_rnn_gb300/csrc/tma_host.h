@@ -44,4 +44,21 @@ inline cudaError_t make_map_4d_bf16(CUtensorMap *map, const void *base, uint64_t
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// A 3-D bf16 tensor [d2][d1][d0] (d0 innermost, contiguous) tiled with a
+// box {b0, b1, b2} and the 128-byte swizzle (b0 * 2 must be <= 128).
+inline cudaError_t make_map_3d_bf16_sw128(CUtensorMap *map, const void *base, uint64_t d0,
+                                          uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
+                                          uint32_t b2) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};  // bytes, dims 1..2
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                   strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace delta
