@@ -61,7 +61,8 @@ ORDER = (3, 2, 4, 5)
 SPEC_HBM_GBS = 7900.0  # GB300 nominal HBM3e bandwidth
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
-    "fwd": ["weight_rnn_gb300/csrc/chunk_tc.cu", "weight_rnn_gb300/csrc/chunk_generic.cu"],
+    "fwd": ["weight_rnn_gb300/csrc/chunk_tc.cu", "weight_rnn_gb300/csrc/ut_tc.cu"],
+    "ut": ["weight_rnn_gb300/csrc/ut_tc.cu"],
     "step": ["weight_rnn_gb300/csrc/step.cu"],
 }
 
@@ -196,8 +197,9 @@ class ClockSampler:
             for name, val in zip(names[1:], parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
-        # samples under load: power well above the idle floor
-        loaded = [s for s, p in zip(sm, power) if power and p > min(power) + 100.0]
+        # samples under load: power well above the first sample's, taken while
+        # the GPU was still idle (before the warm-up steps)
+        loaded = [s for s, p in zip(sm, power) if power and p > power[0] + 50.0]
         return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm),
@@ -406,6 +408,45 @@ def measure(w, wr, dist, dev, args, peaks, peak_src, clocks_on):
     ms_per_step = 1e3 * elapsed / args.steps
     value = tokens * dist.world * args.steps / elapsed
 
+    # ---- the two passes of the tensor-core forward timed one by one, through
+    #      their own entry points (caller-held T), CUDA events around each ----
+    passes = None
+    if not decode and launches == 2:
+        nt = -(-(w.T * w.n_h) // w.chunk)
+        t_mat = torch.empty((w.B, w.H, nt, w.chunk, w.chunk), dtype=torch.bfloat16, device=dev)
+        pe = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for _ in range(2):
+            wr.delta_ut_transform(d["k"], d["beta"], d["g"], t_mat, n_h=w.n_h, chunk=w.chunk)
+            wr.delta_fwd_with_ut(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], t_mat, out,
+                                 hT, n_h=w.n_h, chunk=w.chunk)
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            pe[i][0].record(stream)
+            wr.delta_ut_transform(d["k"], d["beta"], d["g"], t_mat, n_h=w.n_h, chunk=w.chunk)
+            pe[i][1].record(stream)
+            wr.delta_fwd_with_ut(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], t_mat, out,
+                                 hT, n_h=w.n_h, chunk=w.chunk)
+            pe[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        ut_s = dist.max(sum(a.elapsed_time(b) for a, b, _ in pe) / 1e3 / args.steps, dev)
+        st_s = dist.max(sum(b.elapsed_time(c) for _, b, c in pe) / 1e3 / args.steps, dev)
+        e = 2 if w.dtype == "bf16" else 4
+        L = w.T * w.n_h
+        t_bytes = t_mat.numel() * 2
+        ut_bytes = (w.B * L * w.H * (w.dk * e + 4) + (w.B * w.T * w.H * 4 if w.gated else 0)
+                    + t_bytes)
+        st_bytes = kbytes + t_bytes
+        passes = {
+            "ut_pass": {"kernel": "ut_kernel", "us": ut_s * 1e6, "share": ut_s / (ut_s + st_s),
+                        "bytes_moved": ut_bytes, "gbs": ut_bytes / ut_s / 1e9,
+                        "traffic": read_traffic("ut", w.name)},
+            "state_pass": {"kernel": "chunk_tc_kernel", "us": st_s * 1e6,
+                           "share": st_s / (ut_s + st_s), "bytes_moved": st_bytes,
+                           "gbs": st_bytes / st_s / 1e9, "traffic": read_traffic(kind, w.name)},
+            "extra_bytes_vs_algorithmic": ut_bytes + t_bytes,
+        }
+        del t_mat
+
     # ---- end to end through the public API with pinned host buffers:
     #      batch slices on two streams, so that the copies of one slice
     #      overlap the kernels of another ----
@@ -468,6 +509,8 @@ def measure(w, wr, dist, dev, args, peaks, peak_src, clocks_on):
             "kernels_per_step": launches,
             "peak_source": f"hbm_gbs of {peak_src}",
             "spec_peak": SPEC_HBM_GBS, "frac_of_spec_peak": achieved / SPEC_HBM_GBS}
+    if passes:
+        roof["passes"] = passes
     if kflops is not None:
         tc = float(peaks["bf16_tflops"])
         t_tc = kflops / (tc * 1e12)
@@ -533,6 +576,7 @@ def run_ours(args, dist):
                 "roofline_frac": recs[i]["roofline"]["frac"],
                 "frac_of_spec_peak": recs[i]["roofline"]["frac_of_spec_peak"],
                 "kernel_us": recs[i]["roofline"]["kernel_us"],
+                "passes": recs[i]["roofline"].get("passes"),
                 "traffic": recs[i]["roofline"]["traffic"],
                 "algorithmic_bytes_per_launch":
                     recs[i]["roofline"]["algorithmic_bytes_per_launch"],

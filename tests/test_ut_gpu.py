@@ -6,10 +6,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import weight_rnn_gb300 as wr
 from oracle import forms
 from weight_rnn_gb300 import synth
-from parity import check_full, compare, gpu_fwd, to_np
+from parity import check_full, gpu_fwd, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -55,11 +56,30 @@ def gpu_t(inp, w):
     return t
 
 
+def compare_t(x, ref, what="T"):
+    """T against the oracle: the global relative L2 bound of every bf16
+    comparison (2e-2), and per chunk no entry off by more than 2e-2 of the
+    chunk's largest entry.  The entries are rounded to bf16 (relative 2^-9)
+    after a float32 solve whose block merges run on tf32 inputs (2^-11), and
+    many entries are exactly 0, so a bound relative to the RMS of the whole
+    tensor would be meaningless here."""
+    x = np.asarray(x, np.float64)
+    assert x.shape == ref.shape, (what, x.shape, ref.shape)
+    assert np.isfinite(x).all(), f"{what}: non-finite values"
+    rel = oracle.rel_l2(x, ref)
+    assert rel <= 2e-2, f"{what}: rel-L2 {rel:.3e} > 2e-2"
+    err = np.abs(x - ref).reshape(-1, ref.shape[-2] * ref.shape[-1]).max(axis=1)
+    scale = np.abs(ref).reshape(-1, ref.shape[-2] * ref.shape[-1]).max(axis=1)
+    bad = err > 2e-2 * scale + 1e-30
+    assert not bad.any(), (f"{what}: {int(bad.sum())} chunks with max |err| > 2e-2 max |T|, "
+                           f"worst {float((err / np.maximum(scale, 1e-30)).max()):.3e}")
+    return rel
+
+
 def check_t(inp, w):
     t = gpu_t(inp, w)
     ref = oracle_t(inp, w)
-    assert t.shape == ref.shape
-    compare(to_np(t), ref, "bf16", "T")
+    compare_t(to_np(t), ref)
     # identity steps past the end of the sequence: zero rows and columns
     L = w.T * w.n_h
     r = L - 64 * (ref.shape[2] - 1)
@@ -107,8 +127,7 @@ def test_ut_transform_many_chunks_per_cta():
         one = dict(k=inp["k"][b:b + 1, :, :, h:h + 1].contiguous(),
                    beta=inp["beta"][b:b + 1, :, :, h:h + 1].contiguous(),
                    g=inp["g"][b:b + 1, :, h:h + 1].contiguous())
-        compare(to_np(t[b:b + 1, h:h + 1]), oracle_t(one, w.with_(B=1, H=1)), "bf16",
-                f"T head {(b, h)}")
+        compare_t(to_np(t[b:b + 1, h:h + 1]), oracle_t(one, w.with_(B=1, H=1)), f"T head {(b, h)}")
 
 
 @pytest.mark.parametrize("gated,n_h", [(False, 1), (True, 1), (True, 3)])
@@ -124,5 +143,10 @@ def test_two_passes_equal_delta_fwd(gated, n_h):
                                   n_h=n_h)
     o1, s1 = gpu_fwd(inp, w)
     torch.cuda.synchronize()
-    assert torch.equal(o1, o2) and torch.equal(s1, s2)
     check_full(inp, w, o2, s2)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    # the UT pass again, now on shared memory the state pass has used: the
+    # same bits (nothing it reads is left over from an earlier kernel)
+    t2 = wr.delta_ut_transform(d["k"], d["beta"], d["g"], n_h=n_h)
+    torch.cuda.synchronize()
+    assert torch.equal(t, t2)

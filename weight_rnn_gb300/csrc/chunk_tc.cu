@@ -123,7 +123,7 @@ enum {
   NBARS = B_TREMPTY + 2
 };
 constexpr uint32_t SM_MISC = SM_BAR + NBARS * 8;  // tmem slot, abort flag, gate of the chunk
-constexpr uint32_t SMEM_TOTAL = OFF_SM + SM_MISC + 16;
+constexpr uint32_t SMEM_TOTAL = OFF_SM + ((SM_MISC + 16 + 15) & ~15u);
 constexpr uint32_t SMEM_ALLOC = 232448;
 static_assert(SMEM_TOTAL <= SMEM_ALLOC, "shared memory budget");
 
@@ -188,16 +188,18 @@ __device__ __forceinline__ bool wait_bar(const Smem &sm, int idx, uint32_t parit
 // already issued.  They complete on their own, so this wait does NOT give up
 // when another role has aborted (shared memory and TMEM must not be released
 // under them); it is still bounded.  If it runs out, the error word records
-// it and the CTA keeps its TMEM columns at exit instead of freeing them
-// under work that may still be writing them.
-__device__ __noinline__ bool wait_bar_drain(uint8_t *base, int idx, uint32_t parity, int role) {
+// it; if the work waited for writes TMEM (the products), the CTA keeps its
+// TMEM columns at exit instead of freeing them under products that may still
+// be writing them.
+__device__ __noinline__ bool wait_bar_drain(uint8_t *base, int idx, uint32_t parity, int role,
+                                            bool tmem_writer) {
   Smem sm;
   sm.base = base;
   uint64_t *b = sm.bar(idx);
   for (uint32_t i = 0; i < (1u << 24); ++i)
     if (mbar_try_wait(b, parity)) return true;
   *sm.abort_flag() = 1;
-  *sm.keep_tmem() = 1;
+  if (tmem_writer) *sm.keep_tmem() = 1;
   atomicCAS(&g_tc_error, 0u, (unsigned)(1 + role) | ((unsigned)idx << 8));
   return false;
 }
@@ -269,6 +271,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(sm.bar(B_TREMPTY + s), 1);
     }
     *sm.abort_flag() = 0;
+    *sm.keep_tmem() = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -372,11 +375,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // copies still in flight must land before the CTA's shared memory goes
     if (lane == 0) {
       for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n)
-        wait_bar_drain(sm.base, B_FULL + n % NS, (n / NS) & 1, 0);
+        wait_bar_drain(sm.base, B_FULL + n % NS, (n / NS) & 1, 0, false);
       for (int n = (issued_v > NS ? issued_v - NS : 0); n < issued_v; ++n)
-        wait_bar_drain(sm.base, B_VFULL + n % NS, (n / NS) & 1, 0);
+        wait_bar_drain(sm.base, B_VFULL + n % NS, (n / NS) & 1, 0, false);
       for (int n = (issued_t > 2 ? issued_t - 2 : 0); n < issued_t; ++n)
-        wait_bar_drain(sm.base, B_TRFULL + (n & 1), (n >> 1) & 1, 0);
+        wait_bar_drain(sm.base, B_TRFULL + (n & 1), (n >> 1) & 1, 0, false);
     }
     __syncwarp();
   } else if (warp == 1 || (dual_issue(GATED) && warp == 14)) {
@@ -516,7 +519,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         nap = 16;
       }
       mma_commit(sm.bar(B_DRAIN));  // every issuer arrives
-      wait_bar_drain(sm.base, B_DRAIN, 0, 1);
+      wait_bar_drain(sm.base, B_DRAIN, 0, 1, true);
     }
     __syncwarp();
   } else if (warp < 6) {

@@ -73,7 +73,7 @@ enum {
   NBARS
 };
 constexpr uint32_t SM_MISC = SM_BAR + NBARS * 8;  // tmem slot, abort flag, keep-TMEM flag
-constexpr uint32_t SMEM_TOTAL = OFF_SM + SM_MISC + 16;
+constexpr uint32_t SMEM_TOTAL = OFF_SM + ((SM_MISC + 16 + 15) & ~15u);
 constexpr uint32_t UT_SMEM_ALLOC = SMEM_TOTAL + 1024;  // + worst-case alignment
 static_assert(UT_CTAS_PER_SM * (UT_SMEM_ALLOC + 1024) <= 233472, "two CTAs per SM");
 constexpr uint32_t TM_COLS = 128;
@@ -119,15 +119,17 @@ __device__ __forceinline__ bool wait_bar(const Smem &sm, int idx, uint32_t parit
   return wait_bar_slow(sm.base, idx, parity, role);
 }
 // Wait for copies or products already issued: ignores the abort flag (they
-// complete on their own), still bounded; if it runs out, TMEM is kept.
-__device__ __noinline__ bool wait_bar_drain(uint8_t *base, int idx, uint32_t parity, int role) {
+// complete on their own), still bounded; if it runs out on the products
+// (which write TMEM), TMEM is kept at exit.
+__device__ __noinline__ bool wait_bar_drain(uint8_t *base, int idx, uint32_t parity, int role,
+                                            bool tmem_writer) {
   Smem sm;
   sm.base = base;
   uint64_t *b = sm.bar(idx);
   for (uint32_t i = 0; i < (1u << 24); ++i)
     if (mbar_try_wait(b, parity)) return true;
   *sm.abort_flag() = 1;
-  *sm.keep_tmem() = 1;
+  if (tmem_writer) *sm.keep_tmem() = 1;
   atomicCAS(&g_ut_error, 0u, (unsigned)(1 + role) | ((unsigned)idx << 8));
   return false;
 }
@@ -396,11 +398,16 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
 
   // ---- set-up ----
   {
-    uint4 *z = reinterpret_cast<uint4 *>(sm.base + OFF_SM);
-    for (uint32_t i = tid; i < (SM_MISC + 16) / 16; i += UT_THREADS) z[i] = make_uint4(0, 0, 0, 0);
+    // the two T tiles (the solve writes their lower triangle and diagonal
+    // only, the same entries for every pair, so the strict upper triangle
+    // stays zero from here on), the small arrays, the barriers and the flags
+    uint4 *z = reinterpret_cast<uint4 *>(sm.base + OFF_T);
+    for (uint32_t i = tid; i < (SMEM_TOTAL - OFF_T) / 16; i += UT_THREADS) z[i] = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   if (tid == 0) {
+    *sm.abort_flag() = 0;
+    *sm.keep_tmem() = 0;
     for (int s = 0; s < 2; ++s) {
       mbar_init(sm.bar(B_FULL + s), 1);
       mbar_init(sm.bar(B_FREE + s), 2);
@@ -474,7 +481,7 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
     // copies still in flight must land before the CTA's shared memory goes
     if (lane == 0)
       for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
-        wait_bar_drain(sm.base, B_FULL + (i & 1), (i >> 1) & 1, 0);
+        wait_bar_drain(sm.base, B_FULL + (i & 1), (i >> 1) & 1, 0, false);
     __syncwarp();
   } else if (warp == 9) {
     // ===================================================== MMA issuer
@@ -494,7 +501,7 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
         mma_commit(sm.bar(B_GFULL));
       }
       mma_commit(sm.bar(B_DRAIN));
-      wait_bar_drain(sm.base, B_DRAIN, 0, 1);
+      wait_bar_drain(sm.base, B_DRAIN, 0, 1, true);
     }
     __syncwarp();
   } else {
