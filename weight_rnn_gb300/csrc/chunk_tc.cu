@@ -1,16 +1,16 @@
-// chunk_tc.cu -- fused chunked forward of delta-rule attention on the 5th-
-// generation tensor cores (tcgen05 + TMEM + TMA), bf16 I/O, dk = dv = 128,
-// chunk C = 64, any n_h (Gated DeltaProduct), gated or not.
+// chunk_tc.cu -- the state pass of the chunked forward of delta-rule
+// attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), bf16
+// I/O, dk = dv = 128, chunk C = 64, any n_h (Gated DeltaProduct), gated or
+// not.  It takes the UT transform T = (I + A)^{-1} diag(beta) of every chunk
+// from the intra-chunk pass (ut_tc.cu) and runs the state chain.
 //
 // The algorithm is the chunkwise form of "08 · linear 路线（三）：delta rule 与
-// DPLR 统一框架" -- the UT transform of §2.2, the state passing of §2.3 and
-// the gated variant of §3 -- run on the extended sequence of "DeltaProduct：
-// 通过 Householder 乘积增强线性 RNN 的状态追踪" §4.1.  Per chunk of 64 rows:
+// DPLR 统一框架" -- the WY vectors of §2.2, the state passing of §2.3 and the
+// gated variant of §3 -- run on the extended sequence of "DeltaProduct：通过
+// Householder 乘积增强线性 RNN 的状态追踪" §4.1.  Per chunk of 64 rows:
 //
 //   gc   = inclusive cumsum of the log gate (log g_t at each token's first
 //          sub-step, 0 elsewhere; clamped at -80 so g = 0 stays finite)
-//   A    = strictLower(diag(beta) (Gam * K K^T)),  Gam_ij = exp(gc_i - gc_j)
-//   T    = (I + A)^{-1} diag(beta)
 //   W    = T (K * exp(gc)),  U = T V
 //   O    = (Q * exp(gc)) S + P (U - W S),   P = Q K^T * Gam * M (M incl. diag)
 //   S   <- exp(gc_C) S + Kd^T (U - W S),    Kd = K * exp(gc_C - gc)
@@ -28,28 +28,33 @@
 // that every tensor-core product has M = 128 (a d axis) and the state S^T
 // lives in TMEM as an fp32 accumulator [dv lanes x dk columns]:
 //
-//   G     = [K; Q] K^T                  SS  N=64  K=128  (-> A, P)
+//   G     = [K; Q] K^T                  SS  N=64  K=128  (rows 64.. -> P)
 //   W^T   = K^T (T diag exp gc)^T       SS  N=64  K=64
 //   U^T   = V^T T^T                     SS  N=64  K=64
 //   (M-I)^T = -W^T Kd                   TS  N=128 K=64   (A = W^T bf16 in TMEM)
 //   Q'^T  = -W^T P^T (+ exp(gc) Q^T)    TS  N=64  K=64
-//   O^T   = U^T P^T + S^T Q'^T          TS  N=64  K=64 + K=128
 //   S^T  += S^T (M-I)^T + U^T Kd        TS  N=128 K=128 + K=64   (chain)
+//   O^T   = U^T P^T + S^T Q'^T          TS  N=64  K=64 + K=128   (after the chain step)
 //
-// W, U, T, M, Q' and P never leave the SM.  HBM traffic is q, k, v, beta, g
-// in and out, h0/hT once per head.
+// The state step does not wait for the outputs: the output group of chunk n
+// is issued right behind its state step (it reads the same bf16 S^T), and
+// Q' is prepared by other warps while the chain runs.  W, U, M, Q' and P never
+// leave the SM.  HBM traffic is q, k, v, beta, g and T in, out, h0/hT once per
+// head.
 //
-// Warp roles (448 threads ungated, 480 gated; one CTA per (b, h) head):
+// Warp roles (512 threads; one CTA per (b, h) head):
 //   warp 0       TMA producer: K/Q/V tiles (128-byte swizzle, 3 stages, the
-//                chunk after them prefetched into L2) + beta / log-gate rows
-//   warp 1       TMEM owner and MMA issuer (gated: the state-recurrence
-//                products; warp 14 issues the look-ahead W, U, G products)
-//   warps 2-5    prep (chunk n+2): G -> A, P -> UT solve -> T tiles
+//                chunk after them prefetched into L2), the T tile (2-slot
+//                ring), beta / log-gate rows
+//   warps 1, 14, 15  MMA issuers (one thread each): the recurrence (state
+//                step, output group); M and the Q' helper; the look-ahead
+//                G, W, U.  Warp 1 owns the TMEM allocation.
+//   warps 2-5    prep: P from G (chunk n+2), T diag(exp gc) for W, and Q' of
+//                the chunk in flight -> smem operand (warp-MMA fragments)
 //   warps 6-9    feed-forward (chunk n+1): W^T, U^T -> bf16 TMEM operands,
 //                Kd, (M-I)^T -> smem operand
 //   warps 10-13  chain (chunk n): S^T -> bf16 operand, the outputs (staged
-//                through the V slot by transposing 8x8 stores), hT; then Q'
-//                of chunk n+1 -> smem operand, in the same fragment layout
+//                through the V slot by transposing 8x8 stores), hT
 // Every mbarrier wait is bounded; a timeout sets a device error word and the
 // kernel winds down instead of hanging.
 #include <cuda_bf16.h>
@@ -71,12 +76,9 @@ using namespace tc;
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr int NS = 3;  // TMA stages
-// Gated, a second MMA-issuing warp (14) takes the look-ahead products; the
-// ungated step keeps one issuer and its priority order (measured faster)
-__host__ __device__ constexpr bool dual_issue(bool gated) { return gated; }
-__host__ __device__ constexpr bool look_wu(bool gated) { return true; }  // W, U on warp 14
-__host__ __device__ constexpr bool look_g(bool gated) { return true; }   // G on warp 14
-__host__ __device__ constexpr int threads_for(bool gated) { return dual_issue(gated) ? 480 : 448; }
+// Three MMA-issuing threads (warps 1, 14, 15), each blocking on its own
+// barriers in a fixed order; 16 warps = 512 threads, 128 registers each
+constexpr int kThreads = 512;
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ----
 constexpr uint32_t STAGE_BYTES = 49152;
@@ -104,18 +106,19 @@ enum {
   B_GFREE,           // prep -> MMA: G read (per P warp, 2)
   B_TFULL,           // prep -> MMA: T diag(exp gc) and P written (per warp)
   B_WFULL,           // MMA -> ff, prep: W^T, U^T in TMEM (T diag(exp gc) consumed)
-  B_CWD,             // ff -> MMA: W^T, U^T bf16 in TMEM, Kd in smem (per warp)
+  B_CWDW,            // ff -> MMA: W^T bf16 in TMEM, Kd in smem, TM_X1 read (per warp)
   B_MFULL,           // MMA -> ff: (M-I)^T in TMEM
   B_MRDY,            // ff -> MMA: (M-I)^T in smem, TMEM free (per warp)
-  B_QFULL,           // MMA -> ff: -W^T P^T in TMEM
-  B_QRDY,            // ff -> MMA: Q' in smem, TMEM free (per warp)
+  B_QFULL,           // MMA -> prep, ff: -W^T P^T in TMEM (W^T bf16 consumed)
+  B_QRDY,            // prep -> MMA: Q' in smem, TMEM read (per warp)
   B_SRDY,            // chain -> MMA: S^T bf16 in TMEM (per warp)
   B_SFULL,           // MMA -> chain, ff: state step done
-  B_OFULL,           // MMA -> chain: O^T in TMEM
+  B_OFULL,           // MMA -> chain, ff: the output group (U^T P^T + S^T Q'^T) done
   B_OFREE,           // chain -> MMA: O^T read (per warp)
   B_PFREE0,          // MMA -> prep: P buffer 0 consumed
   B_PFREE1,          //                        1
   B_DRAIN,           // MMA: everything issued has completed
+  B_CWDU,            // ff -> MMA: U^T bf16 in TMEM (per warp)
   B_VFULL,           // [NS] producer -> MMA: the V tile of a stage loaded (count 1 + tx)
   B_VEMPTY = B_VFULL + NS,  // [NS] chain -> producer: V slot free (per warp; it stages the outputs)
   B_TRFULL = B_VEMPTY + NS,  // [2] producer -> prep: the chunk's T tile loaded (count 1 + tx)
@@ -230,7 +233,7 @@ struct Rows {
 
 // 14 warps: at most 4 per SM sub-partition, so 128 registers per thread
 template <bool GATED>
-__global__ void __launch_bounds__(threads_for(GATED), 1)
+__global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_t,
                 TcParams p) {
@@ -254,7 +257,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   // ---- set-up: zero shared memory, init barriers, allocate TMEM ----
   {
     uint4 *z = reinterpret_cast<uint4 *>(sm.base);
-    for (uint32_t i = tid; i < SMEM_TOTAL / 16; i += threads_for(GATED)) z[i] = make_uint4(0, 0, 0, 0);
+    for (uint32_t i = tid; i < SMEM_TOTAL / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   if (tid == 0) {
@@ -263,7 +266,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(sm.bar(B_EMPTY + s), 1);
       mbar_init(sm.bar(B_VEMPTY + s), 4);
     }
-    const int cnt[B_VFULL - 2 * NS] = {1, 2, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, dual_issue(GATED) ? 2 : 1};
+    const int cnt[B_VFULL - 2 * NS] = {1, 2, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, 3, 4};
     for (int i = 2 * NS; i < B_VFULL; ++i) mbar_init(sm.bar(i), cnt[i - 2 * NS]);
     for (int s = 0; s < NS; ++s) mbar_init(sm.bar(B_VFULL + s), 1);
     for (int s = 0; s < 2; ++s) {
@@ -382,18 +385,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         wait_bar_drain(sm.base, B_TRFULL + (n & 1), (n >> 1) & 1, 0, false);
     }
     __syncwarp();
-  } else if (warp == 1 || (dual_issue(GATED) && warp == 14)) {
+  } else if (warp == 1 || warp >= 14) {
     // ===================================================== MMA issuers
-    // Gated: warp 1 issues the products on the state recurrence (op, the
-    // state step with the rest of the output, M, the Q' helper) and warp 14
-    // the look-ahead products for later chunks (W, U, G).  Each commits the
-    // barriers of its own products; the hand-offs between the two kinds are
-    // barriers already.  Ungated: warp 1 issues everything.
-    constexpr bool kDual = dual_issue(GATED);
-    const bool crit = warp == 1;
-    // which thread issues the look-ahead kinds
-    const bool do_wu = !kDual || (look_wu(GATED) ? warp == 14 : crit);
-    const bool do_g = !kDual || (look_g(GATED) ? warp == 14 : crit);
+    // Three threads, each issuing one kind of work in a fixed order and
+    // blocking on the barriers of its inputs (a blocked try_wait wakes within
+    // ~100 cycles of the arrival; the tensor pipe interleaves their products
+    // in issue order):
+    //   warp 1   the recurrence: state step n (SRDY, MRDY, CWDU), then the
+    //            output group of n (QRDY), which reads the same bf16 S^T
+    //   warp 14  M(n) (CWDW), then the -W^T P^T helper of Q'(n) (OFREE(n-1))
+    //   warp 15  the look-ahead: G(0); per chunk W(m) (TFULL, MRDY(m-1)),
+    //            U(m) (VFULL), G(m+1) (FULL, GFREE(m))
+    // Each commits the barriers of its own products; every hand-off between
+    // kinds is a barrier.
     if (lane == 0) {
       constexpr uint32_t id_uw = idesc_bf16(128, 64, true, false);
       constexpr uint32_t id_m = idesc_bf16(128, 128, false, true, true);  // B = Kd, MN-major, negated
@@ -401,41 +405,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       constexpr uint32_t id_op = idesc_bf16(128, 64, false, false);       // B = P
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);        // B = (M-I)^T or Kd, MN-major
       constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);        // B = Q' (K-major)
+      constexpr uint32_t id_g = idesc_bf16(128, 64, false, false);
       const uint32_t a_tr = smem_u32(sm.base + OFF_TR), a_tw = smem_u32(sm.base + OFF_TW);
       const uint32_t a_ms = smem_u32(sm.base + OFF_MS), a_p = smem_u32(sm.base + OFF_P);
-      auto rdy = [&](int idx, int k) -> bool { return mbar_test_wait(sm.bar(idx), k & 1); };
       auto kd_desc = [&](int m, int k) -> uint64_t {  // B = Kd (gated: V slot) or K
         const uint32_t kq = smem_u32(sm.stage(m % NS));
         return GATED ? sdesc_sw128(kq + ST_V0 + k * 2048, 8192, 1024)
                      : sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024);
       };
-      // Every product of chunk k is issued as soon as its inputs are ready,
-      // each kind in chunk order; the barriers are the whole dependency graph
-      // (each phase is waited for once, in order).  The tensor pipe runs in
-      // order and a thread's issue blocks while it is busy, so the products
-      // on the state recurrence (chain -> outputs -> Q' -> op -> chain) go
-      // first and the look-ahead work for later chunks after them, in 4-MMA
-      // pieces.  In priority order:
-      //   op(k): QRDY(k)   chain(n): op(n) issued, SRDY(n), MRDY(n)
-      //   m(k): CWD(k)     q(k): M(k) issued, OFREE(k-1)
-      //   W(k): TFULL(k), MRDY(k-1)   U(k): after W(k), VFULL(k)   (they release the T tiles)
-      //   G(k) halves: FULL(k), GFREE(k-1)
-      constexpr uint32_t id_g = idesc_bf16(128, 64, false, false);
-      int c_ch = 0, c_op = 0, c_q = 0, c_m = 0, c_w = 0, c_u = 0, c_g2 = 0;
-      uint32_t idle = 0, nap = 16;
-      while (crit ? c_ch < NT : ((do_wu && c_u < NT) || (do_g && c_g2 < 2 * NT))) {
-        if (crit && c_op < c_q && rdy(B_QRDY, c_op)) {
-          // ---- O^T = U^T P^T (first part of the output) ----
-          const int m = c_op++;
-          tc_fence_after();
-          const uint32_t pb = a_p + (m & 1) * 8192;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_O, tmem + TM_UB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_op, k > 0);
-          mma_commit(sm.bar(B_PFREE0 + (m & 1)));
-        } else if (crit && c_ch < c_op && rdy(B_SRDY, c_ch) && rdy(B_MRDY, c_ch)) {
-          // ---- the state step and the rest of O(n) ----
-          const int n = c_ch++;
+      if (warp == 1) {
+        for (int n = 0; n < NT; ++n) {
+          // ---- the state step ----
+          if (!wait_bar(sm, B_SRDY, n & 1, 1) || !wait_bar(sm, B_MRDY, n & 1, 1) ||
+              !wait_bar(sm, B_CWDU, n & 1, 1))
+            break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
@@ -443,6 +426,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
           for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_S, tmem + TM_UB + k * 8, kd_desc(n, k), id_s, true);
           mma_commit(sm.bar(B_SFULL));
+          // ---- the output group: O^T = U^T P^T + S^T Q'^T ----
+          if (!wait_bar(sm, B_QRDY, n & 1, 1)) break;
+          tc_fence_after();
+          const uint32_t pb = a_p + (n & 1) * 8192;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + TM_O, tmem + TM_UB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_op, k > 0);
           const uint32_t st = smem_u32(sm.stage(n % NS));
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -450,26 +440,49 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mma_ts(tmem + TM_O, tmem + TM_SBF + k * 8, sdesc_sw128(qa, 0, 1024), id_o, true);
           }
           mma_commit(sm.bar(B_OFULL));
+          mma_commit(sm.bar(B_PFREE0 + (n & 1)));
           mma_commit(sm.bar(B_EMPTY + n % NS));
-        } else if (crit && (do_wu ? c_m < c_u : c_m < NT) && rdy(B_CWD, c_m)) {  // CWD(m): U(m) done, converted
+        }
+      } else if (warp == 14) {
+        for (int m = 0; m < NT; ++m) {
           // ---- (M-I)^T = -W^T Kd ----
-          const int m = c_m++;
+          if (!wait_bar(sm, B_CWDW, m & 1, 1)) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_X1, tmem + TM_WB + k * 8, kd_desc(m, k), id_m, k > 0);
           mma_commit(sm.bar(B_MFULL));
-        } else if (crit && c_q < c_m && (c_q == 0 || rdy(B_OFREE, c_q - 1))) {
           // ---- -W^T P^T (the rest of Q' is added on the CUDA cores) ----
-          const int m = c_q++;
+          if (m >= 1 && !wait_bar(sm, B_OFREE, (m - 1) & 1, 1)) break;
           tc_fence_after();
           const uint32_t pb = a_p + (m & 1) * 8192;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ts(tmem + TM_O, tmem + TM_WB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_q, k > 0);
           mma_commit(sm.bar(B_QFULL));
-        } else if (do_wu && c_w < NT && c_w == c_u && rdy(B_TFULL, c_w) && (c_w == 0 || rdy(B_MRDY, c_w - 1))) {
+        }
+      } else if (warp == 15) {
+        // ---- G = [K;Q] K^T of chunk m ----
+        auto issue_g = [&](int m) -> bool {
+          if (!wait_bar(sm, B_FULL + m % NS, (m / NS) & 1, 1)) return false;
+          if (m >= 1 && !wait_bar(sm, B_GFREE, (m - 1) & 1, 1)) return false;
+          tc_fence_after();
+          const uint32_t kq0 = smem_u32(sm.stage(m % NS));
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t kq = kq0 + hf * 16384;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + TM_G, sdesc_sw128(kq + k * 32, 0, 1024), sdesc_sw128(kq + k * 32, 0, 1024),
+                     id_g, hf > 0 || k > 0);
+          }
+          mma_commit(sm.bar(B_GFULL));
+          return true;
+        };
+        bool ok = issue_g(0);
+        for (int m = 0; ok && m < NT; ++m) {
           // ---- W^T = K^T (T diag exp gc)^T (ungated: T itself) ----
-          const int m = c_w++;
+          if (!wait_bar(sm, B_TFULL, m & 1, 1)) break;
+          if (m >= 1 && !wait_bar(sm, B_MRDY, (m - 1) & 1, 1)) break;
           tc_fence_after();
           const uint32_t kq = smem_u32(sm.stage(m % NS));
           const uint32_t wb = GATED ? a_tw : a_tr + (m & 1) * 8192;
@@ -477,11 +490,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_X1, sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024),
                    sdesc_sw128(wb + k * 32, 0, 1024), id_uw, k > 0);
-        } else if (do_wu && c_u < c_w && rdy(B_VFULL + c_u % NS, c_u / NS)) {
           // ---- U^T = V^T T^T ----
-          const int m = c_u++;
+          if (!wait_bar(sm, B_VFULL + m % NS, (m / NS) & 1, 1)) break;
           tc_fence_after();
-          const uint32_t kq = smem_u32(sm.stage(m % NS));
           const uint32_t tb = a_tr + (m & 1) * 8192;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -489,34 +500,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                    sdesc_sw128(tb + k * 32, 0, 1024), id_uw, k > 0);
           mma_commit(sm.bar(B_WFULL));
           mma_commit(sm.bar(B_TREMPTY + (m & 1)));
-        } else if (do_g && c_g2 < 2 * NT && ((c_g2 & 1) ||
-                                     (rdy(B_FULL + (c_g2 >> 1) % NS, (c_g2 >> 1) / NS) &&
-                                      (c_g2 == 0 || rdy(B_GFREE, (c_g2 >> 1) - 1))))) {
-          // ---- G = [K;Q] K^T, one 64-column half of the K dimension ----
-          const int m = c_g2 >> 1, hf = c_g2 & 1;
-          ++c_g2;
-          tc_fence_after();
-          const uint32_t kq = smem_u32(sm.stage(m % NS)) + hf * 16384;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_G, sdesc_sw128(kq + k * 32, 0, 1024), sdesc_sw128(kq + k * 32, 0, 1024), id_g,
-                   hf > 0 || k > 0);
-          if (hf) mma_commit(sm.bar(B_GFULL));
-        } else {
-          // nothing ready: back off (exponentially, so that the polling
-          // leaves the issue slots of this SM sub-partition to the solve),
-          // give up after ~1 s
-          if (++idle > (1u << 22) || ((idle & 63) == 0 && *sm.abort_flag())) {
-            *sm.abort_flag() = 1;
-            atomicCAS(&g_tc_error, 0u, 2u | (0xEEu << 8));
-            break;
-          }
-          __nanosleep(nap);
-          if (nap < 256) nap <<= 1;
-          continue;
+          if (m + 1 < NT) ok = issue_g(m + 1);
         }
-        idle = 0;
-        nap = 16;
       }
       mma_commit(sm.bar(B_DRAIN));  // every issuer arrives
       wait_bar_drain(sm.base, B_DRAIN, 0, 1, true);
@@ -530,6 +515,77 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int q4 = warp & 3;              // TMEM lane quarter
     const int L = q4 * 32 + lane;         // TMEM lane of this thread
     float *eg = sm.arr(SM_EG), *ieg = sm.arr(SM_IEG), *gcs = sm.arr(SM_GC);
+    float *gq = sm.arr(SM_GQ);
+    // Q'(c) = exp(gc) Q - P W, in place over the Q tile of chunk c (same
+    // K-major layout: the output product reads it as its B operand); the
+    // scan for exp(gc) at the readout rows first
+    auto qprime = [&](int c) {
+      const int s = c % NS;
+      const Rows rw(c, n_h, p.T);
+      if (GATED) wait_bar(sm, B_FULL + s, (c / NS) & 1, 2);  // the chunk's log-gate row
+      if (GATED && warp == 2) {
+        float lo, hi;
+        warp_scan64(sm.lam(s), lane, lo, hi);
+        const float elo = fast_exp2(lo), ehi = fast_exp2(hi);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int r = lane + 32 * hf;
+          const int pos = rw.pos(r, n_h);
+          const float a = __shfl_sync(0xffffffffu, elo, pos & 31);
+          const float e = __shfl_sync(0xffffffffu, ehi, pos & 31);
+          gq[r] = r < rw.Cp ? (pos < 32 ? a : e) : 0.f;
+        }
+      }
+      if (GATED) named_sync(1);
+      wait_bar(sm, B_QFULL, c & 1, 2);
+      tc_fence_after();
+      {
+        // Warp-MMA fragments throughout: the tile of this warp (d = 32 q4 ..
+        // 32 q4 + 31, all 64 rows) goes in 8x8 pieces; a thread holds the
+        // pairs (d = t / 4 (+ 8), rows 8 g + 2 (t % 4), + 1) of TMEM, of Q
+        // (transposing 8x8 loads) and of Q' (transposing 8x8 stores, to the
+        // addresses the loads came from)
+        const int tq = lane & 3;
+        float2 gv[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          gv[g] = GATED ? *reinterpret_cast<const float2 *>(gq + 8 * g + 2 * tq) : make_float2(1.f, 1.f);
+        const int cp = rw.Cp;
+        const uint32_t qh = smem_u32(sm.stage(s) + ((q4 >> 1) ? ST_Q1 : ST_Q0));
+        const int mi = lane >> 3, mr = lane & 7;  // the 8x8 piece and row this lane addresses
+#pragma unroll
+        for (int b16 = 0; b16 < 32; b16 += 16) {
+          uint32_t hreg[32];
+          tmem_ld16x256b_x8(tmem_addr(tmem + TM_O, q4 * 32 + b16, 0), hreg);
+          tmem_wait_ld_regs(hreg);
+          const int ck = (32 * (q4 & 1) + b16) / 8 + (mi & 1);  // 16-byte piece of the row
+          // all loads of this half first (the stores go to the same places)
+          uint32_t addr[4], qd[4][4];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int row = 16 * cc + 8 * (mi >> 1) + mr;
+            addr[cc] = qh + (row >> 3) * 1024 + (row & 7) * 128 + ((ck ^ (row & 7)) << 4);
+            ldsm_x4_trans(addr[cc], qd[cc]);
+          }
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int g = 2 * cc + (m >> 1), j = 4 * g + 2 * (m & 1);
+              const int r0 = 8 * g + 2 * tq;
+              const float v0 = fmaf(gv[g].x, __uint_as_float(qd[cc][m] << 16), __uint_as_float(hreg[j]));
+              const float v1 = fmaf(gv[g].y, __uint_as_float(qd[cc][m] & 0xFFFF0000u), __uint_as_float(hreg[j + 1]));
+              o4[m] = pack_bf16(r0 < cp ? v0 : 0.f, r0 + 1 < cp ? v1 : 0.f);
+            }
+            stsm_x4_trans(addr[cc], o4);
+          }
+        }
+        tc_fence_before();
+      }
+      fence_proxy_async_smem();
+      arrive_warp(sm.bar(B_QRDY), lane);
+    };
     for (int m = 0; m < NT; ++m) {
       const int s = m % NS;
       // every warp of the group is done with the previous chunk's gate
@@ -630,7 +686,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
       fence_proxy_async_smem();
       arrive_warp(sm.bar(B_TFULL), lane);
+      // Q' of the previous chunk, as soon as its -W^T P^T helper is in TMEM
+      if (m >= 1) {
+        if (named_sync_or(1, *sm.abort_flag() != 0)) break;
+        qprime(m - 1);
+      }
     }
+    if (NT >= 1 && !named_sync_or(1, *sm.abort_flag() != 0)) qprime(NT - 1);
   } else if (warp < 10) {
     // ===================================================== feed-forward warps
     const int q4 = warp & 3;
@@ -655,25 +717,36 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         named_sync(2);
       }
 
-      // ---- W^T, U^T -> bf16 operands; Kd ----
+      // ---- W^T, U^T -> bf16 operands (both read out of TM_X1 first, so
+      //      that the M product may overwrite it); Kd ----
       wait_bar(sm, B_WFULL, c & 1, 3);
       tc_fence_after();
+      uint32_t pw_[32], pu[32];
       {
-        uint32_t r[64], pw_[32];
+        uint32_t r[64];
         tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
         tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
         tmem_wait_ld_regs(r);
 #pragma unroll
         for (int u = 0; u < 32; ++u)
           pw_[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-        // W^T bf16 of the previous chunk is read by its -W^T P^T product
-        // (after its M product, whose completion was waited for already)
-        if (c >= 1) {
-          wait_bar(sm, B_QFULL, (c - 1) & 1, 3);
-          tc_fence_after();
-        }
-        tmem_st32(tmem_addr(tmem + TM_WB, q4 * 32, 0), pw_);
       }
+      {
+        uint32_t r[64];
+        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 64), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 96), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+        tmem_wait_ld_regs(r);
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          pu[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+      }
+      // W^T bf16 of the previous chunk is read by its M and -W^T P^T products
+      // (the -W^T P^T product is issued after M and commits QFULL)
+      if (c >= 1) {
+        wait_bar(sm, B_QFULL, (c - 1) & 1, 3);
+        tc_fence_after();
+      }
+      tmem_st32(tmem_addr(tmem + TM_WB, q4 * 32, 0), pw_);
       if (GATED) {
         // Kd = diag(exp(gc_C - gc)) K into the V slot (V was consumed by U)
         const uint8_t *kt = sm.stage(s);
@@ -693,25 +766,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         fence_proxy_async_smem();
       }
-      uint32_t pu[32];
-      {
-        uint32_t r[64];
-        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 64), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 96), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
-        tmem_wait_ld_regs(r);
-#pragma unroll
-        for (int u = 0; u < 32; ++u)
-          pu[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+      tmem_wait_st();
+      tc_fence_before();
+      arrive_warp(sm.bar(B_CWDW), lane);
+      // U^T bf16 of the previous chunk is read by its state step and its
+      // output group (U^T P^T) until the output group ends
+      if (c >= 1) {
+        wait_bar(sm, B_OFULL, (c - 1) & 1, 3);
+        tc_fence_after();
       }
-      // U^T bf16 is read by the state step of the previous chunk until it ends
-      if (c >= 1) wait_bar(sm, B_SFULL, (c - 1) & 1, 3);
       tmem_st32(tmem_addr(tmem + TM_UB, q4 * 32, 0), pu);
       tmem_wait_st();
       tc_fence_before();
-      arrive_warp(sm.bar(B_CWD), lane);
+      arrive_warp(sm.bar(B_CWDU), lane);
 
-      // ---- (M-I)^T -> bf16 smem operand (row L = j, columns i) ----
+      // ---- (M-I)^T -> bf16 smem operand (row L = j, columns i); the state
+      //      step of the previous chunk reads the old one until it ends ----
       wait_bar(sm, B_MFULL, c & 1, 3);
+      if (c >= 1) wait_bar(sm, B_SFULL, (c - 1) & 1, 3);
       tc_fence_after();
       const float gm1 = GATED ? *sm.gate_c() - 1.f : 0.f;
 #pragma unroll 1
@@ -742,78 +814,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // ===================================================== chain warps
     const int q4 = warp & 3;
     const int L = q4 * 32 + lane;  // TMEM lane = value column dv
-    float *gq = sm.arr(SM_GQ);
-    // Q'(c) = exp(gc) Q - P W, in place over the Q tile of chunk c (same
-    // K-major layout: the output product reads it as its B operand); the
-    // scan for exp(gc) at the readout rows first
-    auto qprime = [&](int c) {
-      const int s = c % NS;
-      const Rows rw(c, n_h, p.T);
-      if (GATED) wait_bar(sm, B_FULL + s, (c / NS) & 1, 4);  // the chunk's log-gate row
-      if (GATED && warp == 10) {
-        float lo, hi;
-        warp_scan64(sm.lam(s), lane, lo, hi);
-        const float elo = fast_exp2(lo), ehi = fast_exp2(hi);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int r = lane + 32 * hf;
-          const int pos = rw.pos(r, n_h);
-          const float a = __shfl_sync(0xffffffffu, elo, pos & 31);
-          const float e = __shfl_sync(0xffffffffu, ehi, pos & 31);
-          gq[r] = r < rw.Cp ? (pos < 32 ? a : e) : 0.f;
-        }
-      }
-      if (GATED) named_sync(3);
-      wait_bar(sm, B_QFULL, c & 1, 4);
-      tc_fence_after();
-      {
-        // Warp-MMA fragments throughout: the tile of this warp (d = 32 q4 ..
-        // 32 q4 + 31, all 64 rows) goes in 8x8 pieces; a thread holds the
-        // pairs (d = t / 4 (+ 8), rows 8 g + 2 (t % 4), + 1) of TMEM, of Q
-        // (transposing 8x8 loads) and of Q' (transposing 8x8 stores, to the
-        // addresses the loads came from)
-        const int tq = lane & 3;
-        float2 gv[8];
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          gv[g] = GATED ? *reinterpret_cast<const float2 *>(gq + 8 * g + 2 * tq) : make_float2(1.f, 1.f);
-        const int cp = rw.Cp;
-        const uint32_t qh = smem_u32(sm.stage(s) + ((q4 >> 1) ? ST_Q1 : ST_Q0));
-        const int mi = lane >> 3, mr = lane & 7;  // the 8x8 piece and row this lane addresses
-#pragma unroll
-        for (int b16 = 0; b16 < 32; b16 += 16) {
-          uint32_t hreg[32];
-          tmem_ld16x256b_x8(tmem_addr(tmem + TM_O, q4 * 32 + b16, 0), hreg);
-          tmem_wait_ld_regs(hreg);
-          const int ck = (32 * (q4 & 1) + b16) / 8 + (mi & 1);  // 16-byte piece of the row
-          // all loads of this half first (the stores go to the same places)
-          uint32_t addr[4], qd[4][4];
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int row = 16 * cc + 8 * (mi >> 1) + mr;
-            addr[cc] = qh + (row >> 3) * 1024 + (row & 7) * 128 + ((ck ^ (row & 7)) << 4);
-            ldsm_x4_trans(addr[cc], qd[cc]);
-          }
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t o4[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int g = 2 * cc + (m >> 1), j = 4 * g + 2 * (m & 1);
-              const int r0 = 8 * g + 2 * tq;
-              const float v0 = fmaf(gv[g].x, __uint_as_float(qd[cc][m] << 16), __uint_as_float(hreg[j]));
-              const float v1 = fmaf(gv[g].y, __uint_as_float(qd[cc][m] & 0xFFFF0000u), __uint_as_float(hreg[j + 1]));
-              o4[m] = pack_bf16(r0 < cp ? v0 : 0.f, r0 + 1 < cp ? v1 : 0.f);
-            }
-            stsm_x4_trans(addr[cc], o4);
-          }
-        }
-        tc_fence_before();
-      }
-      fence_proxy_async_smem();
-      arrive_warp(sm.bar(B_QRDY), lane);
-      if (GATED) named_sync(3);  // gq is rewritten for the next chunk
-    };
     // ---- initial state S^T (lane = dv, column = dk) ----
     {
       const float *h0 = p.h0 ? p.h0 + (size_t)bh * D * D : nullptr;
@@ -835,7 +835,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       tc_fence_before();
       arrive_warp(sm.bar(B_SRDY), lane);
     }
-    if (!named_sync_or(3, *sm.abort_flag() != 0)) qprime(0);
     for (int n = 0; n < NT; ++n) {
       if (named_sync_or(3, *sm.abort_flag() != 0)) break;
       const Rows rw(n, n_h, p.T);
@@ -927,7 +926,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         // the V slot is free once every warp has read its rows
         arrive_warp(sm.bar(B_VEMPTY + n % NS), lane);
       }
-      if (n + 1 < NT) qprime(n + 1);
     }
   }
 
@@ -1002,7 +1000,7 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const void *t_mat, cudaStream_t s)
   auto kern = a.g ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)(a.B * a.H), threads_for(a.g != nullptr), SMEM_ALLOC, s>>>(mq, mk, mv, mt, p);
+  kern<<<(unsigned)(a.B * a.H), kThreads, SMEM_ALLOC, s>>>(mq, mk, mv, mt, p);
   return cudaGetLastError();
 }
 
