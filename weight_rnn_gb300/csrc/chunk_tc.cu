@@ -7,54 +7,47 @@
 // The algorithm is the chunkwise form of "08 · linear 路线（三）：delta rule 与
 // DPLR 统一框架" -- the WY vectors of §2.2, the state passing of §2.3 and the
 // gated variant of §3 -- run on the extended sequence of "DeltaProduct：通过
-// Householder 乘积增强线性 RNN 的状态追踪" §4.1.  Per chunk of 64 rows:
+// Householder 乘积增强线性 RNN 的状态追踪" §4.1.  Per chunk of 64 rows, with
+// gc the inclusive cumsum of the log gate (log g_t at each token's first
+// sub-step, 0 elsewhere; clamped at -80 so g = 0 stays finite):
 //
-//   gc   = inclusive cumsum of the log gate (log g_t at each token's first
-//          sub-step, 0 elsewhere; clamped at -80 so g = 0 stays finite)
-//   W    = T (K * exp(gc)),  U = T V
-//   O    = (Q * exp(gc)) S + P (U - W S),   P = Q K^T * Gam * M (M incl. diag)
-//   S   <- exp(gc_C) S + Kd^T (U - W S),    Kd = K * exp(gc_C - gc)
+//   W    = T (K * exp(gc)),  U = T V                      (the WY vectors)
+//   V~   = U - W S                                        (pseudo-values)
+//   O    = (Q * exp(gc)) S + P V~,   P = Q K^T * Gam * M  (M incl. diag)
+//   S   <- exp(gc_C) S + Kd^T V~,    Kd = K * exp(gc_C - gc)
 //
-// Everything that does not involve the state is folded into two per-chunk
-// matrices, so that the sequential state chain is ONE tensor-core product:
-//
-//   M - I = (exp(gc_C) - 1) I - Kd^T W          (dk x dk)
-//   Q'    = Q * exp(gc) - P W                    (readout rows x dk)
-//   S    <- S + (M - I) S + Kd^T U               (the chain)
-//   O     = Q' S + P U
-//
-// This is an exact rewrite of the same chunk step (the state enters both
-// products once, as in U - W S).  All products are computed TRANSPOSED, so
-// that every tensor-core product has M = 128 (a d axis) and the state S^T
-// lives in TMEM as an fp32 accumulator [dv lanes x dk columns]:
+// All products are computed TRANSPOSED, so that every tensor-core product has
+// M = 128 (a d axis) and the state S^T lives in TMEM as an fp32 accumulator
+// [dv lanes x dk columns]:
 //
 //   G     = [K; Q] K^T                  SS  N=64  K=128  (rows 64.. -> P)
-//   W^T   = K^T (T diag exp gc)^T       SS  N=64  K=64
-//   U^T   = V^T T^T                     SS  N=64  K=64
-//   (M-I)^T = -W^T Kd                   TS  N=128 K=64   (A = W^T bf16 in TMEM)
-//   Q'^T  = -W^T P^T (+ exp(gc) Q^T)    TS  N=64  K=64
-//   S^T  += S^T (M-I)^T + U^T Kd        TS  N=128 K=128 + K=64   (chain)
-//   O^T   = U^T P^T + S^T Q'^T          TS  N=64  K=64 + K=128   (after the chain step)
+//   W^T   = K^T (T diag exp gc)^T       SS  N=64  K=64   -> bf16 smem operand
+//   U^T   = V^T T^T                     SS  N=64  K=64   (into the V~ accumulator)
+//   V~^T -= S^T W^T                     TS  N=64  K=128  (A = S^T bf16 in TMEM)
+//   S^T  += (V~ diag dec)^T K           TS  N=128 K=64   (= V~^T Kd, dec = exp(gc_C - gc);
+//                                                         S^T scaled by exp(gc_C) first)
+//   O^T   = S^T (Q exp gc)^T + V~^T P^T TS  N=64  K=128 + K=64
 //
-// The state step does not wait for the outputs: the output group of chunk n
-// is issued right behind its state step (it reads the same bf16 S^T), and
-// Q' is prepared by other warps while the chain runs.  W, U, M, Q' and P never
-// leave the SM.  HBM traffic is q, k, v, beta, g and T in, out, h0/hT once per
-// head.
+// The recurrence is S^T -> bf16 -> V~ -> bf16 -> S^T: two products and two
+// conversions per chunk.  Everything else (G, P, W, Q exp(gc), the
+// outputs) is prepared or drained by other warps around it.  W, U, V~ and P
+// never leave the SM.  HBM traffic is q, k, v, beta, g and T in, out, h0/hT
+// once per head.
 //
 // Warp roles (512 threads; one CTA per (b, h) head):
 //   warp 0       TMA producer: K/Q/V tiles (128-byte swizzle, 3 stages, the
 //                chunk after them prefetched into L2), the T tile (2-slot
 //                ring), beta / log-gate rows
-//   warps 1, 14, 15  MMA issuers (one thread each): the recurrence (state
-//                step, output group); M and the Q' helper; the look-ahead
-//                G, W, U.  Warp 1 owns the TMEM allocation.
-//   warps 2-5    prep: P from G (chunk n+2), T diag(exp gc) for W, and Q' of
-//                the chunk in flight -> smem operand (warp-MMA fragments)
-//   warps 6-9    feed-forward (chunk n+1): W^T, U^T -> bf16 TMEM operands,
-//                Kd, (M-I)^T -> smem operand
-//   warps 10-13  chain (chunk n): S^T -> bf16 operand, the outputs (staged
-//                through the V slot by transposing 8x8 stores), hT
+//   warps 1, 14, 15  MMA issuers (one thread each): the recurrence (U, V~,
+//                the state update); the outputs; the look-ahead G, W.
+//                Warp 1 owns the TMEM allocation.
+//   warps 2-5    prep: P from G, T diag(exp gc), Q exp(gc) in place
+//   warps 6-9    feed-forward: W^T -> bf16 smem operand (one chunk ahead),
+//                the outputs (staged through the V slot by transposing 8x8
+//                stores, then 16-byte global stores)
+//   warps 10-13  chain: V~^T -> bf16 operands (plain, and scaled by dec for
+//                the state update), S^T -> bf16 operand and the exp(gc_C)
+//                scaling, hT
 // Every mbarrier wait is bounded; a timeout sets a device error word and the
 // kernel winds down instead of hanging.
 #include <cuda_bf16.h>
@@ -82,10 +75,10 @@ constexpr int kThreads = 512;
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ----
 constexpr uint32_t STAGE_BYTES = 49152;
-constexpr uint32_t ST_K0 = 0, ST_Q0 = 8192, ST_K1 = 16384, ST_Q1 = 24576;
-constexpr uint32_t ST_V0 = 32768;  // V (64 x 128), later Kd, same layout
-constexpr uint32_t OFF_MS = NS * STAGE_BYTES;  // (M-I)^T bf16 [128 j][128 i], MN-major B
-constexpr uint32_t OFF_TW = OFF_MS + 32768;    // T diag(exp gc) bf16 [64][64], K-major
+constexpr uint32_t ST_K0 = 0, ST_Q0 = 8192, ST_K1 = 16384, ST_Q1 = 24576;  // Q later Q*exp(gc)
+constexpr uint32_t ST_V0 = 32768;  // V (64 x 128), later the staged output rows
+constexpr uint32_t OFF_WS = NS * STAGE_BYTES;  // 2 x W^T bf16 [128 dk][64], MN-major B
+constexpr uint32_t OFF_TW = OFF_WS + 32768;    // T diag(exp gc) bf16 [64][64], K-major
 constexpr uint32_t OFF_P = OFF_TW + 8192;      // 2 x P bf16 [64][64], K-major
 constexpr uint32_t OFF_TR = OFF_P + 16384;     // 2 x T bf16 [64][64] (TMA ring), K-major
 constexpr uint32_t OFF_SM = OFF_TR + 16384;    // small arrays and barriers
@@ -94,50 +87,48 @@ constexpr uint32_t SM_LAM = SM_BETA + NS * 256;  // [NS][64] log2 gate
 constexpr uint32_t SM_EG = SM_LAM + NS * 256;    // prep: 2^gc
 constexpr uint32_t SM_IEG = SM_EG + 256;         // prep: 2^-gc
 constexpr uint32_t SM_GC = SM_IEG + 256;         // prep: gc (cumulative log2 gate)
-constexpr uint32_t SM_DEC = SM_GC + 256;         // feed-forward: 2^(gc_C - gc)
-constexpr uint32_t SM_GQ = SM_DEC + 256;         // feed-forward: 2^gc at readout rows
-constexpr uint32_t SM_BAR = SM_GQ + 256;
+constexpr uint32_t SM_DEC = SM_GC + 256;         // chain: 2^(gc_C - gc)
+constexpr uint32_t SM_BAR = SM_DEC + 256;
 
 // ---- barrier indices ----
 enum {
   B_FULL = 0,        // [NS] producer -> all: K, Q tiles, beta, log gate loaded (count 2 + tx)
-  B_EMPTY = NS,      // [NS] MMA -> producer: K, Q tiles of the stage consumed
-  B_GFULL = 2 * NS,  // MMA -> prep: G in TMEM
-  B_GFREE,           // prep -> MMA: G read (per P warp, 2)
-  B_TFULL,           // prep -> MMA: T diag(exp gc) and P written (per warp)
-  B_WFULL,           // MMA -> ff, prep: W^T, U^T in TMEM (T diag(exp gc) consumed)
-  B_CWDW,            // ff -> MMA: W^T bf16 in TMEM, Kd in smem, TM_X1 read (per warp)
-  B_MFULL,           // MMA -> ff: (M-I)^T in TMEM
-  B_MRDY,            // ff -> MMA: (M-I)^T in smem, TMEM free (per warp)
-  B_QFULL,           // MMA -> prep, ff: -W^T P^T in TMEM (W^T bf16 consumed)
-  B_QRDY,            // prep -> MMA: Q' in smem, TMEM read (per warp)
-  B_SRDY,            // chain -> MMA: S^T bf16 in TMEM (per warp)
-  B_SFULL,           // MMA -> chain, ff: state step done
-  B_OFULL,           // MMA -> chain, ff: the output group (U^T P^T + S^T Q'^T) done
-  B_OFREE,           // chain -> MMA: O^T read (per warp)
-  B_PFREE0,          // MMA -> prep: P buffer 0 consumed
-  B_PFREE1,          //                        1
-  B_DRAIN,           // MMA: everything issued has completed
-  B_CWDU,            // ff -> MMA: U^T bf16 in TMEM (per warp)
-  B_VFULL,           // [NS] producer -> MMA: the V tile of a stage loaded (count 1 + tx)
-  B_VEMPTY = B_VFULL + NS,  // [NS] chain -> producer: V slot free (per warp; it stages the outputs)
-  B_TRFULL = B_VEMPTY + NS,  // [2] producer -> prep: the chunk's T tile loaded (count 1 + tx)
-  B_TREMPTY = B_TRFULL + 2,  // [2] MMA -> producer: the T tile consumed (by the U product)
-  NBARS = B_TREMPTY + 2
+  B_EMPTY = NS,      // [NS] MMA -> producer: the stage consumed (state and output issuers, 2)
+  B_VFULL = 2 * NS,  // [NS] producer -> MMA: the V tile of a stage loaded (count 1 + tx)
+  B_VEMPTY = 3 * NS, // [NS] ff -> producer: V slot free (per warp; it stages the outputs)
+  B_TRFULL = 4 * NS, // [2] producer -> prep: the chunk's T tile loaded (count 1 + tx)
+  B_TREMPTY = 4 * NS + 2,  // [2] MMA -> producer: the T tile consumed (U and W products, 2)
+  B_WSFREE = 4 * NS + 4,   // [2] MMA -> ff: the W^T operand buffer consumed (by the S W product)
+  B_PFREE = 4 * NS + 6,    // [2] MMA -> prep: P buffer consumed (by the V~ P product)
+  B_WCVT = 4 * NS + 8,     // [2] ff -> MMA: W^T bf16 operand buffer filled (per warp)
+  B_GFULL = 4 * NS + 10,   // MMA -> prep: G in TMEM
+  B_TFULL,           // prep -> MMA: P, T (diag exp gc) and Q exp(gc) ready, G read (per warp)
+  B_WFULL,           // MMA -> ff, prep: W^T in TMEM (T diag(exp gc) consumed)
+  B_WREAD,           // ff -> MMA: W^T read out of TMEM (per warp)
+  B_VDONE,           // MMA -> chain: V~^T = U^T - S^T W^T in TMEM
+  B_VRDY,            // chain -> MMA: V~^T bf16 in TMEM, TM_V read (per warp)
+  B_SFULL,           // MMA -> chain, ff: the state update done
+  B_SRDY,            // chain -> MMA: S^T bf16 in TMEM, S^T scaled by exp(gc_C) (per warp)
+  B_SQDONE,          // MMA -> chain: the S^T (Q exp gc)^T product done (S^T bf16 consumed)
+  B_OFULL,           // MMA -> ff, chain: O^T in TMEM
+  B_OFREE,           // ff -> MMA: O^T read (per warp)
+  B_DRAIN,           // MMA: everything issued has completed (3 issuers)
+  NBARS
 };
-constexpr uint32_t SM_MISC = SM_BAR + NBARS * 8;  // tmem slot, abort flag, gate of the chunk
+constexpr uint32_t SM_MISC = SM_BAR + NBARS * 8;  // tmem slot, abort flag, spare, keep-TMEM flag
 constexpr uint32_t SMEM_TOTAL = OFF_SM + ((SM_MISC + 16 + 15) & ~15u);
 constexpr uint32_t SMEM_ALLOC = 232448;
-static_assert(SMEM_TOTAL <= SMEM_ALLOC, "shared memory budget");
+static_assert(SMEM_TOTAL + 1023 <= SMEM_ALLOC, "shared memory budget");
 
 // ---- TMEM columns ----
-constexpr uint32_t TM_S = 0;      // S^T fp32 [dv][dk]                128
-constexpr uint32_t TM_SBF = 128;  // S^T bf16 (packed)                 64
-constexpr uint32_t TM_O = 192;    // -W^T P^T, then O^T fp32           64
-constexpr uint32_t TM_X1 = 256;   // W^T | U^T fp32, then (M-I)^T     128
-constexpr uint32_t TM_G = 384;    // G fp32                            64
-constexpr uint32_t TM_WB = 448;   // W^T bf16 (packed)                 32
-constexpr uint32_t TM_UB = 480;   // U^T bf16 (packed)                 32
+constexpr uint32_t TM_S = 0;      // S^T fp32 [dv][dk]                   128
+constexpr uint32_t TM_SBF = 128;  // S^T bf16 (packed)                    64
+constexpr uint32_t TM_O = 192;    // O^T fp32 [dv][readout rows]          64
+constexpr uint32_t TM_G = 256;    // G fp32                               64
+constexpr uint32_t TM_W = 320;    // W^T fp32 [dk][64]                    64
+constexpr uint32_t TM_V = 384;    // U^T, then V~^T fp32 [dv][64]         64
+constexpr uint32_t TM_VB = 448;   // V~^T bf16 (packed)                   32
+constexpr uint32_t TM_VBD = 480;  // (V~ diag exp(gc_C - gc))^T bf16      32  (gated)
 constexpr uint32_t TM_COLS = 512;
 
 struct TcParams {
@@ -160,7 +151,6 @@ struct Smem {
   __device__ volatile int *abort_flag() const {
     return reinterpret_cast<volatile int *>(base + OFF_SM + SM_MISC + 4);
   }
-  __device__ float *gate_c() const { return reinterpret_cast<float *>(base + OFF_SM + SM_MISC + 8); }
   // set when a drain wait ran out: TMEM is then not freed at exit
   __device__ volatile int *keep_tmem() const {
     return reinterpret_cast<volatile int *>(base + OFF_SM + SM_MISC + 12);
@@ -263,16 +253,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(sm.bar(B_FULL + s), 2);
-      mbar_init(sm.bar(B_EMPTY + s), 1);
+      mbar_init(sm.bar(B_EMPTY + s), 2);
+      mbar_init(sm.bar(B_VFULL + s), 1);
       mbar_init(sm.bar(B_VEMPTY + s), 4);
     }
-    const int cnt[B_VFULL - 2 * NS] = {1, 2, 4, 1, 4, 1, 4, 1, 4, 4, 1, 1, 4, 1, 1, 3, 4};
-    for (int i = 2 * NS; i < B_VFULL; ++i) mbar_init(sm.bar(i), cnt[i - 2 * NS]);
-    for (int s = 0; s < NS; ++s) mbar_init(sm.bar(B_VFULL + s), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(sm.bar(B_TRFULL + s), 1);
-      mbar_init(sm.bar(B_TREMPTY + s), 1);
+      mbar_init(sm.bar(B_TREMPTY + s), 2);
+      mbar_init(sm.bar(B_WSFREE + s), 1);
+      mbar_init(sm.bar(B_PFREE + s), 1);
+      mbar_init(sm.bar(B_WCVT + s), 4);
     }
+    // count per barrier, from B_GFULL on
+    const int cnt[NBARS - B_GFULL] = {1, 4, 1, 4, 1, 4, 1, 4, 1, 1, 4, 3};
+    for (int i = B_GFULL; i < NBARS; ++i) mbar_init(sm.bar(i), cnt[i - B_GFULL]);
     *sm.abort_flag() = 0;
     *sm.keep_tmem() = 0;
     fence_mbar_init();
@@ -388,83 +382,101 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   } else if (warp == 1 || warp >= 14) {
     // ===================================================== MMA issuers
     // Three threads, each issuing one kind of work in a fixed order and
-    // blocking on the barriers of its inputs (a blocked try_wait wakes within
-    // ~100 cycles of the arrival; the tensor pipe interleaves their products
-    // in issue order):
-    //   warp 1   the recurrence: state step n (SRDY, MRDY, CWDU), then the
-    //            output group of n (QRDY), which reads the same bf16 S^T
-    //   warp 14  M(n) (CWDW), then the -W^T P^T helper of Q'(n) (OFREE(n-1))
-    //   warp 15  the look-ahead: G(0); per chunk W(m) (TFULL, MRDY(m-1)),
-    //            U(m) (VFULL), G(m+1) (FULL, GFREE(m))
+    // blocking on the barriers of its inputs; the tensor pipe executes their
+    // products in issue order.
+    //   warp 1   the recurrence, per chunk n: U^T = V^T T^T into TM_V (the
+    //            T slot loaded, V~ of n-1 read), V~^T -= S^T W^T (SRDY, the
+    //            W^T slot filled), then S^T += (V~ diag dec)^T K (VRDY)
+    // A thread waits for phase k of a barrier only where phase k+1 needs one
+    // of that thread's own later products (else a slow thread could see two
+    // completions as none): ring barriers carry the slot index.
+    //   warp 14  the outputs of n: O^T = S^T (Q exp gc)^T behind the S W
+    //            product (VDONE, OFREE(n-1)), O^T += V~^T P^T behind the
+    //            state update (SFULL)
+    //   warp 15  the look-ahead: G(0); per chunk W(m) (TFULL, WREAD(m-1)),
+    //            G(m+1) (FULL, TFULL(m))
     // Each commits the barriers of its own products; every hand-off between
     // kinds is a barrier.
     if (lane == 0) {
-      constexpr uint32_t id_uw = idesc_bf16(128, 64, true, false);
-      constexpr uint32_t id_m = idesc_bf16(128, 128, false, true, true);  // B = Kd, MN-major, negated
-      constexpr uint32_t id_q = idesc_bf16(128, 64, false, false, true);  // B = P, negated
-      constexpr uint32_t id_op = idesc_bf16(128, 64, false, false);       // B = P
-      constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);        // B = (M-I)^T or Kd, MN-major
-      constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);        // B = Q' (K-major)
+      constexpr uint32_t id_uw = idesc_bf16(128, 64, true, false);        // A = K^T or V^T (MN-major), B = T
+      constexpr uint32_t id_sw = idesc_bf16(128, 64, false, true, true);  // B = W^T (MN-major), negated
+      constexpr uint32_t id_kd = idesc_bf16(128, 128, false, true);       // B = K (MN-major)
+      constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);        // B = Q exp(gc) or P (K-major)
       constexpr uint32_t id_g = idesc_bf16(128, 64, false, false);
       const uint32_t a_tr = smem_u32(sm.base + OFF_TR), a_tw = smem_u32(sm.base + OFF_TW);
-      const uint32_t a_ms = smem_u32(sm.base + OFF_MS), a_p = smem_u32(sm.base + OFF_P);
-      auto kd_desc = [&](int m, int k) -> uint64_t {  // B = Kd (gated: V slot) or K
-        const uint32_t kq = smem_u32(sm.stage(m % NS));
-        return GATED ? sdesc_sw128(kq + ST_V0 + k * 2048, 8192, 1024)
-                     : sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024);
-      };
+      const uint32_t a_ws = smem_u32(sm.base + OFF_WS), a_p = smem_u32(sm.base + OFF_P);
       if (warp == 1) {
         for (int n = 0; n < NT; ++n) {
-          // ---- the state step ----
-          if (!wait_bar(sm, B_SRDY, n & 1, 1) || !wait_bar(sm, B_MRDY, n & 1, 1) ||
-              !wait_bar(sm, B_CWDU, n & 1, 1))
+          const int s = n % NS;
+          const uint32_t st = smem_u32(sm.stage(s));
+          // ---- U^T = V^T T^T ----
+          // (every wait here and below is on a barrier whose next phase
+          // needs this thread's own later products, so no phase can be
+          // skipped: the T ring slot is refilled only after this U product)
+          if (!wait_bar(sm, B_TRFULL + (n & 1), (n >> 1) & 1, 1) ||
+              !wait_bar(sm, B_VFULL + s, (n / NS) & 1, 1))
             break;
+          if (n >= 1 && !wait_bar(sm, B_VRDY, (n - 1) & 1, 1)) break;
           tc_fence_after();
+          const uint32_t tb = a_tr + (n & 1) * 8192;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + TM_V, sdesc_sw128(st + ST_V0 + k * 2048, 8192, 1024),
+                   sdesc_sw128(tb + k * 32, 0, 1024), id_uw, k > 0);
+          mma_commit(sm.bar(B_TREMPTY + (n & 1)));
+          // ---- V~^T = U^T - S^T W^T ----
+          if (!wait_bar(sm, B_SRDY, n & 1, 1) || !wait_bar(sm, B_WCVT + (n & 1), (n >> 1) & 1, 1)) break;
+          tc_fence_after();
+          const uint32_t wsb = a_ws + (n & 1) * 16384;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + TM_S, tmem + TM_SBF + k * 8, sdesc_sw128(a_ms + k * 2048, 16384, 1024), id_s, true);
+            mma_ts(tmem + TM_V, tmem + TM_SBF + k * 8, sdesc_sw128(wsb + k * 2048, 8192, 1024), id_sw, true);
+          mma_commit(sm.bar(B_VDONE));
+          mma_commit(sm.bar(B_WSFREE + (n & 1)));
+          // ---- S^T += V~^T Kd = (V~ diag exp(gc_C - gc))^T K (S^T was scaled by
+          //      exp(gc_C) by the chain warps) ----
+          if (!wait_bar(sm, B_VRDY, n & 1, 1)) break;
+          tc_fence_after();
+          constexpr uint32_t tm_a = GATED ? TM_VBD : TM_VB;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_S, tmem + TM_UB + k * 8, kd_desc(n, k), id_s, true);
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + TM_S, tmem + tm_a + k * 8, sdesc_sw128(st + ST_K0 + k * 2048, 16384, 1024), id_kd,
+                   true);
           mma_commit(sm.bar(B_SFULL));
-          // ---- the output group: O^T = U^T P^T + S^T Q'^T ----
-          if (!wait_bar(sm, B_QRDY, n & 1, 1)) break;
+          mma_commit(sm.bar(B_EMPTY + s));
+        }
+      } else if (warp == 14) {
+        for (int n = 0; n < NT; ++n) {
+          const int s = n % NS;
+          const uint32_t st = smem_u32(sm.stage(s));
+          // ---- O^T = S^T (Q exp gc)^T, behind the S W product (it reads the
+          //      same bf16 S^T, which is rewritten once both ended) ----
+          if (!wait_bar(sm, B_VDONE, n & 1, 1)) break;
+          if (n >= 1 && !wait_bar(sm, B_OFREE, (n - 1) & 1, 1)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t qa = st + (k < 4 ? ST_Q0 : ST_Q1) + (k & 3) * 32;
+            mma_ts(tmem + TM_O, tmem + TM_SBF + k * 8, sdesc_sw128(qa, 0, 1024), id_o, k > 0);
+          }
+          mma_commit(sm.bar(B_SQDONE));
+          // ---- O^T += V~^T P^T, behind the state update ----
+          if (!wait_bar(sm, B_SFULL, n & 1, 1)) break;
           tc_fence_after();
           const uint32_t pb = a_p + (n & 1) * 8192;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_O, tmem + TM_UB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_op, k > 0);
-          const uint32_t st = smem_u32(sm.stage(n % NS));
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t qa = st + (k < 4 ? ST_Q0 : ST_Q1) + (k & 3) * 32;
-            mma_ts(tmem + TM_O, tmem + TM_SBF + k * 8, sdesc_sw128(qa, 0, 1024), id_o, true);
-          }
+            mma_ts(tmem + TM_O, tmem + TM_VB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_o, true);
           mma_commit(sm.bar(B_OFULL));
-          mma_commit(sm.bar(B_PFREE0 + (n & 1)));
-          mma_commit(sm.bar(B_EMPTY + n % NS));
-        }
-      } else if (warp == 14) {
-        for (int m = 0; m < NT; ++m) {
-          // ---- (M-I)^T = -W^T Kd ----
-          if (!wait_bar(sm, B_CWDW, m & 1, 1)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_X1, tmem + TM_WB + k * 8, kd_desc(m, k), id_m, k > 0);
-          mma_commit(sm.bar(B_MFULL));
-          // ---- -W^T P^T (the rest of Q' is added on the CUDA cores) ----
-          if (m >= 1 && !wait_bar(sm, B_OFREE, (m - 1) & 1, 1)) break;
-          tc_fence_after();
-          const uint32_t pb = a_p + (m & 1) * 8192;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_O, tmem + TM_WB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_q, k > 0);
-          mma_commit(sm.bar(B_QFULL));
+          mma_commit(sm.bar(B_PFREE + (n & 1)));
+          mma_commit(sm.bar(B_EMPTY + s));
         }
       } else if (warp == 15) {
         // ---- G = [K;Q] K^T of chunk m ----
         auto issue_g = [&](int m) -> bool {
           if (!wait_bar(sm, B_FULL + m % NS, (m / NS) & 1, 1)) return false;
-          if (m >= 1 && !wait_bar(sm, B_GFREE, (m - 1) & 1, 1)) return false;
+          // TM_G is free once the prep warps handed over chunk m-1
+          if (m >= 1 && !wait_bar(sm, B_TFULL, (m - 1) & 1, 1)) return false;
           tc_fence_after();
           const uint32_t kq0 = smem_u32(sm.stage(m % NS));
 #pragma unroll
@@ -482,22 +494,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         for (int m = 0; ok && m < NT; ++m) {
           // ---- W^T = K^T (T diag exp gc)^T (ungated: T itself) ----
           if (!wait_bar(sm, B_TFULL, m & 1, 1)) break;
-          if (m >= 1 && !wait_bar(sm, B_MRDY, (m - 1) & 1, 1)) break;
+          if (m >= 1 && !wait_bar(sm, B_WREAD, (m - 1) & 1, 1)) break;
           tc_fence_after();
           const uint32_t kq = smem_u32(sm.stage(m % NS));
           const uint32_t wb = GATED ? a_tw : a_tr + (m & 1) * 8192;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_X1, sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024),
+            mma_ss(tmem + TM_W, sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024),
                    sdesc_sw128(wb + k * 32, 0, 1024), id_uw, k > 0);
-          // ---- U^T = V^T T^T ----
-          if (!wait_bar(sm, B_VFULL + m % NS, (m / NS) & 1, 1)) break;
-          tc_fence_after();
-          const uint32_t tb = a_tr + (m & 1) * 8192;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_X1 + 64, sdesc_sw128(kq + ST_V0 + k * 2048, 8192, 1024),
-                   sdesc_sw128(tb + k * 32, 0, 1024), id_uw, k > 0);
           mma_commit(sm.bar(B_WFULL));
           mma_commit(sm.bar(B_TREMPTY + (m & 1)));
           if (m + 1 < NT) ok = issue_g(m + 1);
@@ -509,83 +513,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncwarp();
   } else if (warp < 6) {
     // ===================================================== prep warps
-    // warps 2, 3 (TMEM lanes 64..127): P from rows 64..127 of G;
-    // warps 4, 5: the T tile of the UT pass, scaled to T diag(exp gc) for the
-    // W product (gated; ungated the W product reads T itself)
+    // per chunk m: P = Q K^T * Gam * M from rows 64..127 of G (warps 2, 3),
+    // T diag(exp gc) for the W product (warps 4, 5; gated), then Q exp(gc)
+    // in place over the Q tile (all four; gated), then TFULL (which also
+    // releases TM_G: every warp that reads G arrives on it after reading)
     const int q4 = warp & 3;              // TMEM lane quarter
     const int L = q4 * 32 + lane;         // TMEM lane of this thread
+    const int pt = tid - 64;              // 0..127 within the group
     float *eg = sm.arr(SM_EG), *ieg = sm.arr(SM_IEG), *gcs = sm.arr(SM_GC);
-    float *gq = sm.arr(SM_GQ);
-    // Q'(c) = exp(gc) Q - P W, in place over the Q tile of chunk c (same
-    // K-major layout: the output product reads it as its B operand); the
-    // scan for exp(gc) at the readout rows first
-    auto qprime = [&](int c) {
-      const int s = c % NS;
-      const Rows rw(c, n_h, p.T);
-      if (GATED) wait_bar(sm, B_FULL + s, (c / NS) & 1, 2);  // the chunk's log-gate row
-      if (GATED && warp == 2) {
-        float lo, hi;
-        warp_scan64(sm.lam(s), lane, lo, hi);
-        const float elo = fast_exp2(lo), ehi = fast_exp2(hi);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int r = lane + 32 * hf;
-          const int pos = rw.pos(r, n_h);
-          const float a = __shfl_sync(0xffffffffu, elo, pos & 31);
-          const float e = __shfl_sync(0xffffffffu, ehi, pos & 31);
-          gq[r] = r < rw.Cp ? (pos < 32 ? a : e) : 0.f;
-        }
-      }
-      if (GATED) named_sync(1);
-      wait_bar(sm, B_QFULL, c & 1, 2);
-      tc_fence_after();
-      {
-        // Warp-MMA fragments throughout: the tile of this warp (d = 32 q4 ..
-        // 32 q4 + 31, all 64 rows) goes in 8x8 pieces; a thread holds the
-        // pairs (d = t / 4 (+ 8), rows 8 g + 2 (t % 4), + 1) of TMEM, of Q
-        // (transposing 8x8 loads) and of Q' (transposing 8x8 stores, to the
-        // addresses the loads came from)
-        const int tq = lane & 3;
-        float2 gv[8];
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          gv[g] = GATED ? *reinterpret_cast<const float2 *>(gq + 8 * g + 2 * tq) : make_float2(1.f, 1.f);
-        const int cp = rw.Cp;
-        const uint32_t qh = smem_u32(sm.stage(s) + ((q4 >> 1) ? ST_Q1 : ST_Q0));
-        const int mi = lane >> 3, mr = lane & 7;  // the 8x8 piece and row this lane addresses
-#pragma unroll
-        for (int b16 = 0; b16 < 32; b16 += 16) {
-          uint32_t hreg[32];
-          tmem_ld16x256b_x8(tmem_addr(tmem + TM_O, q4 * 32 + b16, 0), hreg);
-          tmem_wait_ld_regs(hreg);
-          const int ck = (32 * (q4 & 1) + b16) / 8 + (mi & 1);  // 16-byte piece of the row
-          // all loads of this half first (the stores go to the same places)
-          uint32_t addr[4], qd[4][4];
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int row = 16 * cc + 8 * (mi >> 1) + mr;
-            addr[cc] = qh + (row >> 3) * 1024 + (row & 7) * 128 + ((ck ^ (row & 7)) << 4);
-            ldsm_x4_trans(addr[cc], qd[cc]);
-          }
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t o4[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int g = 2 * cc + (m >> 1), j = 4 * g + 2 * (m & 1);
-              const int r0 = 8 * g + 2 * tq;
-              const float v0 = fmaf(gv[g].x, __uint_as_float(qd[cc][m] << 16), __uint_as_float(hreg[j]));
-              const float v1 = fmaf(gv[g].y, __uint_as_float(qd[cc][m] & 0xFFFF0000u), __uint_as_float(hreg[j + 1]));
-              o4[m] = pack_bf16(r0 < cp ? v0 : 0.f, r0 + 1 < cp ? v1 : 0.f);
-            }
-            stsm_x4_trans(addr[cc], o4);
-          }
-        }
-        tc_fence_before();
-      }
-      fence_proxy_async_smem();
-      arrive_warp(sm.bar(B_QRDY), lane);
-    };
     for (int m = 0; m < NT; ++m) {
       const int s = m % NS;
       // every warp of the group is done with the previous chunk's gate
@@ -605,14 +540,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         ieg[lane + 32] = fast_exp2(-hi);
       }
       if (named_sync_or(1, *sm.abort_flag() != 0)) break;
+      const Rows rw(m, n_h, p.T);
       if (warp < 4) {
-        // ---- P = Q K^T * Gam * M: one readout row per thread, 16 columns
-        //      at a time, into the P buffer of this chunk ----
-        const Rows rw(m, n_h, p.T);
+        // ---- P: one readout row per thread, 16 columns at a time ----
         // exact per-entry decay only when the chunk's gate product leaves
         // the range of the ratio form (uniform per chunk)
         const bool ratio = !GATED || gcs[63] >= kRatioFloor;
-        if (m >= 2) wait_bar(sm, B_PFREE0 + (m & 1), ((m >> 1) - 1) & 1, 2);
+        if (m >= 2) wait_bar(sm, B_PFREE + (m & 1), ((m >> 1) - 1) & 1, 2);
         wait_bar(sm, B_GFULL, m & 1, 2);
         tc_fence_after();
         const int r = L - 64;
@@ -653,28 +587,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           st_chunk(prow + sw128_offset(r, jb, 64), {pk[0], pk[1], pk[2], pk[3]});
           st_chunk(prow + sw128_offset(r, jb + 8, 64), {pk[4], pk[5], pk[6], pk[7]});
         }
-        tc_fence_before();
-        arrive_warp(sm.bar(B_GFREE), lane);
       } else {
         // ---- the T tile of this chunk (UT pass) has landed; gated, T diag(exp gc)
-        //      into its own buffer, free once the previous chunk's W and U ended ----
+        //      into its own buffer, free once the previous chunk's W product ended ----
         wait_bar(sm, B_TRFULL + (m & 1), (m >> 1) & 1, 2);
         if (GATED) {
           if (m >= 1) wait_bar(sm, B_WFULL, (m - 1) & 1, 2);
           const uint8_t *tt = sm.base + OFF_TR + (m & 1) * 8192;
           uint8_t *tw = sm.base + OFF_TW;
           const int ft = tid - 128;  // 0..63
+          uint4 v[8];
+#pragma unroll
+          for (int it = 0; it < 8; ++it) v[it] = *reinterpret_cast<const uint4 *>(tt + (ft + 64 * it) * 16);
 #pragma unroll
           for (int it = 0; it < 8; ++it) {
             // 16-byte piece qi of the swizzled tile: row qi / 8, columns
             // 8 ((qi % 8) ^ (row % 8)) .. + 7
             const int qi = ft + 64 * it, row = qi >> 3;
             const int c0 = 8 * ((qi & 7) ^ (row & 7));
-            const uint4 v = *reinterpret_cast<const uint4 *>(tt + qi * 16);
             const float4 e0 = *reinterpret_cast<const float4 *>(eg + c0);
             const float4 e1 = *reinterpret_cast<const float4 *>(eg + c0 + 4);
             const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t in[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
             uint32_t o4[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -684,199 +618,78 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           }
         }
       }
+      if (GATED) {
+        // ---- Q exp(gc) in place: readout row r scaled by exp(gc) at its
+        //      sub-step, rows past the chunk's readouts zeroed; the G product
+        //      (which read Q) has completed ----
+        if (warp >= 4) wait_bar(sm, B_GFULL, m & 1, 2);
+        uint8_t *qt = sm.stage(s);
+        uint4 v[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int qi = pt + 128 * it;  // 16-byte piece: 512 per 64-column half
+          v[it] = *reinterpret_cast<const uint4 *>(qt + ((qi >> 9) ? ST_Q1 : ST_Q0) + (qi & 511) * 16);
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int qi = pt + 128 * it, row = (qi & 511) >> 3;
+          const float f = row < rw.Cp ? eg[rw.pos(row, n_h)] : 0.f;
+          const uint32_t in[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+          uint32_t o4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            o4[u] = pack_bf16(__uint_as_float(in[u] << 16) * f, __uint_as_float(in[u] & 0xFFFF0000u) * f);
+          st_chunk(qt + ((qi >> 9) ? ST_Q1 : ST_Q0) + (qi & 511) * 16, o4);
+        }
+      }
+      // TFULL also hands TM_G back: the G product of the next chunk waits for it
+      tc_fence_before();
       fence_proxy_async_smem();
       arrive_warp(sm.bar(B_TFULL), lane);
-      // Q' of the previous chunk, as soon as its -W^T P^T helper is in TMEM
-      if (m >= 1) {
-        if (named_sync_or(1, *sm.abort_flag() != 0)) break;
-        qprime(m - 1);
-      }
     }
-    if (NT >= 1 && !named_sync_or(1, *sm.abort_flag() != 0)) qprime(NT - 1);
   } else if (warp < 10) {
     // ===================================================== feed-forward warps
+    // W^T(m) -> bf16 operand in shared memory, one chunk ahead; the outputs
+    // of chunk m -> global memory
     const int q4 = warp & 3;
     const int L = q4 * 32 + lane;  // TMEM lane: a d index
     const int ft = tid - 192;      // 0..127 within the group
-    float *dec = sm.arr(SM_DEC);
-    for (int c = 0; c < NT; ++c) {
-      const int s = c % NS;
-      // every warp of the group is done with the previous chunk's gate
-      // factors before they are rewritten
-      if (named_sync_or(2, *sm.abort_flag() != 0)) break;
-      if (GATED) {
-        wait_bar(sm, B_FULL + s, (c / NS) & 1, 3);
-        if (warp == 6) {
-          float lo, hi;
-          warp_scan64(sm.lam(s), lane, lo, hi);
-          const float tot = __shfl_sync(0xffffffffu, hi, 31);
-          dec[lane] = fast_exp2(tot - lo);
-          dec[lane + 32] = fast_exp2(tot - hi);
-          if (lane == 0) *sm.gate_c() = fast_exp2(tot);
-        }
-        named_sync(2);
-      }
-
-      // ---- W^T, U^T -> bf16 operands (both read out of TM_X1 first, so
-      //      that the M product may overwrite it); Kd ----
-      wait_bar(sm, B_WFULL, c & 1, 3);
+    auto w_convert = [&](int m) {
+      // ---- W^T (row L = a dk index, 64 columns) -> bf16 rows of the MN-major
+      //      operand W^T [dk][64] ----
+      wait_bar(sm, B_WFULL, m & 1, 3);
       tc_fence_after();
-      uint32_t pw_[32], pu[32];
+      uint32_t pw_[32];
       {
         uint32_t r[64];
-        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+        tmem_ld32(tmem_addr(tmem + TM_W, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+        tmem_ld32(tmem_addr(tmem + TM_W, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
         tmem_wait_ld_regs(r);
+        tc_fence_before();
+        arrive_warp(sm.bar(B_WREAD), lane);
 #pragma unroll
         for (int u = 0; u < 32; ++u)
           pw_[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
       }
-      {
-        uint32_t r[64];
-        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 64), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
-        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, 96), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
-        tmem_wait_ld_regs(r);
+      // the S W product of the chunk two back reads this buffer until it ends
+      if (m >= 2) wait_bar(sm, B_WSFREE + (m & 1), ((m >> 1) - 1) & 1, 3);
+      uint8_t *ws = sm.base + OFF_WS + (m & 1) * 16384;
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
-          pu[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-      }
-      // W^T bf16 of the previous chunk is read by its M and -W^T P^T products
-      // (the -W^T P^T product is issued after M and commits QFULL)
-      if (c >= 1) {
-        wait_bar(sm, B_QFULL, (c - 1) & 1, 3);
-        tc_fence_after();
-      }
-      tmem_st32(tmem_addr(tmem + TM_WB, q4 * 32, 0), pw_);
-      if (GATED) {
-        // Kd = diag(exp(gc_C - gc)) K into the V slot (V was consumed by U)
-        const uint8_t *kt = sm.stage(s);
-        uint8_t *kd = sm.stage(s) + ST_V0;
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int qi = ft + 128 * it;  // 16-byte chunk: 512 per 64-column half
-          const int half = qi >> 9, rem = qi & 511, row = rem >> 3;
-          const uint4 v = *reinterpret_cast<const uint4 *>(kt + half * 16384 + rem * 16);
-          const float dr = dec[row];
-          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            o4[u] = pack_bf16(__uint_as_float(in[u] << 16) * dr, __uint_as_float(in[u] & 0xFFFF0000u) * dr);
-          st_chunk(kd + half * 8192 + rem * 16, o4);
-        }
-        fence_proxy_async_smem();
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      arrive_warp(sm.bar(B_CWDW), lane);
-      // U^T bf16 of the previous chunk is read by its state step and its
-      // output group (U^T P^T) until the output group ends
-      if (c >= 1) {
-        wait_bar(sm, B_OFULL, (c - 1) & 1, 3);
-        tc_fence_after();
-      }
-      tmem_st32(tmem_addr(tmem + TM_UB, q4 * 32, 0), pu);
-      tmem_wait_st();
-      tc_fence_before();
-      arrive_warp(sm.bar(B_CWDU), lane);
-
-      // ---- (M-I)^T -> bf16 smem operand (row L = j, columns i); the state
-      //      step of the previous chunk reads the old one until it ends ----
-      wait_bar(sm, B_MFULL, c & 1, 3);
-      if (c >= 1) wait_bar(sm, B_SFULL, (c - 1) & 1, 3);
-      tc_fence_after();
-      const float gm1 = GATED ? *sm.gate_c() - 1.f : 0.f;
-#pragma unroll 1
-      for (int cb = 0; cb < 128; cb += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tmem + TM_X1, q4 * 32, cb), r);
-        tmem_wait_ld_regs(r);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t o4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            o4[u] = pack_bf16(__uint_as_float(r[q * 8 + 2 * u]), __uint_as_float(r[q * 8 + 2 * u + 1]));
-          st_chunk(sm.base + OFF_MS + sw128_offset(L, cb + q * 8, 128), o4);
-        }
-      }
-      if (GATED) {
-        // the (exp(gc_C) - 1) I term, on this thread's own diagonal entry
-        __nv_bfloat16 *dg = reinterpret_cast<__nv_bfloat16 *>(sm.base + OFF_MS + sw128_offset(L, L, 128));
-        *dg = __float2bfloat16_rn(__bfloat162float(*dg) + gm1);
-      }
-      tc_fence_before();
+      for (int q = 0; q < 8; ++q)
+        st_chunk(ws + sw128_offset(L, 8 * q, 128), {pw_[4 * q], pw_[4 * q + 1], pw_[4 * q + 2], pw_[4 * q + 3]});
       fence_proxy_async_smem();
-      arrive_warp(sm.bar(B_MRDY), lane);
-
-    }
-  } else {
-    // ===================================================== chain warps
-    const int q4 = warp & 3;
-    const int L = q4 * 32 + lane;  // TMEM lane = value column dv
-    // ---- initial state S^T (lane = dv, column = dk) ----
-    {
-      const float *h0 = p.h0 ? p.h0 + (size_t)bh * D * D : nullptr;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t f[32], pk[16];
-#pragma unroll
-        for (int u = 0; u < 32; u += 2) {
-          const float x0 = h0 ? h0[(size_t)(c0 + u) * D + L] : 0.f;
-          const float x1 = h0 ? h0[(size_t)(c0 + u + 1) * D + L] : 0.f;
-          f[u] = __float_as_uint(x0);
-          f[u + 1] = __float_as_uint(x1);
-          pk[u >> 1] = pack_bf16(x0, x1);
-        }
-        tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, c0), f);
-        tmem_st16(tmem_addr(tmem + TM_SBF, q4 * 32, c0 / 2), pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      arrive_warp(sm.bar(B_SRDY), lane);
-    }
+      arrive_warp(sm.bar(B_WCVT + (m & 1)), lane);
+    };
+    if (!named_sync_or(2, *sm.abort_flag() != 0)) w_convert(0);
     for (int n = 0; n < NT; ++n) {
-      if (named_sync_or(3, *sm.abort_flag() != 0)) break;
+      if (named_sync_or(2, *sm.abort_flag() != 0)) break;
+      if (n + 1 < NT) w_convert(n + 1);
       const Rows rw(n, n_h, p.T);
-      // ---- state: S^T -> bf16 operand for the next chunk, or hT ----
-      wait_bar(sm, B_SFULL, n & 1, 4);
-      tc_fence_after();
-      if (n + 1 < NT) {
-        uint32_t pk[64];
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, cb * 32), r);
-          tmem_wait_ld_regs(r);
-#pragma unroll
-          for (int u = 0; u < 16; ++u)
-            pk[cb * 16 + u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-        }
-        // the output products of chunk n read the bf16 copy until they end
-        wait_bar(sm, B_OFULL, n & 1, 4);
-        tc_fence_after();
-        tmem_st32(tmem_addr(tmem + TM_SBF, q4 * 32, 0), *reinterpret_cast<uint32_t (*)[32]>(&pk[0]));
-        tmem_st32(tmem_addr(tmem + TM_SBF, q4 * 32, 32), *reinterpret_cast<uint32_t (*)[32]>(&pk[32]));
-        tmem_wait_st();
-        tc_fence_before();
-        arrive_warp(sm.bar(B_SRDY), lane);
-      } else if (p.hT) {
-        float *hT = p.hT + (size_t)bh * D * D;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0), r);
-          tmem_wait_ld_regs(r);
-#pragma unroll
-          for (int u = 0; u < 32; ++u) hT[(size_t)(c0 + u) * D + L] = __uint_as_float(r[u]);
-        }
-      }
-      // ---- outputs of this chunk: the accumulator is read at once (TMEM is
+      // ---- outputs of chunk n: the accumulator is read at once (TMEM is
       //      released early), staged as bf16 rows in the V slot of this chunk
-      //      (its last reader, the U product or, gated, the state step on Kd,
-      //      has completed) by transposing 8x8 stores, then written out in
-      //      16-byte pieces ----
-      wait_bar(sm, B_OFULL, n & 1, 4);
+      //      (its reader, the U product, has completed) by transposing 8x8
+      //      stores, then written out in 16-byte pieces ----
+      wait_bar(sm, B_OFULL, n & 1, 3);
       tc_fence_after();
       uint32_t o0[32], o1[32];
       tmem_ld16x256b_x8(tmem_addr(tmem + TM_O, q4 * 32, 0), o0);
@@ -899,32 +712,154 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t o4[4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int j = 4 * (2 * cc + (m >> 1)) + 2 * (m & 1);
-              o4[m] = pack_bf16(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]));
+            for (int mm = 0; mm < 4; ++mm) {
+              const int j = 4 * (2 * cc + (mm >> 1)) + 2 * (mm & 1);
+              o4[mm] = pack_bf16(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]));
             }
             const int r = 16 * cc + 8 * (mi >> 1) + mr;
             stsm_x4_trans(srow(r) + ((k ^ (r & 7)) << 4), o4);
           }
         }
-        named_sync(3);  // every value column of every row staged
-        const int ct = tid - 320;  // 0..127 within the group
-        const int k = ct & 15, cp = rw.Cp;
+        named_sync(2);  // every value column of every row staged
+        const int k = ft & 15, cp = rw.Cp;
         __nv_bfloat16 *obase = p.out + (((size_t)b * p.T + rw.t_lo) * p.H + h) * D + 8 * k;
         const size_t rstride = (size_t)p.H * D;
         uint4 v[8];  // every load before the first store
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
-          const int r = 8 * it + (ct >> 4);
+          const int r = 8 * it + (ft >> 4);
           v[it] = lds128(srow(r) + ((k ^ (r & 7)) << 4));
         }
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
-          const int r = 8 * it + (ct >> 4);
+          const int r = 8 * it + (ft >> 4);
           if (r < cp) *reinterpret_cast<uint4 *>(obase + r * rstride) = v[it];
         }
         // the V slot is free once every warp has read its rows
         arrive_warp(sm.bar(B_VEMPTY + n % NS), lane);
+      }
+    }
+  } else {
+    // ===================================================== chain warps
+    // the recurrence: V~^T -> bf16 operand; the updated state S^T -> bf16
+    // operand and, gated, scaled in place by the next chunk's exp(gc_C); hT
+    const int q4 = warp & 3;
+    const int L = q4 * 32 + lane;  // TMEM lane = value column dv
+    // exp(gc_C) of chunk m: 2^(sum of its log2 gate)
+    auto gate_total = [&](int m) -> float {
+      const int s = m % NS;
+      wait_bar(sm, B_FULL + s, (m / NS) & 1, 4);
+      float t = sm.lam(s)[lane] + sm.lam(s)[lane + 32];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      return fast_exp2(t);
+    };
+    // ---- initial state: S^T bf16 = h0^T, S^T fp32 = exp(gc_C) h0^T ----
+    {
+      const float *h0 = p.h0 ? p.h0 + (size_t)bh * D * D : nullptr;
+      const float gc0 = GATED ? gate_total(0) : 1.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t f[32], pk[16];
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+          const float x0 = h0 ? h0[(size_t)(c0 + u) * D + L] : 0.f;
+          const float x1 = h0 ? h0[(size_t)(c0 + u + 1) * D + L] : 0.f;
+          f[u] = __float_as_uint(x0 * gc0);
+          f[u + 1] = __float_as_uint(x1 * gc0);
+          pk[u >> 1] = pack_bf16(x0, x1);
+        }
+        tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, c0), f);
+        tmem_st16(tmem_addr(tmem + TM_SBF, q4 * 32, c0 / 2), pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      arrive_warp(sm.bar(B_SRDY), lane);
+    }
+    float *dec = sm.arr(SM_DEC);
+    for (int n = 0; n < NT; ++n) {
+      if (named_sync_or(3, *sm.abort_flag() != 0)) break;
+      if (GATED) {
+        // exp(gc_C - gc) of chunk n (the factor of the state update's keys)
+        wait_bar(sm, B_FULL + n % NS, (n / NS) & 1, 4);
+        if (warp == 10) {
+          float lo, hi;
+          warp_scan64(sm.lam(n % NS), lane, lo, hi);
+          const float tot = __shfl_sync(0xffffffffu, hi, 31);
+          dec[lane] = fast_exp2(tot - lo);
+          dec[lane + 32] = fast_exp2(tot - hi);
+        }
+        named_sync(3);
+      }
+      // ---- V~^T -> bf16 operands: V~^T for the V~ P product and, gated,
+      //      (V~ diag exp(gc_C - gc))^T for the state update; the products of
+      //      the previous chunk read the old ones until the output group ended
+      //      (it is issued after the state update) ----
+      wait_bar(sm, B_VDONE, n & 1, 4);
+      tc_fence_after();
+      if (n >= 1) {
+        wait_bar(sm, B_OFULL, (n - 1) & 1, 4);
+        tc_fence_after();
+      }
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t r[32], pv[16];
+        tmem_ld32(tmem_addr(tmem + TM_V, q4 * 32, 32 * hf), r);
+        tmem_wait_ld_regs(r);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) pv[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+        tmem_st16(tmem_addr(tmem + TM_VB, q4 * 32, 16 * hf), pv);
+        if (GATED) {
+#pragma unroll
+          for (int u = 0; u < 16; u += 2) {
+            const float4 d4 = *reinterpret_cast<const float4 *>(dec + 32 * hf + 2 * u);
+            pv[u] = pack_bf16(__uint_as_float(r[2 * u]) * d4.x, __uint_as_float(r[2 * u + 1]) * d4.y);
+            pv[u + 1] = pack_bf16(__uint_as_float(r[2 * u + 2]) * d4.z, __uint_as_float(r[2 * u + 3]) * d4.w);
+          }
+          tmem_st16(tmem_addr(tmem + TM_VBD, q4 * 32, 16 * hf), pv);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      arrive_warp(sm.bar(B_VRDY), lane);
+      // ---- the updated state: S^T -> bf16 operand for the next chunk (and,
+      //      gated, S^T <- exp(gc_C) S^T in place), or hT; the S W and
+      //      S (Q exp gc) products of this chunk read the old bf16 copy ----
+      wait_bar(sm, B_SFULL, n & 1, 4);
+      tc_fence_after();
+      if (n + 1 < NT) {
+        const float gcn = GATED ? gate_total(n + 1) : 1.f;
+        wait_bar(sm, B_SQDONE, n & 1, 4);
+        tc_fence_after();
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r[64], pk[32];
+          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, 64 * hf), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, 64 * hf + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+          tmem_wait_ld_regs(r);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) pk[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+          tmem_st32(tmem_addr(tmem + TM_SBF, q4 * 32, 32 * hf), pk);
+          if (GATED) {
+#pragma unroll
+            for (int u = 0; u < 64; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * gcn);
+            tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, 64 * hf), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
+            tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, 64 * hf + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        arrive_warp(sm.bar(B_SRDY), lane);
+      } else if (p.hT) {
+        float *hT = p.hT + (size_t)bh * D * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0), r);
+          tmem_wait_ld_regs(r);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) hT[(size_t)(c0 + u) * D + L] = __uint_as_float(r[u]);
+        }
       }
     }
   }
