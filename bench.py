@@ -545,6 +545,10 @@ def run_ours(args, dist):
     recs, hosts = {}, {}
     for wid in ids:
         w = synth.WORKLOADS[wid]
+        if args.batch:
+            # a smaller copy of the workload (profiler captures): same heads,
+            # lengths and distributions, fewer batch rows
+            w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
         recs[wid], host = measure(w, wr, dist, dev, args, peaks, peak_src,
                                   clocks_on=dist.local == 0)
         if wid == ids[0]:
@@ -553,6 +557,8 @@ def run_ours(args, dist):
     head_id = ids[0]
     head = recs[head_id]
     w = synth.WORKLOADS[head_id]
+    if args.batch:
+        w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
 
     # ---- CPU oracle on the headline workload (rank 0, N = 1 only) ----
     cpu = None
@@ -598,7 +604,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="all", choices=["all", "2", "3", "4", "5"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the selected workload(s) with this many batch rows "
+                         "instead (for profiler captures; not a bench line)")
     args = ap.parse_args(argv)
+    if args.batch < 0:
+        ap.error("--batch must be >= 0")
     # at least 3 untimed warm-up steps, whatever is asked
     args.warmup = max(args.warmup, 3)
     dist = Dist()

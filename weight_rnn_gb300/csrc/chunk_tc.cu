@@ -41,8 +41,9 @@
 //   warps 1, 14, 15  MMA issuers (one thread each): the recurrence (U, V~,
 //                the state update); the outputs; the look-ahead G, W.
 //                Warp 1 owns the TMEM allocation.
-//   warps 2-5    prep: P from G, T diag(exp gc), Q exp(gc) in place
-//   warps 6-9    feed-forward: W^T -> bf16 smem operand (one chunk ahead),
+//   warps 2-5    prep: P from G, T diag(exp gc)
+//   warps 6-9    feed-forward: W^T -> bf16 smem operand and Q exp(gc) in
+//                place (one chunk ahead),
 //                the outputs (staged through the V slot by transposing 8x8
 //                stores, then 16-byte global stores)
 //   warps 10-13  chain: V~^T -> bf16 operands (plain, and scaled by dec for
@@ -82,17 +83,17 @@ constexpr uint32_t OFF_TW = OFF_WS + 32768;    // T diag(exp gc) bf16 [64][64], 
 constexpr uint32_t OFF_P = OFF_TW + 8192;      // 2 x P bf16 [64][64], K-major
 constexpr uint32_t OFF_TR = OFF_P + 16384;     // 2 x T bf16 [64][64] (TMA ring), K-major
 constexpr uint32_t OFF_SM = OFF_TR + 16384;    // small arrays and barriers
-constexpr uint32_t SM_BETA = 0;                // [NS][64]
-constexpr uint32_t SM_LAM = SM_BETA + NS * 256;  // [NS][64] log2 gate
-constexpr uint32_t SM_EG = SM_LAM + NS * 256;    // prep: 2^gc
-constexpr uint32_t SM_IEG = SM_EG + 256;         // prep: 2^-gc
-constexpr uint32_t SM_GC = SM_IEG + 256;         // prep: gc (cumulative log2 gate)
-constexpr uint32_t SM_DEC = SM_GC + 256;         // chain: 2^(gc_C - gc)
-constexpr uint32_t SM_BAR = SM_DEC + 256;
+constexpr uint32_t SM_LAM = 0;                 // prep: the chunk's log2 gate
+constexpr uint32_t SM_EG = SM_LAM + 256;         // prep: 2^gc
+constexpr uint32_t SM_GC = SM_EG + 256;          // prep: gc (cumulative log2 gate)
+constexpr uint32_t SM_DEC = SM_GC + 256;         // [4][64] prep -> chain: 2^(gc_C - gc) / sigma'
+constexpr uint32_t SM_QF = SM_DEC + 1024;        // [4][64] prep -> ff: 2^gc at each readout row's sub-step
+constexpr uint32_t SM_PLAN = SM_QF + 1024;       // [4] ChunkPlan, prep -> chain, MMA, ff
+constexpr uint32_t SM_BAR = SM_PLAN + 64;
 
 // ---- barrier indices ----
 enum {
-  B_FULL = 0,        // [NS] producer -> all: K, Q tiles, beta, log gate loaded (count 2 + tx)
+  B_FULL = 0,        // [NS] producer -> all: K, Q tiles loaded (count 1 + tx)
   B_EMPTY = NS,      // [NS] MMA -> producer: the stage consumed (state and output issuers, 2)
   B_VFULL = 2 * NS,  // [NS] producer -> MMA: the V tile of a stage loaded (count 1 + tx)
   B_VEMPTY = 3 * NS, // [NS] ff -> producer: V slot free (per warp; it stages the outputs)
@@ -101,8 +102,10 @@ enum {
   B_WSFREE = 4 * NS + 4,   // [2] MMA -> ff: the W^T operand buffer consumed (by the S W product)
   B_PFREE = 4 * NS + 6,    // [2] MMA -> prep: P buffer consumed (by the V~ P product)
   B_WCVT = 4 * NS + 8,     // [2] ff -> MMA: W^T bf16 operand buffer filled (per warp)
-  B_GFULL = 4 * NS + 10,   // MMA -> prep: G in TMEM
-  B_TFULL,           // prep -> MMA: P, T (diag exp gc) and Q exp(gc) ready, G read (per warp)
+  B_TFULL = 4 * NS + 10,   // [2] prep -> MMA: P, T (diag exp gc) and Q exp(gc) of a chunk ready (per warp)
+  B_PLAN = 4 * NS + 12,    // [4] prep -> chain, MMA: the chunk's ChunkPlan, dec and readout factors (gated)
+  B_GFULL = 4 * NS + 16,   // MMA -> prep: G in TMEM
+  B_GFREE,           // prep -> MMA: G read (per P warp, 2)
   B_WFULL,           // MMA -> ff, prep: W^T in TMEM (T diag(exp gc) consumed)
   B_WREAD,           // ff -> MMA: W^T read out of TMEM (per warp)
   B_VDONE,           // MMA -> chain: V~^T = U^T - S^T W^T in TMEM
@@ -131,6 +134,21 @@ constexpr uint32_t TM_VB = 448;   // V~^T bf16 (packed)                   32
 constexpr uint32_t TM_VBD = 480;  // (V~ diag exp(gc_C - gc))^T bf16      32  (gated)
 constexpr uint32_t TM_COLS = 512;
 
+// Gated: TMEM holds S~ = S / sigma, sigma = 2^ls.  Each chunk's decay
+// exp(gc_C) goes into sigma (sigma' = exp(gc_C) sigma) and the accumulator is
+// only added to, until sigma would fall below 2^-kSigmaRange: then the state
+// is rescaled in TMEM instead (sigma' = 1), so S~ stays within 2^64 |S|.
+constexpr float kSigmaRange = 64.f;
+
+// The per-chunk decisions of the gated state update, made by the prep warps
+// (in chunk order, ahead of the chain) and read by the others.
+struct ChunkPlan {
+  float rs;   // TMEM factor before the chunk's update (1 unless rescaled)
+  float sig;  // sigma of the state after the chunk's update
+  int ratio;  // the chunk is in the ratio regime (decay product >= 2^-100)
+  int pad;
+};
+
 struct TcParams {
   const float *beta, *g, *h0;
   __nv_bfloat16 *out;
@@ -142,8 +160,10 @@ struct Smem {
   uint8_t *base;
   __device__ uint8_t *stage(int s) const { return base + s * STAGE_BYTES; }
   __device__ float *arr(uint32_t off) const { return reinterpret_cast<float *>(base + OFF_SM + off); }
-  __device__ float *beta(int s) const { return arr(SM_BETA + s * 256); }
-  __device__ float *lam(int s) const { return arr(SM_LAM + s * 256); }
+  __device__ float *lam() const { return arr(SM_LAM); }
+  __device__ volatile ChunkPlan *plan(int m) const {
+    return reinterpret_cast<volatile ChunkPlan *>(base + OFF_SM + SM_PLAN) + (m & 3);
+  }
   __device__ uint64_t *bar(int i) const {
     return reinterpret_cast<uint64_t *>(base + OFF_SM + SM_BAR) + i;
   }
@@ -252,7 +272,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   __syncthreads();
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(sm.bar(B_FULL + s), 2);
+      mbar_init(sm.bar(B_FULL + s), 1);
       mbar_init(sm.bar(B_EMPTY + s), 2);
       mbar_init(sm.bar(B_VFULL + s), 1);
       mbar_init(sm.bar(B_VEMPTY + s), 4);
@@ -263,9 +283,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(sm.bar(B_WSFREE + s), 1);
       mbar_init(sm.bar(B_PFREE + s), 1);
       mbar_init(sm.bar(B_WCVT + s), 4);
+      mbar_init(sm.bar(B_TFULL + s), 4);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(sm.bar(B_PLAN + s), 1);
     // count per barrier, from B_GFULL on
-    const int cnt[NBARS - B_GFULL] = {1, 4, 1, 4, 1, 4, 1, 4, 1, 1, 4, 3};
+    const int cnt[NBARS - B_GFULL] = {1, 2, 1, 4, 1, 4, 1, 4, 1, 1, 4, 3};
     for (int i = B_GFULL; i < NBARS; ++i) mbar_init(sm.bar(i), cnt[i - B_GFULL]);
     *sm.abort_flag() = 0;
     *sm.keep_tmem() = 0;
@@ -289,24 +311,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 
   if (warp == 0) {
     // ===================================================== TMA producer
-    // beta and the log gate of a chunk are read from global memory one chunk
-    // ahead (registers), so that a stage is complete as soon as its tiles land
-    float nb[2], nl[2];
-    auto fetch = [&](int n) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int e = n * C + lane + 32 * k;
-        float bt = 0.f, lg = 0.f;
-        if (n < NT && e < p.L) {
-          bt = p.beta[((size_t)b * p.L + e) * p.H + h];
-          if (GATED && (e % n_h) == 0)
-            lg = fmaxf(logf(p.g[((size_t)b * p.T + e / n_h) * p.H + h]), kLogGateFloor) * kLog2e;
-        }
-        nb[k] = bt;
-        nl[k] = lg;
-      }
-    };
-    fetch(0);
+    // (tiles only: beta is inside T, and the prep warps read the gate)
     int issued = 0, issued_v = 0, issued_t = 0;
     const int tc0 = bh * NT;  // this head's first chunk in the T tensor
     for (int n = 0; n < NT; ++n) {
@@ -339,13 +344,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         tma_load_4d(st + ST_Q1, &map_q, fb, 64, h, t_lo, b);
       }
       issued = n + 1;
-      float *sb = sm.beta(s), *sl = sm.lam(s);
-      sb[lane] = nb[0];
-      sb[lane + 32] = nb[1];
-      sl[lane] = nl[0];
-      sl[lane + 32] = nl[1];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(B_FULL + s));
       // V on its own barrier: its slot stages the outputs of the chunk NS
       // back, until the chain warps have written them out
       if (n >= NS && lane == 0) ok = wait_bar(sm, B_VEMPTY + s, ((n / NS) - 1) & 1, 0);
@@ -367,7 +365,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         tma_load_3d(sm.base + OFF_TR + (n & 1) * 8192, &map_t, tb, 0, 0, tc0 + n);
       }
       issued_t = n + 1;
-      fetch(n + 1);
     }
     // copies still in flight must land before the CTA's shared memory goes
     if (lane == 0) {
@@ -394,7 +391,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     //            product (VDONE, OFREE(n-1)), O^T += V~^T P^T behind the
     //            state update (SFULL)
     //   warp 15  the look-ahead: G(0); per chunk W(m) (TFULL, WREAD(m-1)),
-    //            G(m+1) (FULL, TFULL(m))
+    //            then G(m+1) (FULL, GFREE(m))
     // Each commits the barriers of its own products; every hand-off between
     // kinds is a barrier.
     if (lane == 0) {
@@ -437,11 +434,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           //      exp(gc_C) by the chain warps) ----
           if (!wait_bar(sm, B_VRDY, n & 1, 1)) break;
           tc_fence_after();
-          constexpr uint32_t tm_a = GATED ? TM_VBD : TM_VB;
+          // (gated: S~ += ((V~ diag dec) / sigma')^T K, the decay carried by
+          // the scale sigma of the accumulator)
+          const uint32_t vb = GATED ? TM_VBD : TM_VB;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_S, tmem + tm_a + k * 8, sdesc_sw128(st + ST_K0 + k * 2048, 16384, 1024), id_kd,
-                   true);
+            mma_ts(tmem + TM_S, tmem + vb + k * 8, sdesc_sw128(st + ST_K0 + k * 2048, 16384, 1024),
+                   id_kd, true);
           mma_commit(sm.bar(B_SFULL));
           mma_commit(sm.bar(B_EMPTY + s));
         }
@@ -460,13 +459,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mma_ts(tmem + TM_O, tmem + TM_SBF + k * 8, sdesc_sw128(qa, 0, 1024), id_o, k > 0);
           }
           mma_commit(sm.bar(B_SQDONE));
-          // ---- O^T += V~^T P^T, behind the state update ----
+          // ---- O^T += V~^T P^T, behind the state update (gated, ratio
+          //      regime: the dec-scaled copy of V~, P carrying 1 / dec) ----
           if (!wait_bar(sm, B_SFULL, n & 1, 1)) break;
+          if (GATED && !wait_bar(sm, B_PLAN + (n & 3), (n >> 2) & 1, 1)) break;
           tc_fence_after();
           const uint32_t pb = a_p + (n & 1) * 8192;
+          const uint32_t vsrc = (GATED && sm.plan(n)->ratio) ? TM_VBD : TM_VB;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_O, tmem + TM_VB + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_o, true);
+            mma_ts(tmem + TM_O, tmem + vsrc + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_o, true);
           mma_commit(sm.bar(B_OFULL));
           mma_commit(sm.bar(B_PFREE + (n & 1)));
           mma_commit(sm.bar(B_EMPTY + s));
@@ -475,8 +477,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         // ---- G = [K;Q] K^T of chunk m ----
         auto issue_g = [&](int m) -> bool {
           if (!wait_bar(sm, B_FULL + m % NS, (m / NS) & 1, 1)) return false;
-          // TM_G is free once the prep warps handed over chunk m-1
-          if (m >= 1 && !wait_bar(sm, B_TFULL, (m - 1) & 1, 1)) return false;
+          // TM_G is free once the P warps have read chunk m-1's G
+          if (m >= 1 && !wait_bar(sm, B_GFREE, (m - 1) & 1, 1)) return false;
           tc_fence_after();
           const uint32_t kq0 = smem_u32(sm.stage(m % NS));
 #pragma unroll
@@ -493,7 +495,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         bool ok = issue_g(0);
         for (int m = 0; ok && m < NT; ++m) {
           // ---- W^T = K^T (T diag exp gc)^T (ungated: T itself) ----
-          if (!wait_bar(sm, B_TFULL, m & 1, 1)) break;
+          if (!wait_bar(sm, B_TFULL + (m & 1), (m >> 1) & 1, 1)) break;
           if (m >= 1 && !wait_bar(sm, B_WREAD, (m - 1) & 1, 1)) break;
           tc_fence_after();
           const uint32_t kq = smem_u32(sm.stage(m % NS));
@@ -513,31 +515,43 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncwarp();
   } else if (warp < 6) {
     // ===================================================== prep warps
-    // per chunk m: P = Q K^T * Gam * M from rows 64..127 of G (warps 2, 3),
-    // T diag(exp gc) for the W product (warps 4, 5; gated), then Q exp(gc)
-    // in place over the Q tile (all four; gated), then TFULL (which also
-    // releases TM_G: every warp that reads G arrives on it after reading)
+    // per chunk m: P = Q K^T * Gam * M from rows 64..127 of G, then GFREE
+    // (warps 2, 3); T diag(exp gc) for the W product (warps 4, 5; gated);
+    // then TFULL
     const int q4 = warp & 3;              // TMEM lane quarter
     const int L = q4 * 32 + lane;         // TMEM lane of this thread
-    const int pt = tid - 64;              // 0..127 within the group
-    float *eg = sm.arr(SM_EG), *ieg = sm.arr(SM_IEG), *gcs = sm.arr(SM_GC);
+    float *eg = sm.arr(SM_EG), *gcs = sm.arr(SM_GC);
+    float ls = 0.f;  // P warps, gated: log2 sigma of the state before chunk m's update
+    // gated, warp 2: the linear gate at the extended steps lane and lane + 32
+    // of a chunk (1 where no token starts, and past the end), read one chunk
+    // ahead so that the loads are in flight while the chunk before is prepared
+    float gnx[2] = {1.f, 1.f};
+    auto gate_fetch = [&](int m) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int e = m * C + lane + 32 * k;
+        gnx[k] = (m < NT && e < p.L && (e % n_h) == 0) ? p.g[((size_t)b * p.T + e / n_h) * p.H + h] : 1.f;
+      }
+    };
+    if (GATED && warp == 2) gate_fetch(0);
     for (int m = 0; m < NT; ++m) {
-      const int s = m % NS;
       // every warp of the group is done with the previous chunk's gate
       // factors (they are rewritten below)
       if (named_sync_or(1, *sm.abort_flag() != 0)) break;
       // a failed wait sets the abort flag; every thread still reaches the
       // next named barrier and all of them leave together after it
-      wait_bar(sm, B_FULL + s, (m / NS) & 1, 2);
       if (GATED && warp == 2) {
+        float *lam = sm.lam();
+        lam[lane] = fmaxf(logf(gnx[0]), kLogGateFloor) * kLog2e;
+        lam[lane + 32] = fmaxf(logf(gnx[1]), kLogGateFloor) * kLog2e;
+        __syncwarp();
+        gate_fetch(m + 1);
         float lo, hi;
-        warp_scan64(sm.lam(s), lane, lo, hi);
+        warp_scan64(lam, lane, lo, hi);
         gcs[lane] = lo;
         gcs[lane + 32] = hi;
         eg[lane] = fast_exp2(lo);
         eg[lane + 32] = fast_exp2(hi);
-        ieg[lane] = fast_exp2(-lo);
-        ieg[lane + 32] = fast_exp2(-hi);
       }
       if (named_sync_or(1, *sm.abort_flag() != 0)) break;
       const Rows rw(m, n_h, p.T);
@@ -547,12 +561,49 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         // the range of the ratio form (uniform per chunk)
         const bool ratio = !GATED || gcs[63] >= kRatioFloor;
         if (m >= 2) wait_bar(sm, B_PFREE + (m & 1), ((m >> 1) - 1) & 1, 2);
+        float cp = 1.f;  // ratio regime: the uniform factor of P
+        if (GATED) {
+          // ---- the plan of chunk m's state update.  Both P warps track sigma
+          //      alike and take the same decisions; warp 2 publishes them with
+          //      dec = exp(gc_C - gc) / sigma' (the chain's factor of V~) and
+          //      the readout factor 2^gc of each readout row (0 past the last
+          //      one).  Slot m % 4 was last read for chunk m - 4, whose readers
+          //      all finished before the V~ P product of chunk m - 2 (waited for
+          //      just above) was issued ----
+          const float gl = gcs[63];
+          const float e = -(gl + ls);
+          float rs = 1.f;
+          if (e < kSigmaRange) {
+            ls = -e;
+          } else {
+            ls = 0.f;
+            rs = fast_exp2(-e);
+          }
+          // the V~ P product reads V~ diag(dec): P = Q K^T * M * 2^(ls' - gc_C)
+          // (the readout row's own 2^gc is applied to the output row)
+          cp = fast_exp2(ls - gl);
+          if (warp == 2) {
+            float *dec = sm.arr(SM_DEC + (m & 3) * 256), *qf = sm.arr(SM_QF + (m & 3) * 256);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int j = lane + 32 * hf;
+              dec[j] = fast_exp2(gl - gcs[j] - ls);
+              qf[j] = j < rw.Cp ? eg[rw.pos(j, n_h)] : 0.f;
+            }
+            if (lane == 0) {
+              volatile ChunkPlan *pl = sm.plan(m);
+              pl->rs = rs;
+              pl->sig = fast_exp2(ls);
+              pl->ratio = ratio ? 1 : 0;
+            }
+            arrive_warp(sm.bar(B_PLAN + (m & 3)), lane);
+          }
+        }
         wait_bar(sm, B_GFULL, m & 1, 2);
         tc_fence_after();
         const int r = L - 64;
         const int pos = r < rw.Cp ? rw.pos(r, n_h) : -1;
         const float gp = (GATED && pos >= 0) ? gcs[pos] : 0.f;
-        const float ep = (GATED && pos >= 0) ? eg[pos] : 1.f;
         uint8_t *prow = sm.base + OFF_P + (m & 1) * 8192;
 #pragma unroll 1
         for (int jb = 0; jb < 64; jb += 16) {
@@ -564,13 +615,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             for (int jj = 0; jj < 16; ++jj) cf[jj] = 1.f;
           } else if (ratio) {
 #pragma unroll
-            for (int jj = 0; jj < 16; jj += 4) {
-              const float4 e4 = *reinterpret_cast<const float4 *>(ieg + jb + jj);
-              cf[jj] = ep * e4.x;
-              cf[jj + 1] = ep * e4.y;
-              cf[jj + 2] = ep * e4.z;
-              cf[jj + 3] = ep * e4.w;
-            }
+            for (int jj = 0; jj < 16; ++jj) cf[jj] = cp;
           } else {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) cf[jj] = fast_exp2(gp - gcs[jb + jj]);
@@ -587,6 +632,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           st_chunk(prow + sw128_offset(r, jb, 64), {pk[0], pk[1], pk[2], pk[3]});
           st_chunk(prow + sw128_offset(r, jb + 8, 64), {pk[4], pk[5], pk[6], pk[7]});
         }
+        tc_fence_before();
+        arrive_warp(sm.bar(B_GFREE), lane);
       } else {
         // ---- the T tile of this chunk (UT pass) has landed; gated, T diag(exp gc)
         //      into its own buffer, free once the previous chunk's W product ended ----
@@ -618,39 +665,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           }
         }
       }
-      if (GATED) {
-        // ---- Q exp(gc) in place: readout row r scaled by exp(gc) at its
-        //      sub-step, rows past the chunk's readouts zeroed; the G product
-        //      (which read Q) has completed ----
-        if (warp >= 4) wait_bar(sm, B_GFULL, m & 1, 2);
-        uint8_t *qt = sm.stage(s);
-        uint4 v[8];
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int qi = pt + 128 * it;  // 16-byte piece: 512 per 64-column half
-          v[it] = *reinterpret_cast<const uint4 *>(qt + ((qi >> 9) ? ST_Q1 : ST_Q0) + (qi & 511) * 16);
-        }
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int qi = pt + 128 * it, row = (qi & 511) >> 3;
-          const float f = row < rw.Cp ? eg[rw.pos(row, n_h)] : 0.f;
-          const uint32_t in[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
-          uint32_t o4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            o4[u] = pack_bf16(__uint_as_float(in[u] << 16) * f, __uint_as_float(in[u] & 0xFFFF0000u) * f);
-          st_chunk(qt + ((qi >> 9) ? ST_Q1 : ST_Q0) + (qi & 511) * 16, o4);
-        }
-      }
-      // TFULL also hands TM_G back: the G product of the next chunk waits for it
-      tc_fence_before();
       fence_proxy_async_smem();
-      arrive_warp(sm.bar(B_TFULL), lane);
+      arrive_warp(sm.bar(B_TFULL + (m & 1)), lane);
     }
   } else if (warp < 10) {
     // ===================================================== feed-forward warps
-    // W^T(m) -> bf16 operand in shared memory, one chunk ahead; the outputs
-    // of chunk m -> global memory
+    // W^T(m) -> bf16 operand in shared memory and (gated) Q exp(gc) in place,
+    // one chunk ahead; the outputs of chunk m -> global memory
     const int q4 = warp & 3;
     const int L = q4 * 32 + lane;  // TMEM lane: a d index
     const int ft = tid - 192;      // 0..127 within the group
@@ -677,6 +698,39 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         st_chunk(ws + sw128_offset(L, 8 * q, 128), {pw_[4 * q], pw_[4 * q + 1], pw_[4 * q + 2], pw_[4 * q + 3]});
+      if (GATED) {
+        // ---- the readout factor exp(gc) at each readout row's sub-step
+        //      (published by the prep warps with the chunk's T diag(exp gc),
+        //      before TFULL).  Ratio regime (the chunk's decay stays above
+        //      2^-100; P' = Q K^T * 2^-gc_j): the output rows are scaled by
+        //      it at write-out.  Exact regime: Q exp(gc) in place (rows past
+        //      the readouts zeroed) and no output scaling.  The G product
+        //      (which read Q) completed before P and W; the output product
+        //      that reads Q waits for the S W product, which waits for WCVT ----
+        wait_bar(sm, B_TFULL + (m & 1), (m >> 1) & 1, 3);
+        if (!sm.plan(m)->ratio) {
+          wait_bar(sm, B_FULL + m % NS, (m / NS) & 1, 3);  // the Q tile landed
+          const float *qf = sm.arr(SM_QF + (m & 3) * 256);
+          uint8_t *qt = sm.stage(m % NS);
+          uint4 v[8];
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int qi = ft + 128 * it;  // 16-byte piece: 512 per 64-column half
+            v[it] = *reinterpret_cast<const uint4 *>(qt + ((qi >> 9) ? ST_Q1 : ST_Q0) + (qi & 511) * 16);
+          }
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int qi = ft + 128 * it;
+            const float f = qf[(qi & 511) >> 3];
+            const uint32_t in[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+            uint32_t o4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              o4[u] = pack_bf16(__uint_as_float(in[u] << 16) * f, __uint_as_float(in[u] & 0xFFFF0000u) * f);
+            st_chunk(qt + ((qi >> 9) ? ST_Q1 : ST_Q0) + (qi & 511) * 16, o4);
+          }
+        }
+      }
       fence_proxy_async_smem();
       arrive_warp(sm.bar(B_WCVT + (m & 1)), lane);
     };
@@ -699,6 +753,22 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       tc_fence_before();
       arrive_warp(sm.bar(B_OFREE), lane);
       {
+        if (GATED && sm.plan(n)->ratio) {
+          // ratio regime: every output row times its readout factor
+          const int tq = lane & 3;
+          const float *qf = sm.arr(SM_QF + (n & 3) * 256);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            // register 4 g + j holds output row (column of O^T) 8 g + 2 tq + j % 2
+            const float2 f = *reinterpret_cast<const float2 *>(qf + 8 * g + 2 * tq);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float fj = (j & 1) ? f.y : f.x;
+              o0[4 * g + j] = __float_as_uint(__uint_as_float(o0[4 * g + j]) * fj);
+              o1[4 * g + j] = __float_as_uint(__uint_as_float(o1[4 * g + j]) * fj);
+            }
+          }
+        }
         // staging row r (a readout row): 256 bytes, the 16-byte piece k
         // (values 8 k .. 8 k + 7) at (k ^ (r % 8)) * 16
         const uint32_t sv = smem_u32(sm.stage(n % NS) + ST_V0);
@@ -741,23 +811,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     }
   } else {
     // ===================================================== chain warps
-    // the recurrence: V~^T -> bf16 operand; the updated state S^T -> bf16
-    // operand and, gated, scaled in place by the next chunk's exp(gc_C); hT
+    // the recurrence: V~^T -> bf16 operand (gated: V~ diag dec); the updated
+    // state S^T -> bf16 operand (gated: sigma S~^T, and the rare rescale of
+    // TMEM the plan of the next chunk asks for); hT
     const int q4 = warp & 3;
     const int L = q4 * 32 + lane;  // TMEM lane = value column dv
-    // exp(gc_C) of chunk m: 2^(sum of its log2 gate)
-    auto gate_total = [&](int m) -> float {
-      const int s = m % NS;
-      wait_bar(sm, B_FULL + s, (m / NS) & 1, 4);
-      float t = sm.lam(s)[lane] + sm.lam(s)[lane + 32];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-      return fast_exp2(t);
-    };
-    // ---- initial state: S^T bf16 = h0^T, S^T fp32 = exp(gc_C) h0^T ----
+    // ---- initial state: S^T bf16 = h0^T, S~^T fp32 = h0^T (sigma = 1) ----
     {
       const float *h0 = p.h0 ? p.h0 + (size_t)bh * D * D : nullptr;
-      const float gc0 = GATED ? gate_total(0) : 1.f;
+      float r0 = 1.f;
+      if (GATED) {
+        wait_bar(sm, B_PLAN, 0, 4);
+        r0 = sm.plan(0)->rs;
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t f[32], pk[16];
@@ -765,8 +831,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         for (int u = 0; u < 32; u += 2) {
           const float x0 = h0 ? h0[(size_t)(c0 + u) * D + L] : 0.f;
           const float x1 = h0 ? h0[(size_t)(c0 + u + 1) * D + L] : 0.f;
-          f[u] = __float_as_uint(x0 * gc0);
-          f[u + 1] = __float_as_uint(x1 * gc0);
+          f[u] = __float_as_uint(x0 * r0);
+          f[u + 1] = __float_as_uint(x1 * r0);
           pk[u >> 1] = pack_bf16(x0, x1);
         }
         tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, c0), f);
@@ -776,39 +842,32 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       tc_fence_before();
       arrive_warp(sm.bar(B_SRDY), lane);
     }
-    float *dec = sm.arr(SM_DEC);
     for (int n = 0; n < NT; ++n) {
       if (named_sync_or(3, *sm.abort_flag() != 0)) break;
-      if (GATED) {
-        // exp(gc_C - gc) of chunk n (the factor of the state update's keys)
-        wait_bar(sm, B_FULL + n % NS, (n / NS) & 1, 4);
-        if (warp == 10) {
-          float lo, hi;
-          warp_scan64(sm.lam(n % NS), lane, lo, hi);
-          const float tot = __shfl_sync(0xffffffffu, hi, 31);
-          dec[lane] = fast_exp2(tot - lo);
-          dec[lane + 32] = fast_exp2(tot - hi);
-        }
-        named_sync(3);
-      }
-      // ---- V~^T -> bf16 operands: V~^T for the V~ P product and, gated,
-      //      (V~ diag exp(gc_C - gc))^T for the state update; the products of
-      //      the previous chunk read the old ones until the output group ended
-      //      (it is issued after the state update) ----
+      // ---- V~^T -> bf16 operands: gated, (V~ diag dec / sigma')^T for the
+      //      state update (and, in the ratio regime, for the V~ P product);
+      //      V~^T itself for the V~ P product otherwise.  The products of the
+      //      previous chunk read the old ones until the output group ended (it
+      //      is issued after the state update) ----
       wait_bar(sm, B_VDONE, n & 1, 4);
       tc_fence_after();
       if (n >= 1) {
         wait_bar(sm, B_OFULL, (n - 1) & 1, 4);
         tc_fence_after();
       }
+      // (the plan of chunk n was waited for at the previous chunk's end)
+      const bool plain = !GATED || !sm.plan(n)->ratio;
+      const float *dec = sm.arr(SM_DEC + (n & 3) * 256);
 #pragma unroll 1
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t r[32], pv[16];
         tmem_ld32(tmem_addr(tmem + TM_V, q4 * 32, 32 * hf), r);
         tmem_wait_ld_regs(r);
+        if (plain) {
 #pragma unroll
-        for (int u = 0; u < 16; ++u) pv[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-        tmem_st16(tmem_addr(tmem + TM_VB, q4 * 32, 16 * hf), pv);
+          for (int u = 0; u < 16; ++u) pv[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+          tmem_st16(tmem_addr(tmem + TM_VB, q4 * 32, 16 * hf), pv);
+        }
         if (GATED) {
 #pragma unroll
           for (int u = 0; u < 16; u += 2) {
@@ -822,13 +881,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       tmem_wait_st();
       tc_fence_before();
       arrive_warp(sm.bar(B_VRDY), lane);
-      // ---- the updated state: S^T -> bf16 operand for the next chunk (and,
-      //      gated, S^T <- exp(gc_C) S^T in place), or hT; the S W and
-      //      S (Q exp gc) products of this chunk read the old bf16 copy ----
+      // ---- the updated state: S^T -> bf16 operand for the next chunk (gated:
+      //      sigma S~^T, and the rescale of the next chunk's plan), or hT; the
+      //      S W and S (Q) products of this chunk read the old bf16 copy ----
       wait_bar(sm, B_SFULL, n & 1, 4);
       tc_fence_after();
+      const float sig = GATED ? sm.plan(n)->sig : 1.f;  // sigma of S~ in TMEM now
       if (n + 1 < NT) {
-        const float gcn = GATED ? gate_total(n + 1) : 1.f;
+        float rs = 1.f;
+        if (GATED) {
+          wait_bar(sm, B_PLAN + ((n + 1) & 3), ((n + 1) >> 2) & 1, 4);
+          rs = sm.plan(n + 1)->rs;
+        }
         wait_bar(sm, B_SQDONE, n & 1, 4);
         tc_fence_after();
 #pragma unroll 1
@@ -838,11 +902,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, 64 * hf + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
           tmem_wait_ld_regs(r);
 #pragma unroll
-          for (int u = 0; u < 32; ++u) pk[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+          for (int u = 0; u < 32; ++u)
+            pk[u] = pack_bf16(__uint_as_float(r[2 * u]) * sig, __uint_as_float(r[2 * u + 1]) * sig);
           tmem_st32(tmem_addr(tmem + TM_SBF, q4 * 32, 32 * hf), pk);
-          if (GATED) {
+          if (GATED && rs != 1.f) {
+            // the next chunk's sigma' would fall below 2^-64: TMEM <-
+            // exp(gc_C) S, with sigma' = 1
 #pragma unroll
-            for (int u = 0; u < 64; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * gcn);
+            for (int u = 0; u < 64; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * rs);
             tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, 64 * hf), *reinterpret_cast<uint32_t (*)[32]>(&r[0]));
             tmem_st32(tmem_addr(tmem + TM_S, q4 * 32, 64 * hf + 32), *reinterpret_cast<uint32_t (*)[32]>(&r[32]));
           }
@@ -858,7 +925,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           tmem_ld32(tmem_addr(tmem + TM_S, q4 * 32, c0), r);
           tmem_wait_ld_regs(r);
 #pragma unroll
-          for (int u = 0; u < 32; ++u) hT[(size_t)(c0 + u) * D + L] = __uint_as_float(r[u]);
+          for (int u = 0; u < 32; ++u) hT[(size_t)(c0 + u) * D + L] = __uint_as_float(r[u]) * sig;
         }
       }
     }
