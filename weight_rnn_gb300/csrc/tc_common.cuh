@@ -68,13 +68,5 @@ __device__ __forceinline__ void warp_scan64(const float *lam, int lane, float &l
   hi += __shfl_sync(0xffffffffu, lo, 31);
 }
 
-// The log2 gate entry of extended step e (0 unless e is a token's first
-// sub-step), from the linear gate g [B, T, H].
-__device__ __forceinline__ float log2_gate(const float *g, int e, int n_h, int T, int H, int b,
-                                           int h) {
-  if ((e % n_h) != 0) return 0.f;
-  return fmaxf(logf(g[((size_t)b * T + e / n_h) * H + h]), kLogGateFloor) * kLog2e;
-}
-
 }  // namespace tc
 }  // namespace delta

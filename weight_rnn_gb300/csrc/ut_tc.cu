@@ -433,6 +433,30 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
 
   if (warp == 8) {
     // ===================================================== TMA producer
+    // beta and the linear gate of a pair's two chunks are read into registers
+    // one pair ahead (lanes: steps lane and lane + 32 of each chunk), so that
+    // the loads are in flight while the producer waits for a free slot
+    float pb[4], pg[4];
+    auto fetch = [&](int i) {
+      const long long pr = pair_of(i);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const long long c = 2 * pr + x;
+        const bool live = i < mine && c < p.total;
+        const int bh = live ? (int)(c / p.nchunks) : 0, n = live ? (int)(c % p.nchunks) : 0;
+        const int b = bh / p.H, h = bh % p.H;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int e = n * C + lane + 32 * k;
+          const bool in = live && e < p.L;
+          pb[2 * x + k] = in ? __ldg(p.beta + ((size_t)b * p.L + e) * p.H + h) : 0.f;
+          pg[2 * x + k] = (GATED && in && (e % p.n_h) == 0)
+                              ? __ldg(p.g + ((size_t)b * p.T + e / p.n_h) * p.H + h)
+                              : 1.f;
+        }
+      }
+    };
+    fetch(0);
     int issued = 0;
     for (int i = 0; i < mine; ++i) {
       const int s = i & 1;
@@ -443,22 +467,15 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
       uint32_t bytes = 0;
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
-        const long long c = 2 * pr + x;
         float *sb = sm.arr(SM_BETA + (s * 2 + x) * 256), *sl = sm.arr(SM_LAM + (s * 2 + x) * 256);
-        if (c < p.total) {
-          const int bh = (int)(c / p.nchunks), n = (int)(c % p.nchunks);
-          const int b = bh / p.H, h = bh % p.H, e0 = n * C;
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int e = e0 + lane + 32 * k;
-            sb[lane + 32 * k] = e < p.L ? p.beta[((size_t)b * p.L + e) * p.H + h] : 0.f;
-            sl[lane + 32 * k] = (GATED && e < p.L) ? log2_gate(p.g, e, p.n_h, p.T, p.H, b, h) : 0.f;
-          }
-          bytes += 16384u;
-        } else {
-          sb[lane] = sb[lane + 32] = 0.f;
-          sl[lane] = sl[lane + 32] = 0.f;
+        for (int k = 0; k < 2; ++k) {
+          sb[lane + 32 * k] = pb[2 * x + k];
+          // the log2 gate (log g at each token's first sub-step, clamped so
+          // that g = 0 stays finite; 0 elsewhere and past the end)
+          sl[lane + 32 * k] = GATED ? fmaxf(logf(pg[2 * x + k]), kLogGateFloor) * kLog2e : 0.f;
         }
+        if (2 * pr + x < p.total) bytes += 16384u;
       }
       __syncwarp();
       if (lane == 0) {
@@ -477,6 +494,7 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
         }
       }
       issued = i + 1;
+      fetch(i + 1);
     }
     // copies still in flight must land before the CTA's shared memory goes
     if (lane == 0)
