@@ -104,6 +104,33 @@ int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
               delta_dtype dtype, struct CUstream_st *stream);
 
 /*
+ * delta_fwd_static_scratch -- delta_fwd for callers that cannot allocate
+ * device memory.  The pages have no counterpart: it is delta_fwd's
+ * tensor-core path with its scratch (the T tiles handed from the UT pass to
+ * the state pass) in a static device array of the library instead of the
+ * memory pool.  Arguments, layouts and results as in delta_fwd.
+ *
+ *   - Allocates nothing.  The array holds 32 MiB: the T tiles of at most
+ *     4096 chunks, i.e. B*H*ceil(n_h*T/64) <= 4096 (e.g. B=1, H=32,
+ *     T=8192).  Larger problems return DELTA_ERR_UNSUPPORTED, with the
+ *     sizes in delta_last_error(), before anything is enqueued.
+ *   - Only DELTA_BF16 with dk = dv = 128 and chunk = 64 (DELTA_ERR_UNSUPPORTED
+ *     otherwise); T = 0 copies h0 to hT as delta_fwd does.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current) and keeps it; make that first call before
+ *     any stream capture.
+ *   - Nothing in the array needs clearing: each call writes every tile it
+ *     reads.
+ *   - There is one array per device: calls that overlap in time on the same
+ *     device (on any streams, from any threads) race on it and give wrong
+ *     results.  Callers serialise them, e.g. on one stream.
+ */
+int delta_fwd_static_scratch(const void *q, const void *k, const void *v, const float *beta,
+                             const float *g, const float *h0, void *out, float *hT,
+                             int B, int H, int T, int dk, int dv, int n_h, int chunk,
+                             delta_dtype dtype, struct CUstream_st *stream);
+
+/*
  * delta_ut_transform -- the intra-chunk pass of delta_fwd on its own: the UT
  * transform of "08 · linear 路线（三）" §2.2 with the gated decay of §3, for
  * every chunk n of 64 steps of the extended sequence (length L = n_h*T,

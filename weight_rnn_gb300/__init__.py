@@ -15,7 +15,7 @@ import threading
 
 import torch
 
-__all__ = ["delta_fwd", "delta_ut_transform", "delta_fwd_with_ut", "delta_step",
+__all__ = ["delta_fwd", "delta_fwd_static_scratch", "delta_ut_transform", "delta_fwd_with_ut", "delta_step",
            "fwd_launches", "delta_status_string", "delta_last_error",
            "delta_check_device", "delta_inject_failure", "delta_selftest_wait",
            "delta_version", "DeltaError", "library_path", "load_library",
@@ -32,7 +32,8 @@ DELTA_F32 = 0
 DELTA_BF16 = 1
 
 #: every extern "C" entry point include/delta.h declares
-EXPORTED_SYMBOLS = ("delta_fwd", "delta_ut_transform", "delta_fwd_with_ut",
+EXPORTED_SYMBOLS = ("delta_fwd", "delta_fwd_static_scratch", "delta_ut_transform",
+                    "delta_fwd_with_ut",
                     "delta_fwd_kernel_count", "delta_step", "delta_status_string",
                     "delta_last_error", "delta_check_device", "delta_version",
                     "delta_inject_failure", "delta_selftest_wait")
@@ -69,6 +70,8 @@ def load_library():
         p, i = ctypes.c_void_p, ctypes.c_int
         lib.delta_fwd.restype = i
         lib.delta_fwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.delta_fwd_static_scratch.restype = i
+        lib.delta_fwd_static_scratch.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
         lib.delta_ut_transform.restype = i
         lib.delta_ut_transform.argtypes = [p, p, p, p, i, i, i, i, i, i, i, p]
         lib.delta_fwd_with_ut.restype = i
@@ -202,6 +205,41 @@ def delta_fwd(q, k, v, beta, g=None, h0=None, out=None, hT=None, *, n_h=1,
     st = lib.delta_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
                        _ptr(out), _ptr(hT), B, H, T, dk, dv, n_h, chunk, code,
                        _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return out, hT
+
+
+def delta_fwd_static_scratch(q, k, v, beta, g=None, h0=None, out=None, hT=None, *, n_h=1,
+                             chunk=64, want_state=True, stream=None):
+    """``delta_fwd`` that allocates no device memory: its scratch is a static
+    array of the library (at most B*H*ceil(n_h*T/64) = 4096 chunks; bf16 with
+    dk = dv = 128 and chunk = 64 only).  Calls that overlap in time on one
+    device race on that array.  Arguments and results as in ``delta_fwd``."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("delta_fwd_static_scratch needs CUDA tensors")
+    dt = q.dtype
+    code = _dtype_code(dt)
+    dv = v.shape[-1]
+    kshape, vshape, bshape = _kvb_shapes(k, v, beta, B, T, H, dk, n_h)
+    _check(q, "q", (B, T, H, dk), dt, dev)
+    _check(k, "k", kshape, dt, dev)
+    _check(v, "v", vshape, dt, dev)
+    _check(beta, "beta", bshape, torch.float32, dev)
+    _check(g, "g", (B, T, H), torch.float32, dev)
+    _check(h0, "h0", (B, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=dt, device=dev)
+    _check(out, "out", (B, T, H, dv), dt, dev)
+    if hT is None and want_state:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(hT, "hT", (B, H, dk, dv), torch.float32, dev)
+    st = lib.delta_fwd_static_scratch(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                      _ptr(h0), _ptr(out), _ptr(hT), B, H, T, dk, dv, n_h,
+                                      chunk, code, _stream(dev, stream))
     if st != DELTA_OK:
         raise DeltaError(st, delta_last_error())
     return out, hT

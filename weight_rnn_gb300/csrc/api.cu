@@ -14,6 +14,13 @@
 #include "../../include/delta.h"
 #include "kernels.h"
 
+// Scratch of delta_fwd_static_scratch: the T tiles of at most 4096 chunks
+// (8 KiB each), in a file-scope device array, so that the call allocates
+// nothing.  Every tile the state pass reads is written by the same call's UT
+// pass first, so nothing in it has to start at zero.
+constexpr int64_t kStaticScratchBytes = int64_t(32) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
 namespace {
 
 thread_local char g_last_error[256] = "no error";
@@ -88,6 +95,26 @@ cudaError_t scratch_pool(cudaMemPool_t *out) {
     g_pool[dev] = pool;
   }
   *out = g_pool[dev];
+  return cudaSuccess;
+}
+
+// Device address of g_static_scratch on the current device, looked up (with
+// that device current) the first time each device asks.
+std::mutex g_static_mu;
+void *g_static_addr[kMaxDevices] = {};
+
+cudaError_t static_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void *p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_static_scratch)) != cudaSuccess) return e;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
   return cudaSuccess;
 }
 
@@ -240,6 +267,36 @@ int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
   }
   err = delta::launch_chunk_generic(a, s);
   return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "generic chunk kernel launch");
+}
+
+int delta_fwd_static_scratch(const void *q, const void *k, const void *v, const float *beta,
+                             const float *g, const float *h0, void *out, float *hT, int B,
+                             int H, int T, int dk, int dv, int n_h, int chunk,
+                             delta_dtype dtype, struct CUstream_st *stream) {
+  delta::FwdArgs a;
+  const int st = validate_fwd(q, k, v, beta, g, h0, out, hT, B, H, T, dk, dv, n_h, chunk, dtype, a);
+  if (st != DELTA_OK || a.B * a.H == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (T == 0) {
+    err = delta::launch_state_passthrough(a, s);
+    return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "state passthrough launch");
+  }
+  if (!delta::chunk_tc_supports(a))
+    return fail(DELTA_ERR_UNSUPPORTED,
+                "the static-scratch forward runs for bf16 with dk = dv = 128 and chunk = 64 only");
+  const int64_t need = delta::ut_workspace_bytes(a);
+  if (need > kStaticScratchBytes)
+    return fail(DELTA_ERR_UNSUPPORTED,
+                "the T tiles of B*H*ceil(n_h*T/64) = %lld chunks need %lld bytes; the static "
+                "scratch holds %lld bytes (4096 chunks)",
+                (long long)(need / 8192), (long long)need, (long long)kStaticScratchBytes);
+  void *t_mat = nullptr;
+  if ((err = static_scratch(&t_mat)) != cudaSuccess) return cuda_fail(err, "static scratch address");
+  err = delta::launch_ut(a, t_mat, s);
+  if (err != cudaSuccess) return cuda_fail(err, "UT-pass kernel launch");
+  err = delta::launch_chunk_tc(a, t_mat, s);
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "tensor-core chunk kernel launch");
 }
 
 int delta_ut_transform(const void *k, const float *beta, const float *g, void *t_mat, int B,
