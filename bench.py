@@ -63,6 +63,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "fwd": ["weight_rnn_gb300/csrc/chunk_tc.cu", "weight_rnn_gb300/csrc/ut_tc.cu"],
     "ut": ["weight_rnn_gb300/csrc/ut_tc.cu"],
+    "state": ["weight_rnn_gb300/csrc/chunk_tc.cu"],
     "step": ["weight_rnn_gb300/csrc/step.cu"],
 }
 
@@ -442,7 +443,7 @@ def measure(w, wr, dist, dev, args, peaks, peak_src, clocks_on):
                         "traffic": read_traffic("ut", w.name)},
             "state_pass": {"kernel": "chunk_tc_kernel", "us": st_s * 1e6,
                            "share": st_s / (ut_s + st_s), "bytes_moved": st_bytes,
-                           "gbs": st_bytes / st_s / 1e9, "traffic": read_traffic(kind, w.name)},
+                           "gbs": st_bytes / st_s / 1e9, "traffic": read_traffic("state", w.name)},
             "extra_bytes_vs_algorithmic": ut_bytes + t_bytes,
         }
         del t_mat
