@@ -181,6 +181,10 @@ int delta_fwd_with_ut(const void *q, const void *k, const void *v, const float *
  *   g     [B, H]              float32 linear gate, or NULL (=> 1)
  *   state [B, H, dk, dv]      float32, in/out
  *   out   [B, H, dv]          dtype
+ *
+ * The kernel runs one block per (b, h) and 32-column slab of the state, so
+ * B*H*max(1, dv/32) must stay below 2^31; larger sizes return
+ * DELTA_ERR_UNSUPPORTED.
  */
 int delta_step(const void *q, const void *k, const void *v, const float *beta,
                const float *g, float *state, void *out,
