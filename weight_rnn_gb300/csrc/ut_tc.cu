@@ -231,140 +231,48 @@ __device__ __forceinline__ void warp_store_16x8(float *M, int r0, int n0, const 
 }
 
 // One warp inverts the unit lower-triangular 16x16 diagonal block at offset
-// o of (I + A): closed-form 4x4 leaves, then the merges 4 -> 8 -> 16, each
-// X21 = -X22 (A21 X11).  Every entry of A the warp needs is loaded at once;
-// the partial inverses move between lanes by shuffles, not through shared
-// memory.  X goes to the lower triangle of the solve array and, scaled by
-// beta of its column, to the T tile.
+// o of (I + A) by column-oriented forward substitution: lane j (and lane
+// j + 16, which repeats it) carries column j of X = (I + A_oo)^{-1} in
+// registers, starting from e_j.  At step k its entry k is final; it is x_kj,
+// and every row i > k takes -A_ik x_kj.  Column k of A sits in row o + k of
+// the solve array's upper triangle (A_ik at (k, i)), read as float4 groups
+// that every lane shares.  The dependent chain is one multiply-add per step.
+// X goes to the lower triangle of the solve array and, scaled by beta of its
+// column, to the T tile.
 __device__ __forceinline__ void invert_diag16(float *AX, uint8_t *tu, const float *beta, int o,
                                               int lane) {
-  const unsigned full = 0xffffffffu;
-  // leaf lanes (0..11): leaf a, column cc;  merge-1 lanes: (hh, r4, c4);
-  // merge-2 lanes: (r8, c0 and c0 + 4)
-  const int a = lane < 12 ? lane / 3 : 0, cc = lane < 12 ? lane - 3 * (lane / 3) : 0;
-  const int b0 = o + 4 * a;
-  const int hh = lane >> 4, r4 = (lane >> 2) & 3, c4 = lane & 3, o8 = o + 8 * hh;
-  const int r8 = lane >> 2, c0 = lane & 3;
-  const float a10 = ldA(AX, b0 + 1, b0), a20 = ldA(AX, b0 + 2, b0), a21 = ldA(AX, b0 + 2, b0 + 1);
-  const float a30 = ldA(AX, b0 + 3, b0), a31 = ldA(AX, b0 + 3, b0 + 1), a32 = ldA(AX, b0 + 3, b0 + 2);
-  float am1[4], am2[8];
+  const int j = lane & 15;
+  float x[16];
 #pragma unroll
-  for (int m = 0; m < 4; ++m) am1[m] = ldA(AX, o8 + 4 + r4, o8 + m);
+  for (int i = 0; i < 16; ++i) x[i] = i == j ? 1.f : 0.f;
 #pragma unroll
-  for (int m = 0; m < 8; ++m) am2[m] = ldA(AX, o + 8 + r8, o + m);
-
-  // ---- leaves: column cc of leaf a by forward substitution ----
-  const float x0 = cc == 0 ? 1.f : 0.f;
-  const float x1 = cc == 1 ? 1.f : (cc < 1 ? -(a10 * x0) : 0.f);
-  const float x2 = cc == 2 ? 1.f : (cc < 2 ? -fmaf(a21, x1, a20 * x0) : 0.f);
-  const float x3 = -fmaf(a32, x2, fmaf(a31, x1, a30 * x0));
-  if (lane < 12) {
-    const int col = b0 + cc;
-    const float bc = beta[col];
-    if (cc < 1) {
-      AX[swz(b0 + 1, col)] = x1;
-      put_t(tu, b0 + 1, col, x1, bc);
+  for (int k = 0; k < 15; ++k) {
+    // A_{o+i, o+k} for i = 0..15 from row o + k (the 128-bit groups keep
+    // their 4 columns together under the row swizzle)
+    const float *row = AX + (o + k) * 64;
+    float a[16];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (4 * g + 3 <= k) continue;  // every column of the group is at or left of the diagonal
+      const float4 v = *reinterpret_cast<const float4 *>(row + ((o + 4 * g) ^ (((o + k) & 7) << 2)));
+      a[4 * g] = v.x;
+      a[4 * g + 1] = v.y;
+      a[4 * g + 2] = v.z;
+      a[4 * g + 3] = v.w;
     }
-    if (cc < 2) {
-      AX[swz(b0 + 2, col)] = x2;
-      put_t(tu, b0 + 2, col, x2, bc);
-    }
-    AX[swz(b0 + 3, col)] = x3;
-    put_t(tu, b0 + 3, col, x3, bc);
+    const float xk = x[k];
+#pragma unroll
+    for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-a[i], xk, x[i]);
   }
-  if (lane < 16) put_t(tu, o + lane, o + lane, 1.f, beta[o + lane]);
-
-  // ---- 4 -> 8: X[o8+4+r4][o8+c4] ----
-  float xm1;
-  {
-    // X11 = leaf 2 hh, column c4 (lane 6 hh + c4); X11[m][c4] for m > c4
-    const int s11 = 6 * hh + c4;
-    const float u1 = __shfl_sync(full, x1, s11), u2 = __shfl_sync(full, x2, s11),
-                u3 = __shfl_sync(full, x3, s11);
-    const float xc[4] = {c4 == 0 ? 1.f : 0.f, c4 == 1 ? 1.f : (c4 < 1 ? u1 : 0.f),
-                         c4 == 2 ? 1.f : (c4 < 2 ? u2 : 0.f), c4 == 3 ? 1.f : u3};
-    float y = 0.f;
+  if (lane < 16) {
+    const float bj = beta[o + j];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) y = fmaf(am1[m], xc[m], y);
-    // Y[m][c4] from lane (hh, m, c4); X22[r4][m] = leaf 2 hh + 1, column m, row r4
-    float z = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const float ym = __shfl_sync(full, y, (lane & 16) | (m << 2) | c4);
-      float xr = 1.f;
-      if (m < 3) {
-        const int s22 = 6 * hh + 3 + m;
-        const float w1 = __shfl_sync(full, x1, s22), w2 = __shfl_sync(full, x2, s22),
-                    w3 = __shfl_sync(full, x3, s22);
-        xr = r4 == 1 ? w1 : (r4 == 2 ? w2 : w3);
-      }
-      if (m < r4) z = fmaf(xr, ym, z);
-      if (m == r4) z += ym;
+    for (int i = 0; i < 16; ++i) {
+      if (i > j) AX[swz(o + i, o + j)] = x[i];
+      if (i >= j) put_t(tu, o + i, o + j, x[i], bj);
     }
-    xm1 = -z;
-    AX[swz(o8 + 4 + r4, o8 + c4)] = xm1;
-    put_t(tu, o8 + 4 + r4, o8 + c4, xm1, beta[o8 + c4]);
-  }
-
-  // ---- 8 -> 16: X[o+8+r8][o+c0] and X[o+8+r8][o+c0+4] ----
-  {
-    // column c0 of X11 = X[o..o+8][o..o+8]: rows < 4 from leaf 0 (lane c0),
-    // rows >= 4 from the 4 -> 8 merge (lane (0, m-4, c0))
-    const float u1 = __shfl_sync(full, x1, c0), u2 = __shfl_sync(full, x2, c0),
-                u3 = __shfl_sync(full, x3, c0);
-    // column c0 + 4: rows >= 4 from leaf 1 (lane 3 + c0)
-    const float v1 = __shfl_sync(full, x1, 3 + c0), v2 = __shfl_sync(full, x2, 3 + c0),
-                v3 = __shfl_sync(full, x3, 3 + c0);
-    float y0 = 0.f, y1 = 0.f;
-    const float lo[4] = {c0 == 0 ? 1.f : 0.f, c0 == 1 ? 1.f : (c0 < 1 ? u1 : 0.f),
-                         c0 == 2 ? 1.f : (c0 < 2 ? u2 : 0.f), c0 == 3 ? 1.f : u3};
-    const float hi[4] = {c0 == 0 ? 1.f : 0.f, c0 == 1 ? 1.f : (c0 < 1 ? v1 : 0.f),
-                         c0 == 2 ? 1.f : (c0 < 2 ? v2 : 0.f), c0 == 3 ? 1.f : v3};
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      y0 = fmaf(am2[m], lo[m], y0);
-      const float wm = __shfl_sync(full, xm1, (m << 2) | c0);
-      y0 = fmaf(am2[m + 4], wm, y0);
-      y1 = fmaf(am2[m + 4], hi[m], y1);
-    }
-    // X22 = X[o+8..o+16][o+8..o+16]: rows < 4 from leaf 2, rows >= 4 from
-    // leaf 3 (same columns) or, for columns < 4, from the 4 -> 8 merge (hh 1)
-    float z0 = 0.f, z1 = 0.f;
-    const int rr = r8 & 3;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float ya = __shfl_sync(full, y0, (m << 2) | c0);
-      const float yb = __shfl_sync(full, y1, (m << 2) | c0);
-      float xr;
-      if ((m & 3) < 3) {
-        // leaf 2 (r8 < 4) or leaf 3 (r8 >= 4), column m & 3, row r8 & 3
-        const int sl = (r8 < 4 ? 6 : 9) + (m & 3);
-        const float w1 = __shfl_sync(full, x1, sl), w2 = __shfl_sync(full, x2, sl),
-                    w3 = __shfl_sync(full, x3, sl);
-        xr = rr == 1 ? w1 : (rr == 2 ? w2 : w3);
-      } else {
-        xr = 0.f;
-      }
-      if (m < 4) {
-        const float xq = __shfl_sync(full, xm1, 16 | ((r8 & 3) << 2) | m);
-        if (r8 >= 4) xr = xq;
-      }
-      if (m < r8) {
-        z0 = fmaf(xr, ya, z0);
-        z1 = fmaf(xr, yb, z1);
-      }
-      if (m == r8) {
-        z0 += ya;
-        z1 += yb;
-      }
-    }
-    AX[swz(o + 8 + r8, o + c0)] = -z0;
-    AX[swz(o + 8 + r8, o + c0 + 4)] = -z1;
-    put_t(tu, o + 8 + r8, o + c0, -z0, beta[o + c0]);
-    put_t(tu, o + 8 + r8, o + c0 + 4, -z1, beta[o + c0 + 4]);
   }
 }
-
 
 // Named barrier of solve group gi (ids 1 and 2, immediate operands, so that
 // the kernel reserves only the barriers it uses).
