@@ -236,6 +236,37 @@ def parallel_form(q, k, v, beta):
     return Amap @ v
 
 
+def attention_map(q, k, beta, log_g=None):
+    """[DR] §2.4, the fully parallel form, with the gated decay of §3: for a
+    sequence of L steps processed as one block (zero initial state), the
+    L x L matrix A with o_i = sum_j A_ij v_j,
+        A = (Q K^T * Gam * M) T,   T = (I + strictLower(diag(beta) (Gam * K K^T)))^{-1} diag(beta)
+    with Gam_ij = exp(gc_i - gc_j) (gc the inclusive cumulative log gate) and
+    M the causal mask including the diagonal.  q, k [L, dk]; beta [L];
+    log_g [L] or None.  Returns A [L, L] (float64)."""
+    L = k.shape[0]
+    if log_g is None:
+        log_g = np.zeros(L)
+    Tm = ut_transform(np.asarray(k, float), beta, log_g, C=L)[0]
+    gc = np.cumsum(np.asarray(log_g, float))
+    incl = np.tril(np.ones((L, L), dtype=bool))
+    Gam = np.exp(np.where(incl, gc[:, None] - gc[None, :], -np.inf))  # mask before exp
+    return ((np.asarray(q, float) @ np.asarray(k, float).T) * Gam) @ Tm
+
+
+def effective_rank(Hm):
+    """[DP] §4.6, the effective rank of a matrix state: with sigma_k its
+    singular values and p_k = sigma_k / sum_j sigma_j,
+        erank(H) = exp(-sum_k p_k log p_k)     (0 log 0 = 0).
+    The definition does not apply to H = 0; that case returns 0."""
+    sv = np.linalg.svd(np.asarray(Hm, dtype=np.float64), compute_uv=False)
+    tot = sv.sum()
+    if tot == 0.0:
+        return 0.0
+    p = sv[sv > 0] / tot
+    return float(np.exp(-np.sum(p * np.log(p))))
+
+
 def dplr(q, w, a, b, kk, vv, S0=None):
     """[DR] §5 DPLR loop: S_t = (Diag(w_t) + a_t b_t^T) S_{t-1} + kk_t vv_t^T,
     o_t = S_t^T q_t.  b_t^T acts on the UNdecayed previous state."""

@@ -200,3 +200,57 @@ def test_ut_transform_special_cases():
     T = forms.ut_transform(k, np.ones(C), lg, C)[0]
     assert not T[5:, :5].any()
     assert np.allclose(T[:5, :5], forms.ut_transform(k[:5], np.ones(5), None, 5)[0])
+
+
+# --- diagnostics on the outputs: the attention map and the effective rank ---
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("L", [1, 9, 64])
+def test_attention_map_reproduces_the_recurrence(gated, L):
+    # [DR] §2.4: o_i = sum_j A_ij v_j for a zero initial state -- pinned to
+    # the token-by-token C oracle
+    rng = np.random.default_rng(40 + L)
+    q, k, v, beta, g, _ = head_inputs(rng, L, 8, 5, gated, beta_hi=2.0)
+    o, _ = run_oracle(q, k, v, beta, g, None)
+    A = forms.attention_map(q, k, beta, None if g is None else np.log(g.astype(np.float64)))
+    assert rel_l2(A @ v, o) < TOL
+
+
+def test_attention_map_structure():
+    # causal (zero above the diagonal); A_ii = beta_i (q_i . k_i) because T is
+    # lower triangular with T_ii = beta_i; ungated it is the map of the
+    # fully parallel form
+    rng = np.random.default_rng(43)
+    q, k, v, beta, g, _ = head_inputs(rng, 20, 6, 4, True)
+    A = forms.attention_map(q, k, beta, np.log(g.astype(np.float64)))
+    assert np.all(np.triu(A, 1) == 0.0)
+    qk = np.einsum("id,id->i", q.astype(np.float64), k.astype(np.float64))
+    assert np.allclose(np.diag(A), beta * qk, rtol=1e-12, atol=1e-14)
+    A0 = forms.attention_map(q, k, beta)
+    assert rel_l2(A0 @ v, forms.parallel_form(q, k, v, beta)) < TOL
+
+
+def test_effective_rank_closed_forms():
+    # [DP] §4.6: erank = exp(entropy of sigma / sum sigma)
+    er = forms.effective_rank
+    assert abs(er(np.eye(7)) - 7.0) < 1e-12                       # 7 equal singular values
+    rng = np.random.default_rng(44)
+    a, b = rng.standard_normal(6), rng.standard_normal(9)
+    assert abs(er(np.outer(a, b)) - 1.0) < 1e-12                  # rank one
+    sv = np.array([1.0, 1.0, 2.0])                                # p = 1/4, 1/4, 1/2
+    want = np.exp(-(0.5 * np.log(0.25) + 0.5 * np.log(0.5)))      # = 2^(3/2)
+    assert abs(want - 2.0 ** 1.5) < 1e-12
+    assert abs(er(np.diag(sv)) - want) < 1e-12
+    # invariant under orthogonal maps on either side and under scaling
+    U, _ = np.linalg.qr(rng.standard_normal((3, 3)))
+    V, _ = np.linalg.qr(rng.standard_normal((3, 3)))
+    assert abs(er(-3.5 * U @ np.diag(sv) @ V.T) - want) < 1e-12
+    assert er(np.zeros((4, 5))) == 0.0                            # the definition does not apply
+
+
+def test_effective_rank_bounds():
+    # 1 <= erank <= rank for nonzero matrices
+    rng = np.random.default_rng(45)
+    for r in (1, 2, 5, 8):
+        M = rng.standard_normal((8, r)) @ rng.standard_normal((r, 10))
+        e = forms.effective_rank(M)
+        assert 1.0 - 1e-12 <= e <= r + 1e-9
