@@ -534,6 +534,41 @@ def measure(w, wr, dist, dev, args, peaks, peak_src, clocks_on):
     return rec, host
 
 
+def measure_diagnostics(wr, dev, args):
+    """The two diagnostics on the outputs, timed with CUDA events: the
+    effective rank of the headline workload's B*H states (128 x 128 float32,
+    seeded normal entries) and the attention map of 64-step blocks (B32 H32,
+    dk = 128, bf16, gated)."""
+    stream = torch.cuda.current_stream(dev)
+    w = synth.WORKLOADS[HEADLINE]
+    gen = torch.Generator().manual_seed(w.seed + 7)
+    states = torch.randn((w.B, w.H, w.dk, w.dv), generator=gen).to(dev)
+    mw = synth.WORKLOADS[HEADLINE].with_(name="attention_map_b32_h32_n64_d128_bf16", B=32, H=32, T=64)
+    mi = synth.fwd_inputs(mw)
+    q, k = mi["q"].to(dev), mi["k"].reshape(mw.B, mw.T, mw.H, mw.dk).to(dev)
+    beta, g = mi["beta"].reshape(mw.B, mw.T, mw.H).to(dev), mi["g"].to(dev)
+    out = {}
+    for name, fn, units, unit in (
+            ("effective_rank", lambda: wr.delta_state_erank(states), w.B * w.H, "matrices/s"),
+            ("attention_map", lambda: wr.delta_attention_map(q, k, beta, g), mw.B * mw.H, "maps/s")):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+        out[name] = {"us_per_call": us, "value": units / (us * 1e-6), "unit": unit,
+                     "units_per_call": units}
+    out["effective_rank"]["input"] = f"{w.B}x{w.H} states {w.dk}x{w.dv} float32"
+    out["attention_map"]["input"] = f"B{mw.B} H{mw.H} N{mw.T} dk{mw.dk} bf16, gated"
+    return out
+
+
 def run_ours(args, dist):
     import weight_rnn_gb300 as wr
 
@@ -557,6 +592,7 @@ def run_ours(args, dist):
         torch.cuda.empty_cache()
     head_id = ids[0]
     head = recs[head_id]
+    diagnostics = measure_diagnostics(wr, dev, args) if args.workload == "all" else None
     w = synth.WORKLOADS[head_id]
     if args.batch:
         w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
@@ -576,6 +612,7 @@ def run_ours(args, dist):
         "e2e": head["e2e"], "clocks": head["clocks"], "step_ms": head["step_ms"],
         "gpu_launches": head["gpu_launches"],
         "gpu": torch.cuda.get_device_name(dev),
+        "diagnostics": diagnostics,
         "per_workload": {
             recs[i]["workload"]: {
                 "value": recs[i]["value"], "unit": UNIT,

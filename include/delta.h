@@ -192,6 +192,48 @@ int delta_step(const void *q, const void *k, const void *v, const float *beta,
                delta_dtype dtype, struct CUstream_st *stream);
 
 /*
+ * delta_state_erank -- the effective rank of each state matrix, the spectral
+ * diagnostic of "DeltaProduct" §4.6:
+ *
+ *   erank(S) = exp(-sum_k p_k log p_k),  p_k = sigma_k / sum_j sigma_j
+ *
+ * over the singular values sigma_k of S (1 <= erank <= rank(S) for S != 0).
+ *
+ *   state [B, H, dk, dv]  float32 (e.g. hT of delta_fwd, or delta_step's state)
+ *   erank [B, H]          float32, written
+ *
+ * The singular values come from a one-sided Jacobi SVD of each matrix in
+ * float32 (columns rotated until every pair is orthogonal to 1e-5 of their
+ * norms, at most 40 sweeps).  A zero matrix, where the definition does not
+ * apply, gives 0.  dk, dv in {16, 32, 64, 128}; pointers 16-byte aligned,
+ * erank not overlapping state.
+ */
+int delta_state_erank(const float *state, float *erank, int B, int H, int dk, int dv,
+                      struct CUstream_st *stream);
+
+/*
+ * delta_attention_map -- the fully parallel form of "08 · linear 路线（三）"
+ * §2.4 with the gated decay of §3: for a block of N <= 64 steps per (b, h)
+ * (n_h = 1, zero initial state), the N x N matrix with o_i = sum_j A_ij v_j,
+ *
+ *   A = (Q K^T * Gam * M) T,   T = (I + strictLower(diag(beta) (Gam * K K^T)))^{-1} diag(beta)
+ *
+ * with Gam_ij = exp(gc_i - gc_j), gc the inclusive cumulative log gate, and M
+ * the causal mask including the diagonal.
+ *
+ *   q, k  [B, N, H, dk]   dtype
+ *   beta  [B, N, H]       float32
+ *   g     [B, N, H]       float32 linear gate, or NULL (=> 1)
+ *   attn  [B, H, N, N]    float32, written (row i = readout step i; 0 above the diagonal)
+ *
+ * float32 arithmetic throughout; log g is clamped at -80 as in delta_fwd.
+ * N > 64 returns DELTA_ERR_UNSUPPORTED; dk in {16, 32, 64, 128}.
+ */
+int delta_attention_map(const void *q, const void *k, const float *beta, const float *g,
+                        float *attn, int B, int H, int N, int dk, delta_dtype dtype,
+                        struct CUstream_st *stream);
+
+/*
  * delta_fwd_kernel_count -- how many kernels one delta_fwd call with these
  * sizes enqueues (0 for an empty batch), or -1 if delta_fwd would reject
  * them.  Pure host function; nothing is enqueued.
@@ -224,7 +266,8 @@ int delta_version(void);
 
 /*
  * delta_inject_failure -- test hook: the next `count` calls of delta_fwd,
- * delta_ut_transform, delta_fwd_with_ut and delta_step (together) return DELTA_ERR_CUDA, with "injected failure" in
+ * delta_ut_transform, delta_fwd_with_ut, delta_step, delta_state_erank and
+ * delta_attention_map (together) return DELTA_ERR_CUDA, with "injected failure" in
  * delta_last_error(), right after their arguments pass validation and before
  * anything is enqueued.  count = 0 clears a pending injection; count < 0 is
  * DELTA_ERR_INVALID.  The counter is process-wide.

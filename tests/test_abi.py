@@ -215,3 +215,25 @@ def test_kernel_count(lib):
     assert lib.delta_fwd_kernel_count(1, 1, 64, 16, 16, 1, 16, wr.DELTA_F32) == 1
     assert lib.delta_fwd_kernel_count(0, 1, 64, 128, 128, 1, 64, wr.DELTA_BF16) == 0
     assert lib.delta_fwd_kernel_count(1, 1, 64, 48, 16, 1, 16, wr.DELTA_F32) == -1
+
+
+def test_erank_rejects_bad_arguments(lib):
+    P = [ctypes.c_void_p((i + 1) << 40) for i in range(2)]
+    assert lib.delta_state_erank(P[0], P[1], -1, 1, 128, 128, None) == wr.DELTA_ERR_INVALID
+    assert lib.delta_state_erank(P[0], P[1], 1, 1, 96, 128, None) == wr.DELTA_ERR_UNSUPPORTED
+    assert lib.delta_state_erank(None, P[1], 1, 1, 128, 128, None) == wr.DELTA_ERR_INVALID
+    assert lib.delta_state_erank(ctypes.c_void_p((1 << 40) + 8), P[1], 1, 1, 128, 128, None) == wr.DELTA_ERR_ALIGN
+    # erank inside the state
+    assert lib.delta_state_erank(P[0], ctypes.c_void_p((1 << 40) + 1024), 1, 1, 128, 128, None) == wr.DELTA_ERR_INVALID
+    assert lib.delta_state_erank(P[0], P[1], 0, 5, 128, 128, None) == wr.DELTA_OK
+
+
+def test_attention_map_rejects_bad_arguments(lib):
+    P = [ctypes.c_void_p((i + 1) << 40) for i in range(5)]
+    call = lambda *a: lib.delta_attention_map(*a)
+    assert call(P[0], P[1], P[2], None, P[4], 1, 1, 65, 128, wr.DELTA_BF16, None) == wr.DELTA_ERR_UNSUPPORTED
+    assert call(P[0], P[1], P[2], None, P[4], 1, 1, 64, 96, wr.DELTA_BF16, None) == wr.DELTA_ERR_UNSUPPORTED
+    assert call(P[0], P[1], P[2], None, P[4], 1, 1, 8, 128, 7, None) == wr.DELTA_ERR_INVALID
+    assert call(None, P[1], P[2], None, P[4], 1, 1, 8, 128, wr.DELTA_BF16, None) == wr.DELTA_ERR_INVALID
+    assert call(P[0], P[1], P[2], None, P[0], 1, 1, 8, 128, wr.DELTA_BF16, None) == wr.DELTA_ERR_INVALID
+    assert call(P[0], P[1], P[2], None, P[4], 1, 1, 0, 128, wr.DELTA_BF16, None) == wr.DELTA_OK

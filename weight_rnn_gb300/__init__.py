@@ -15,7 +15,8 @@ import threading
 
 import torch
 
-__all__ = ["delta_fwd", "delta_fwd_static_scratch", "delta_ut_transform", "delta_fwd_with_ut", "delta_step",
+__all__ = ["delta_fwd", "delta_fwd_static_scratch", "delta_state_erank",
+           "delta_attention_map", "delta_ut_transform", "delta_fwd_with_ut", "delta_step",
            "fwd_launches", "delta_status_string", "delta_last_error",
            "delta_check_device", "delta_inject_failure", "delta_selftest_wait",
            "delta_version", "DeltaError", "library_path", "load_library",
@@ -36,7 +37,8 @@ EXPORTED_SYMBOLS = ("delta_fwd", "delta_fwd_static_scratch", "delta_ut_transform
                     "delta_fwd_with_ut",
                     "delta_fwd_kernel_count", "delta_step", "delta_status_string",
                     "delta_last_error", "delta_check_device", "delta_version",
-                    "delta_inject_failure", "delta_selftest_wait")
+                    "delta_inject_failure", "delta_selftest_wait", "delta_state_erank",
+                    "delta_attention_map")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -72,6 +74,10 @@ def load_library():
         lib.delta_fwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
         lib.delta_fwd_static_scratch.restype = i
         lib.delta_fwd_static_scratch.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.delta_state_erank.restype = i
+        lib.delta_state_erank.argtypes = [p, p, i, i, i, i, p]
+        lib.delta_attention_map.restype = i
+        lib.delta_attention_map.argtypes = [p, p, p, p, p, i, i, i, i, i, p]
         lib.delta_ut_transform.restype = i
         lib.delta_ut_transform.argtypes = [p, p, p, p, i, i, i, i, i, i, i, p]
         lib.delta_fwd_with_ut.restype = i
@@ -243,6 +249,50 @@ def delta_fwd_static_scratch(q, k, v, beta, g=None, h0=None, out=None, hT=None, 
     if st != DELTA_OK:
         raise DeltaError(st, delta_last_error())
     return out, hT
+
+
+def delta_state_erank(state, erank=None, *, stream=None):
+    """Effective rank of each state matrix ("DeltaProduct" §4.6): state
+    [B,H,dk,dv] float32 on the GPU -> erank [B,H] float32 (0 for a zero
+    matrix)."""
+    lib = load_library()
+    B, H, dk, dv = state.shape
+    dev = state.device
+    if dev.type != "cuda":
+        raise ValueError("delta_state_erank needs CUDA tensors")
+    _check(state, "state", (B, H, dk, dv), torch.float32, dev)
+    if erank is None:
+        erank = torch.empty((B, H), dtype=torch.float32, device=dev)
+    _check(erank, "erank", (B, H), torch.float32, dev)
+    st = lib.delta_state_erank(_ptr(state), _ptr(erank), B, H, dk, dv, _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return erank
+
+
+def delta_attention_map(q, k, beta, g=None, attn=None, *, stream=None):
+    """The fully parallel form ([DR] §2.4, gated as in §3) for N <= 64 steps:
+    q, k [B,N,H,dk] (bf16 or float32), beta [B,N,H], g [B,N,H] or None ->
+    attn [B,H,N,N] float32 with o_i = sum_j attn[i, j] v_j for a zero initial
+    state."""
+    lib = load_library()
+    B, N, H, dk = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("delta_attention_map needs CUDA tensors")
+    dt = q.dtype
+    _check(q, "q", (B, N, H, dk), dt, dev)
+    _check(k, "k", (B, N, H, dk), dt, dev)
+    _check(beta, "beta", (B, N, H), torch.float32, dev)
+    _check(g, "g", (B, N, H), torch.float32, dev)
+    if attn is None:
+        attn = torch.empty((B, H, N, N), dtype=torch.float32, device=dev)
+    _check(attn, "attn", (B, H, N, N), torch.float32, dev)
+    st = lib.delta_attention_map(_ptr(q), _ptr(k), _ptr(beta), _ptr(g), _ptr(attn), B, H, N,
+                                 dk, _dtype_code(dt), _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return attn
 
 
 def _kvb_shapes(k, v, beta, B, T, H, dk, n_h):

@@ -344,6 +344,53 @@ int delta_fwd_with_ut(const void *q, const void *k, const void *v, const float *
   return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "tensor-core chunk kernel launch");
 }
 
+int delta_state_erank(const float *state, float *erank, int B, int H, int dk, int dv,
+                      struct CUstream_st *stream) {
+  if (B < 0 || H < 0) return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d", B, H);
+  if (!supported_dim(dk) || !supported_dim(dv))
+    return fail(DELTA_ERR_UNSUPPORTED, "dk=%d dv=%d not in {16,32,64,128}", dk, dv);
+  if ((int64_t)B * H >= (int64_t(1) << 31))
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
+  const int64_t BH = (int64_t)B * H;
+  if (BH == 0) return DELTA_OK;
+  if (!state || !erank) return fail(DELTA_ERR_INVALID, "state and erank must be non-NULL");
+  if (!aligned16(state) || !aligned16(erank))
+    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+  if (overlap(range(state, BH * dk * dv * 4), range(erank, BH * 4)))
+    return fail(DELTA_ERR_INVALID, "erank overlaps state");
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+  const cudaError_t err = delta::launch_erank(state, erank, BH, dk, dv, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "effective-rank kernel launch");
+}
+
+int delta_attention_map(const void *q, const void *k, const float *beta, const float *g,
+                        float *attn, int B, int H, int N, int dk, delta_dtype dtype,
+                        struct CUstream_st *stream) {
+  if (B < 0 || H < 0 || N < 0) return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d N=%d", B, H, N);
+  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
+    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (!supported_dim(dk)) return fail(DELTA_ERR_UNSUPPORTED, "dk=%d not in {16,32,64,128}", dk);
+  if (N > 64) return fail(DELTA_ERR_UNSUPPORTED, "N=%d: the attention map is built for N <= 64", N);
+  if ((int64_t)B * H >= (int64_t(1) << 31))
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
+  const int64_t BH = (int64_t)B * H;
+  if (BH == 0 || N == 0) return DELTA_OK;
+  if (!q || !k || !beta || !attn) return fail(DELTA_ERR_INVALID, "q, k, beta and attn must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(beta) || !aligned16(g) || !aligned16(attn))
+    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+  const int64_t esz = dtype == DELTA_BF16 ? 2 : 4;
+  const Range r_a = range(attn, BH * N * N * 4);
+  const Range inputs[] = {range(q, BH * N * dk * esz), range(k, BH * N * dk * esz),
+                          range(beta, BH * N * 4), range(g, g ? BH * N * 4 : 0)};
+  for (const Range &r : inputs)
+    if (overlap(r_a, r)) return fail(DELTA_ERR_INVALID, "attn overlaps an input");
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+  const cudaError_t err = delta::launch_attention_map(q, k, beta, g, attn, B, H, N, dk,
+                                                     dtype == DELTA_BF16,
+                                                     reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "attention-map kernel launch");
+}
+
 int delta_fwd_kernel_count(int B, int H, int T, int dk, int dv, int n_h, int chunk,
                            delta_dtype dtype) {
   if (B < 0 || H < 0 || T < 0 || (dtype != DELTA_F32 && dtype != DELTA_BF16) ||

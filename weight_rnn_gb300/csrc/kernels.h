@@ -64,4 +64,16 @@ cudaError_t launch_state_passthrough(const FwdArgs &a, cudaStream_t s);
 // One decode step, state updated in place.
 cudaError_t launch_step(const StepArgs &a, cudaStream_t s);
 
+// Effective rank of each of the BH state matrices [dk][dv] (float32) into
+// erank[BH]; one block per matrix with erank_smem_bytes of shared memory.
+int64_t erank_smem_bytes(int dk, int dv);
+cudaError_t launch_erank(const float *state, float *erank, int64_t BH, int dk, int dv,
+                         cudaStream_t s);
+
+// The attention map of the fully parallel form for N <= 64 steps (n_h = 1):
+// q, k [B][N][H][dk] (bf16 or float32), beta, g [B][N][H], attn [B][H][N][N].
+cudaError_t launch_attention_map(const void *q, const void *k, const float *beta, const float *g,
+                                 float *attn, int64_t B, int64_t H, int N, int dk, bool bf16,
+                                 cudaStream_t s);
+
 }  // namespace delta
