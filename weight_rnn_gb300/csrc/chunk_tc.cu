@@ -743,6 +743,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       //      released early), staged as bf16 rows in the V slot of this chunk
       //      (its reader, the U product, has completed) by transposing 8x8
       //      stores, then written out in 16-byte pieces ----
+      // read O^T only once the chain's TMEM work of this chunk (the S^T
+      // conversion, SRDY phase n + 1) is done; the next SRDY phase needs
+      // this chunk's OFREE (through the output product of the next chunk)
+      if (n + 1 < NT) wait_bar(sm, B_SRDY, (n + 1) & 1, 3);
       wait_bar(sm, B_OFULL, n & 1, 3);
       tc_fence_after();
       uint32_t o0[32], o1[32];
