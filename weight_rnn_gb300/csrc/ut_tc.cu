@@ -467,25 +467,29 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
       float *AX = reinterpret_cast<float *>(sm.slot(s) + gi * 16384);
 
       // ---- A = strictLower(diag(beta) (Gam * K K^T)) from the Gram block of
-      //      this chunk (TMEM lanes 64 gi.., columns 64 gi..), transposed into
-      //      the upper triangle of the solve array ----
+      //      this chunk (TMEM lanes 64 gi.., columns 64 gi..), into the upper
+      //      triangle of the solve array: A_ir sits at (r, i) for i > r, and
+      //      as K K^T is symmetric, row r of that triangle comes from TMEM row
+      //      r of the Gram block, A_ir = beta_i 2^gc_i * 2^-gc_r * G_ri: each
+      //      thread writes its own row in 16-byte pieces.  Rows 32..63 have no
+      //      entry in columns 0..31, so that warp has nothing to do ----
       wait_bar(sm, B_GFULL, i & 1, 2);
       tc_fence_after();
-      {
-        const int jlo = hf == 0 ? 0 : 32, jhi = hf == 0 ? 32 : (q == 1 ? 64 : 32);
-        const float bi = sb[row], rf = beg[row], gr = GATED ? gc[row] : 0.f;
+      if (!(q == 1 && hf == 0)) {
+        const int clo = 32 * hf;
+        // ratio regime: row factor 2^-gc_r (column factors beta_i 2^gc_i in beg)
+        const float rf = (GATED && ratio) ? ieg[row] : 1.f, gr = GATED ? gc[row] : 0.f;
+        float *arow = AX + row * 64;
+        const int sw = (row & 7) << 2;
 #pragma unroll 1
-        for (int jb = jlo; jb < jhi; jb += 16) {
+        for (int jb = clo; jb < clo + 32; jb += 16) {
           uint32_t g[16];
           tmem_ld16(tmem_addr(tmem, 32 * (warp & 3), 64 * gi + jb), g);
           float cf[16];
-          if (!GATED) {
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) cf[jj] = bi;
-          } else if (ratio) {
+          if (!GATED || ratio) {
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {
-              const float4 e4 = *reinterpret_cast<const float4 *>(ieg + jb + jj);
+              const float4 e4 = *reinterpret_cast<const float4 *>(beg + jb + jj);
               cf[jj] = rf * e4.x;
               cf[jj + 1] = rf * e4.y;
               cf[jj + 2] = rf * e4.z;
@@ -493,15 +497,24 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
             }
           } else {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) cf[jj] = bi * fast_exp2(gr - gc[jb + jj]);
+            for (int jj = 0; jj < 16; ++jj) cf[jj] = sb[jb + jj] * fast_exp2(gc[jb + jj] - gr);
           }
           tmem_wait_ld_regs(g);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = jb + jj;
-            if (j < row) AX[swz(j, row)] = cf[jj] * __uint_as_float(g[jj]);
+          for (int t = 0; t < 4; ++t) {
+            const int c0 = jb + 4 * t;
+            // a piece wholly at or below the diagonal holds no entry of A (the
+            // lower triangle is written with X later and never read before)
+            if (c0 + 3 > row)
+              *reinterpret_cast<float4 *>(arow + (c0 ^ sw)) =
+                  make_float4(cf[4 * t] * __uint_as_float(g[4 * t]),
+                              cf[4 * t + 1] * __uint_as_float(g[4 * t + 1]),
+                              cf[4 * t + 2] * __uint_as_float(g[4 * t + 2]),
+                              cf[4 * t + 3] * __uint_as_float(g[4 * t + 3]));
           }
         }
+      }
+      {
         tc_fence_before();
         arrive_warp(sm.bar(B_GFREE), lane);
       }
