@@ -141,7 +141,7 @@ __device__ __forceinline__ int swz(int r, int c) { return r * 64 + (c ^ ((r & 7)
 
 // The solve's 64x64 array holds A_ij (i > j) at (j, i) -- the upper triangle --
 // and X_ij = ((I + A)^{-1})_ij (i > j) at (i, j) -- the lower triangle.  The
-// diagonal holds the chunk's cumulative log gate (X_ii = 1 is implicit).
+// diagonal is never read (X_ii = 1 is implicit).
 __device__ __forceinline__ float ldA(const float *AX, int i, int j) { return AX[swz(j, i)]; }
 // X_rc of a block that touches the diagonal: 1 on it, 0 above it.
 __device__ __forceinline__ float ldXm(const float *M, int r, int c) {
