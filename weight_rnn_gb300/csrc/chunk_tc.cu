@@ -153,7 +153,7 @@ struct TcParams {
   const float *beta, *g, *h0;
   __nv_bfloat16 *out;
   float *hT;
-  int H, T, L, n_h, nchunks;
+  int H, T, n_h, nchunks;
 };
 
 struct Smem {
@@ -241,6 +241,27 @@ struct Rows {
   __device__ int pos(int r, int n_h) const { return (t_lo + r) * n_h + (n_h - 1) - e0; }
 };
 
+// Exact regime of the gated path: the Q rows of a stage times their readout
+// factor qf, in place (thread ft of the 128 takes the 16-byte pieces ft,
+// ft + 128, ... of both 64-column halves).  Out of line: it runs only for the
+// chunks whose decay leaves the range of the ratio form, and inline it would
+// spread the hot code over more instruction cache lines.
+__device__ __noinline__ void scale_q_rows(uint8_t *qt, const float *qf, int ft) {
+#pragma unroll 2
+  for (int it = 0; it < 8; ++it) {
+    const int qi = ft + 128 * it;  // 16-byte piece: 512 per 64-column half
+    uint8_t *pc = qt + ((qi >> 9) ? ST_Q1 : ST_Q0) + (qi & 511) * 16;
+    const uint4 v = *reinterpret_cast<const uint4 *>(pc);
+    const float f = qf[(qi & 511) >> 3];
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      o4[u] = pack_bf16(__uint_as_float(in[u] << 16) * f, __uint_as_float(in[u] & 0xFFFF0000u) * f);
+    *reinterpret_cast<uint4 *>(pc) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+  }
+}
+
 // 14 warps: at most 4 per SM sub-partition, so 128 registers per thread
 template <bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -253,7 +274,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   // access below in the shared state space
   sm.base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __builtin_assume(__isShared(sm.base));
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31;
+  // the warp index through a shuffle from lane 0: the compiler then knows it
+  // is the same in every lane, so that branches on a warp's role are not
+  // divergent and need no reconvergence code around the warp-wide
+  // instructions in them (a much smaller kernel)
+  const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   // the layout needs SMEM_TOTAL bytes after the 1024-byte alignment
   if ((uint32_t)(sm.base - smem_raw) + SMEM_TOTAL > SMEM_ALLOC) {
     if (tid == 0) atomicCAS(&g_tc_error, 0u, 0xFFu);
@@ -323,17 +349,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       const int t_lo = e0 / n_h;
       uint8_t *st = sm.stage(s);
       if (lane == 0) {
-        // keep the chunk after the ones in the ring warm in L2
-        for (int pf = (n == 0 ? NS : n + NS); pf <= n + NS && pf < NT; ++pf) {
-          const int pe = pf * C, pt = pe / n_h;
-          tma_prefetch_4d(&map_k, 0, h, pe, b);
-          tma_prefetch_4d(&map_k, 64, h, pe, b);
-          tma_prefetch_4d(&map_v, 0, h, pe, b);
-          tma_prefetch_4d(&map_v, 64, h, pe, b);
-          tma_prefetch_4d(&map_q, 0, h, pt, b);
-          tma_prefetch_4d(&map_q, 64, h, pt, b);
-          tma_prefetch_3d(&map_t, 0, 0, tc0 + pf);
-        }
         // K and Q first, on their own barrier (the G product waits for them
         // only); V, needed later, on a second one
         mbar_arrive_expect_tx(sm.bar(B_FULL + s), 2u * (8192u + (uint32_t)QR * 128u));
@@ -393,7 +408,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     //   warp 15  the look-ahead: G(0); per chunk W(m) (TFULL, WREAD(m-1)),
     //            then G(m+1) (FULL, GFREE(m))
     // Each commits the barriers of its own products; every hand-off between
-    // kinds is a barrier.
+    // kinds is a barrier.  A descriptor's address field is the byte address
+    // / 16 and every operand lies below 256 KiB, so a K step of an operand is
+    // the descriptor plus its byte offset / 16.  Only the two products on the recurrence (S W and
+    // the state update) are unrolled: the kernel's hot code has to fit the
+    // SM's instruction cache, and with every SM of a GPC running this kernel
+    // the refills of a miss are slow.
     if (lane == 0) {
       constexpr uint32_t id_uw = idesc_bf16(128, 64, true, false);        // A = K^T or V^T (MN-major), B = T
       constexpr uint32_t id_sw = idesc_bf16(128, 64, false, true, true);  // B = W^T (MN-major), negated
@@ -415,19 +435,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             break;
           if (n >= 1 && !wait_bar(sm, B_VRDY, (n - 1) & 1, 1)) break;
           tc_fence_after();
-          const uint32_t tb = a_tr + (n & 1) * 8192;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_V, sdesc_sw128(st + ST_V0 + k * 2048, 8192, 1024),
-                   sdesc_sw128(tb + k * 32, 0, 1024), id_uw, k > 0);
+          const uint64_t du = sdesc_sw128(st + ST_V0, 8192, 1024);
+          const uint64_t dt = sdesc_sw128(a_tr + (n & 1) * 8192, 0, 1024);
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) mma_ss(tmem + TM_V, du + k * 128, dt + k * 2, id_uw, k > 0);
           mma_commit(sm.bar(B_TREMPTY + (n & 1)));
           // ---- V~^T = U^T - S^T W^T ----
           if (!wait_bar(sm, B_SRDY, n & 1, 1) || !wait_bar(sm, B_WCVT + (n & 1), (n >> 1) & 1, 1)) break;
           tc_fence_after();
-          const uint32_t wsb = a_ws + (n & 1) * 16384;
+          const uint64_t dw = sdesc_sw128(a_ws + (n & 1) * 16384, 8192, 1024);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + TM_V, tmem + TM_SBF + k * 8, sdesc_sw128(wsb + k * 2048, 8192, 1024), id_sw, true);
+          for (int k = 0; k < 8; ++k) mma_ts(tmem + TM_V, tmem + TM_SBF + k * 8, dw + k * 128, id_sw, true);
           mma_commit(sm.bar(B_VDONE));
           mma_commit(sm.bar(B_WSFREE + (n & 1)));
           // ---- S^T += V~^T Kd = (V~ diag exp(gc_C - gc))^T K (S^T was scaled by
@@ -437,10 +455,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           // (gated: S~ += ((V~ diag dec) / sigma')^T K, the decay carried by
           // the scale sigma of the accumulator)
           const uint32_t vb = GATED ? TM_VBD : TM_VB;
+          const uint64_t dk = sdesc_sw128(st + ST_K0, 16384, 1024);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_S, tmem + vb + k * 8, sdesc_sw128(st + ST_K0 + k * 2048, 16384, 1024),
-                   id_kd, true);
+          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_S, tmem + vb + k * 8, dk + k * 128, id_kd, true);
           mma_commit(sm.bar(B_SFULL));
           mma_commit(sm.bar(B_EMPTY + s));
         }
@@ -453,22 +470,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           if (!wait_bar(sm, B_VDONE, n & 1, 1)) break;
           if (n >= 1 && !wait_bar(sm, B_OFREE, (n - 1) & 1, 1)) break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t qa = st + (k < 4 ? ST_Q0 : ST_Q1) + (k & 3) * 32;
-            mma_ts(tmem + TM_O, tmem + TM_SBF + k * 8, sdesc_sw128(qa, 0, 1024), id_o, k > 0);
-          }
+          // (the two 64-column halves of Q are 16 KiB apart)
+          const uint64_t dq = sdesc_sw128(st + ST_Q0, 0, 1024);
+#pragma unroll 1
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + TM_O, tmem + TM_SBF + k * 8, dq + (k >> 2) * 1024 + (k & 3) * 2, id_o, k > 0);
           mma_commit(sm.bar(B_SQDONE));
           // ---- O^T += V~^T P^T, behind the state update (gated, ratio
           //      regime: the dec-scaled copy of V~, P carrying 1 / dec) ----
           if (!wait_bar(sm, B_SFULL, n & 1, 1)) break;
           if (GATED && !wait_bar(sm, B_PLAN + (n & 3), (n >> 2) & 1, 1)) break;
           tc_fence_after();
-          const uint32_t pb = a_p + (n & 1) * 8192;
+          const uint64_t dp = sdesc_sw128(a_p + (n & 1) * 8192, 0, 1024);
           const uint32_t vsrc = (GATED && sm.plan(n)->ratio) ? TM_VBD : TM_VB;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_O, tmem + vsrc + k * 8, sdesc_sw128(pb + k * 32, 0, 1024), id_o, true);
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) mma_ts(tmem + TM_O, tmem + vsrc + k * 8, dp + k * 2, id_o, true);
           mma_commit(sm.bar(B_OFULL));
           mma_commit(sm.bar(B_PFREE + (n & 1)));
           mma_commit(sm.bar(B_EMPTY + s));
@@ -480,14 +496,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           // TM_G is free once the P warps have read chunk m-1's G
           if (m >= 1 && !wait_bar(sm, B_GFREE, (m - 1) & 1, 1)) return false;
           tc_fence_after();
-          const uint32_t kq0 = smem_u32(sm.stage(m % NS));
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const uint32_t kq = kq0 + hf * 16384;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(tmem + TM_G, sdesc_sw128(kq + k * 32, 0, 1024), sdesc_sw128(kq + k * 32, 0, 1024),
-                     id_g, hf > 0 || k > 0);
+          // [K;Q] is 128 rows (K then Q, 64 rows = 8 KiB each) per 64-column
+          // half, the halves 16 KiB apart
+          const uint64_t dg = sdesc_sw128(smem_u32(sm.stage(m % NS)), 0, 1024);
+#pragma unroll 1
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t d = dg + (k >> 2) * 1024 + (k & 3) * 2;
+            mma_ss(tmem + TM_G, d, d, id_g, k > 0);
           }
           mma_commit(sm.bar(B_GFULL));
           return true;
@@ -498,12 +513,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           if (!wait_bar(sm, B_TFULL + (m & 1), (m >> 1) & 1, 1)) break;
           if (m >= 1 && !wait_bar(sm, B_WREAD, (m - 1) & 1, 1)) break;
           tc_fence_after();
-          const uint32_t kq = smem_u32(sm.stage(m % NS));
-          const uint32_t wb = GATED ? a_tw : a_tr + (m & 1) * 8192;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_W, sdesc_sw128(kq + ST_K0 + k * 2048, 16384, 1024),
-                   sdesc_sw128(wb + k * 32, 0, 1024), id_uw, k > 0);
+          const uint64_t dk = sdesc_sw128(smem_u32(sm.stage(m % NS)) + ST_K0, 16384, 1024);
+          const uint64_t dt = sdesc_sw128(GATED ? a_tw : a_tr + (m & 1) * 8192, 0, 1024);
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) mma_ss(tmem + TM_W, dk + k * 128, dt + k * 2, id_uw, k > 0);
           mma_commit(sm.bar(B_WFULL));
           mma_commit(sm.bar(B_TREMPTY + (m & 1)));
           if (m + 1 < NT) ok = issue_g(m + 1);
@@ -522,15 +535,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int L = q4 * 32 + lane;         // TMEM lane of this thread
     float *eg = sm.arr(SM_EG), *gcs = sm.arr(SM_GC);
     float ls = 0.f;  // P warps, gated: log2 sigma of the state before chunk m's update
-    // gated, warp 2: the linear gate at the extended steps lane and lane + 32
-    // of a chunk (1 where no token starts, and past the end), read one chunk
-    // ahead so that the loads are in flight while the chunk before is prepared
+    // gated, warp 2: the linear gate of the tokens whose first sub-step lies
+    // in a chunk, one token per lane (and lane + 32), and that sub-step's
+    // place in the chunk (-1: no such token); read one chunk ahead so that
+    // the loads are in flight while the chunk before is prepared
     float gnx[2] = {1.f, 1.f};
+    int gpos[2] = {-1, -1};
     auto gate_fetch = [&](int m) {
+      const int e0 = m * C;
+      const int t0 = (e0 + n_h - 1) / n_h;  // the first token that starts in the chunk
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int e = m * C + lane + 32 * k;
-        gnx[k] = (m < NT && e < p.L && (e % n_h) == 0) ? p.g[((size_t)b * p.T + e / n_h) * p.H + h] : 1.f;
+        const int t = t0 + lane + 32 * k, e = t * n_h - e0;
+        const bool in = m < NT && e < C && t < p.T;
+        gpos[k] = in ? e : -1;
+        gnx[k] = in ? p.g[((size_t)b * p.T + t) * p.H + h] : 1.f;
       }
     };
     if (GATED && warp == 2) gate_fetch(0);
@@ -541,9 +560,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       // a failed wait sets the abort flag; every thread still reaches the
       // next named barrier and all of them leave together after it
       if (GATED && warp == 2) {
+        // log2 g at each token's first sub-step, 0 at the others
         float *lam = sm.lam();
-        lam[lane] = fmaxf(logf(gnx[0]), kLogGateFloor) * kLog2e;
-        lam[lane + 32] = fmaxf(logf(gnx[1]), kLogGateFloor) * kLog2e;
+        lam[lane] = 0.f;
+        lam[lane + 32] = 0.f;
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (gpos[k] >= 0) lam[gpos[k]] = gate_log2(gnx[k]);
         __syncwarp();
         gate_fetch(m + 1);
         float lo, hi;
@@ -643,11 +667,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           const uint8_t *tt = sm.base + OFF_TR + (m & 1) * 8192;
           uint8_t *tw = sm.base + OFF_TW;
           const int ft = tid - 128;  // 0..63
-          uint4 v[8];
-#pragma unroll
-          for (int it = 0; it < 8; ++it) v[it] = *reinterpret_cast<const uint4 *>(tt + (ft + 64 * it) * 16);
-#pragma unroll
+#pragma unroll 2
           for (int it = 0; it < 8; ++it) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(tt + (ft + 64 * it) * 16);
             // 16-byte piece qi of the swizzled tile: row qi / 8, columns
             // 8 ((qi % 8) ^ (row % 8)) .. + 7
             const int qi = ft + 64 * it, row = qi >> 3;
@@ -655,7 +677,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const float4 e0 = *reinterpret_cast<const float4 *>(eg + c0);
             const float4 e1 = *reinterpret_cast<const float4 *>(eg + c0 + 4);
             const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-            const uint32_t in[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
             uint32_t o4[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -710,25 +732,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         wait_bar(sm, B_TFULL + (m & 1), (m >> 1) & 1, 3);
         if (!sm.plan(m)->ratio) {
           wait_bar(sm, B_FULL + m % NS, (m / NS) & 1, 3);  // the Q tile landed
-          const float *qf = sm.arr(SM_QF + (m & 3) * 256);
-          uint8_t *qt = sm.stage(m % NS);
-          uint4 v[8];
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int qi = ft + 128 * it;  // 16-byte piece: 512 per 64-column half
-            v[it] = *reinterpret_cast<const uint4 *>(qt + ((qi >> 9) ? ST_Q1 : ST_Q0) + (qi & 511) * 16);
-          }
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int qi = ft + 128 * it;
-            const float f = qf[(qi & 511) >> 3];
-            const uint32_t in[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
-            uint32_t o4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              o4[u] = pack_bf16(__uint_as_float(in[u] << 16) * f, __uint_as_float(in[u] & 0xFFFF0000u) * f);
-            st_chunk(qt + ((qi >> 9) ? ST_Q1 : ST_Q0) + (qi & 511) * 16, o4);
-          }
+          scale_q_rows(sm.stage(m % NS), sm.arr(SM_QF + (m & 3) * 256), ft);
         }
       }
       fence_proxy_async_smem();
@@ -1000,7 +1004,6 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const void *t_mat, cudaStream_t s)
   p.hT = a.hT;
   p.H = (int)a.H;
   p.T = (int)a.T;
-  p.L = (int)a.L;
   p.n_h = a.n_h;
   p.nchunks = nt;
   auto kern = a.g ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;

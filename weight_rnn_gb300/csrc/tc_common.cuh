@@ -23,6 +23,15 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// log2 g of a gate g in [0, 1], clamped at kLogGateFloor nats: lg2 on the
+// MUFU unit (absolute error ~2^-22 near 1; g = 0 and subnormal g give the
+// floor).  A short body: the gate scan runs in every chunk of the state pass.
+__device__ __forceinline__ float gate_log2(float g) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(g));
+  return fmaxf(y, kLogGateFloor * kLog2e);
+}
+
 // Named barrier over 128 threads.
 __device__ __forceinline__ void named_sync(int id) {
   asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");

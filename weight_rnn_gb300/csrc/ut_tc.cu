@@ -294,7 +294,12 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
   Smem sm;
   sm.base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __builtin_assume(__isShared(sm.base));
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31;
+  // the warp index through a shuffle from lane 0: the compiler then knows it
+  // is the same in every lane, so that branches on a warp's role are not
+  // divergent and need no reconvergence code around the warp-wide
+  // instructions in them (a much smaller kernel)
+  const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   if ((uint32_t)(sm.base - smem_raw) + SMEM_TOTAL > UT_SMEM_ALLOC) {
     if (tid == 0) atomicCAS(&g_ut_error, 0u, 0xFFu);
     return;
@@ -381,7 +386,7 @@ ut_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUt
           sb[lane + 32 * k] = pb[2 * x + k];
           // the log2 gate (log g at each token's first sub-step, clamped so
           // that g = 0 stays finite; 0 elsewhere and past the end)
-          sl[lane + 32 * k] = GATED ? fmaxf(logf(pg[2 * x + k]), kLogGateFloor) * kLog2e : 0.f;
+          sl[lane + 32 * k] = GATED ? gate_log2(pg[2 * x + k]) : 0.f;
         }
         if (2 * pr + x < p.total) bytes += 16384u;
       }
