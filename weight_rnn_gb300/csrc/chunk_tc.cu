@@ -102,9 +102,10 @@ enum {
   B_WSFREE = 4 * NS + 4,   // [2] MMA -> ff: the W^T operand buffer consumed (by the S W product)
   B_PFREE = 4 * NS + 6,    // [2] MMA -> prep: P buffer consumed (by the V~ P product)
   B_WCVT = 4 * NS + 8,     // [2] ff -> MMA: W^T bf16 operand buffer filled (per warp)
-  B_TFULL = 4 * NS + 10,   // [2] prep -> MMA: P, T (diag exp gc) and Q exp(gc) of a chunk ready (per warp)
-  B_PLAN = 4 * NS + 12,    // [4] prep -> chain, MMA: the chunk's ChunkPlan, dec and readout factors (gated)
-  B_GFULL = 4 * NS + 16,   // MMA -> prep: G in TMEM
+  B_TFULL = 4 * NS + 10,   // [2] prep -> MMA: T (gated: T diag exp gc) of a chunk ready (warps 4, 5)
+  B_PLAN = 4 * NS + 12,    // [4] prep -> chain, MMA, ff: the chunk's ChunkPlan, dec and readout factors (gated)
+  B_PRDY = 4 * NS + 16,    // [2] prep -> MMA: P of a chunk in shared memory (warps 2, 3)
+  B_GFULL = 4 * NS + 18,   // MMA -> prep: G in TMEM
   B_GFREE,           // prep -> MMA: G read (per P warp, 2)
   B_WFULL,           // MMA -> ff, prep: W^T in TMEM (T diag(exp gc) consumed)
   B_WREAD,           // ff -> MMA: W^T read out of TMEM (per warp)
@@ -309,7 +310,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mbar_init(sm.bar(B_WSFREE + s), 1);
       mbar_init(sm.bar(B_PFREE + s), 1);
       mbar_init(sm.bar(B_WCVT + s), 4);
-      mbar_init(sm.bar(B_TFULL + s), 4);
+      mbar_init(sm.bar(B_TFULL + s), 2);
+      mbar_init(sm.bar(B_PRDY + s), 2);
     }
     for (int s = 0; s < 4; ++s) mbar_init(sm.bar(B_PLAN + s), 1);
     // count per barrier, from B_GFULL on
@@ -404,7 +406,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // completions as none): ring barriers carry the slot index.
     //   warp 14  the outputs of n: O^T = S^T (Q exp gc)^T behind the S W
     //            product (VDONE, OFREE(n-1)), O^T += V~^T P^T behind the
-    //            state update (SFULL)
+    //            state update (SFULL, PRDY(n))
     //   warp 15  the look-ahead: G(0); per chunk W(m) (TFULL, WREAD(m-1)),
     //            then G(m+1) (FULL, GFREE(m))
     // Each commits the barriers of its own products; every hand-off between
@@ -479,6 +481,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           // ---- O^T += V~^T P^T, behind the state update (gated, ratio
           //      regime: the dec-scaled copy of V~, P carrying 1 / dec) ----
           if (!wait_bar(sm, B_SFULL, n & 1, 1)) break;
+          if (!wait_bar(sm, B_PRDY + (n & 1), (n >> 1) & 1, 1)) break;
           if (GATED && !wait_bar(sm, B_PLAN + (n & 3), (n >> 2) & 1, 1)) break;
           tc_fence_after();
           const uint64_t dp = sdesc_sw128(a_p + (n & 1) * 8192, 0, 1024);
@@ -529,8 +532,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   } else if (warp < 6) {
     // ===================================================== prep warps
     // per chunk m: P = Q K^T * Gam * M from rows 64..127 of G, then GFREE
-    // (warps 2, 3); T diag(exp gc) for the W product (warps 4, 5; gated);
-    // then TFULL
+    // and PRDY (warps 2, 3); T diag(exp gc) for the W product, then TFULL
+    // (warps 4, 5; ungated: TFULL once the T tile has landed)
     const int q4 = warp & 3;              // TMEM lane quarter
     const int L = q4 * 32 + lane;         // TMEM lane of this thread
     float *eg = sm.arr(SM_EG), *gcs = sm.arr(SM_GC);
@@ -687,8 +690,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           }
         }
       }
+      // P goes to the V~ P product; T diag(exp gc) to the W product, which
+      // thus does not wait for P
       fence_proxy_async_smem();
-      arrive_warp(sm.bar(B_TFULL + (m & 1)), lane);
+      arrive_warp(sm.bar((warp < 4 ? B_PRDY : B_TFULL) + (m & 1)), lane);
     }
   } else if (warp < 10) {
     // ===================================================== feed-forward warps
@@ -722,14 +727,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         st_chunk(ws + sw128_offset(L, 8 * q, 128), {pw_[4 * q], pw_[4 * q + 1], pw_[4 * q + 2], pw_[4 * q + 3]});
       if (GATED) {
         // ---- the readout factor exp(gc) at each readout row's sub-step
-        //      (published by the prep warps with the chunk's T diag(exp gc),
-        //      before TFULL).  Ratio regime (the chunk's decay stays above
+        //      (published by prep warp 2 with the chunk's plan).  Ratio regime (the chunk's decay stays above
         //      2^-100; P' = Q K^T * 2^-gc_j): the output rows are scaled by
         //      it at write-out.  Exact regime: Q exp(gc) in place (rows past
         //      the readouts zeroed) and no output scaling.  The G product
         //      (which read Q) completed before P and W; the output product
         //      that reads Q waits for the S W product, which waits for WCVT ----
-        wait_bar(sm, B_TFULL + (m & 1), (m >> 1) & 1, 3);
+        // (the plan of chunk m + 4 needs this thread's W^T of chunk m + 2)
+        wait_bar(sm, B_PLAN + (m & 3), (m >> 2) & 1, 3);
         if (!sm.plan(m)->ratio) {
           wait_bar(sm, B_FULL + m % NS, (m / NS) & 1, 3);  // the Q tile landed
           scale_q_rows(sm.stage(m % NS), sm.arr(SM_QF + (m & 3) * 256), ft);
