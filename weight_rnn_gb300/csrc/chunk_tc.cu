@@ -443,7 +443,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int k = 0; k < 4; ++k) mma_ss(tmem + TM_V, du + k * 128, dt + k * 2, id_uw, k > 0);
           mma_commit(sm.bar(B_TREMPTY + (n & 1)));
           // ---- V~^T = U^T - S^T W^T ----
-          if (!wait_bar(sm, B_SRDY, n & 1, 1) || !wait_bar(sm, B_WCVT + (n & 1), (n >> 1) & 1, 1)) break;
+          if (!wait_bar(sm, B_WCVT + (n & 1), (n >> 1) & 1, 1) || !wait_bar(sm, B_SRDY, n & 1, 1)) break;
           tc_fence_after();
           const uint64_t dw = sdesc_sw128(a_ws + (n & 1) * 16384, 8192, 1024);
 #pragma unroll
@@ -469,8 +469,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           const uint32_t st = smem_u32(sm.stage(s));
           // ---- O^T = S^T (Q exp gc)^T, behind the S W product (it reads the
           //      same bf16 S^T, which is rewritten once both ended) ----
-          if (!wait_bar(sm, B_VDONE, n & 1, 1)) break;
           if (n >= 1 && !wait_bar(sm, B_OFREE, (n - 1) & 1, 1)) break;
+          if (!wait_bar(sm, B_VDONE, n & 1, 1)) break;
           tc_fence_after();
           // (the two 64-column halves of Q are 16 KiB apart)
           const uint64_t dq = sdesc_sw128(st + ST_Q0, 0, 1024);
@@ -480,9 +480,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           mma_commit(sm.bar(B_SQDONE));
           // ---- O^T += V~^T P^T, behind the state update (gated, ratio
           //      regime: the dec-scaled copy of V~, P carrying 1 / dec) ----
-          if (!wait_bar(sm, B_SFULL, n & 1, 1)) break;
           if (!wait_bar(sm, B_PRDY + (n & 1), (n >> 1) & 1, 1)) break;
           if (GATED && !wait_bar(sm, B_PLAN + (n & 3), (n >> 2) & 1, 1)) break;
+          if (!wait_bar(sm, B_SFULL, n & 1, 1)) break;
           tc_fence_after();
           const uint64_t dp = sdesc_sw128(a_p + (n & 1) * 8192, 0, 1024);
           const uint32_t vsrc = (GATED && sm.plan(n)->ratio) ? TM_VBD : TM_VB;
@@ -755,8 +755,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       // read O^T only once the chain's TMEM work of this chunk (the S^T
       // conversion, SRDY phase n + 1) is done; the next SRDY phase needs
       // this chunk's OFREE (through the output product of the next chunk)
-      if (n + 1 < NT) wait_bar(sm, B_SRDY, (n + 1) & 1, 3);
       wait_bar(sm, B_OFULL, n & 1, 3);
+      if (n + 1 < NT) wait_bar(sm, B_SRDY, (n + 1) & 1, 3);
       tc_fence_after();
       uint32_t o0[32], o1[32];
       tmem_ld16x256b_x8(tmem_addr(tmem + TM_O, q4 * 32, 0), o0);
@@ -862,12 +862,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       //      V~^T itself for the V~ P product otherwise.  The products of the
       //      previous chunk read the old ones until the output group ended (it
       //      is issued after the state update) ----
+      if (n >= 1) wait_bar(sm, B_OFULL, (n - 1) & 1, 4);
       wait_bar(sm, B_VDONE, n & 1, 4);
       tc_fence_after();
-      if (n >= 1) {
-        wait_bar(sm, B_OFULL, (n - 1) & 1, 4);
-        tc_fence_after();
-      }
       // (the plan of chunk n was waited for at the previous chunk's end)
       const bool plain = !GATED || !sm.plan(n)->ratio;
       const float *dec = sm.arr(SM_DEC + (n & 3) * 256);
@@ -897,17 +894,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       // ---- the updated state: S^T -> bf16 operand for the next chunk (gated:
       //      sigma S~^T, and the rescale of the next chunk's plan), or hT; the
       //      S W and S (Q) products of this chunk read the old bf16 copy ----
-      wait_bar(sm, B_SFULL, n & 1, 4);
-      tc_fence_after();
-      const float sig = GATED ? sm.plan(n)->sig : 1.f;  // sigma of S~ in TMEM now
+      // (the waits that usually completed earlier go first, so that the
+      // state update's is the last one)
+      float rs = 1.f;
       if (n + 1 < NT) {
-        float rs = 1.f;
         if (GATED) {
           wait_bar(sm, B_PLAN + ((n + 1) & 3), ((n + 1) >> 2) & 1, 4);
           rs = sm.plan(n + 1)->rs;
         }
         wait_bar(sm, B_SQDONE, n & 1, 4);
-        tc_fence_after();
+      }
+      wait_bar(sm, B_SFULL, n & 1, 4);
+      tc_fence_after();
+      const float sig = GATED ? sm.plan(n)->sig : 1.f;  // sigma of S~ in TMEM now
+      if (n + 1 < NT) {
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t r[64], pk[32];
