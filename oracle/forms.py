@@ -306,3 +306,32 @@ def product_expansion(q, k, v, beta, S0=None):
         S = P.T @ S0 + Hm.T
         o[r] = S.T @ q[r]
     return o, S
+
+
+# --------------------------------------------------------------------------
+# input prologue ([DP] §2.2; [DR] §3 layer design)
+# --------------------------------------------------------------------------
+def silu(x):
+    """psi of [DP] §2.2 (SiLU): x * sigmoid(x)."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def prologue(q_raw, k_raw, beta_raw, beta_map="sigmoid"):
+    """The inputs of the recurrence from raw projections, [DP] §2.2: each key
+    (and, per the [DR] §3 layer design, each query) is psi(.) / ||psi(.)||_2
+    over the key dimension with psi = SiLU, and beta = phi(.) with phi =
+    sigmoid, or 2 sigmoid (so that beta reaches (0, 2): reflections).  The
+    last axis of q_raw and k_raw is the key dimension; beta_raw is
+    elementwise.  Reading: a vector whose SiLU is all zero (it has no
+    direction) maps to the zero vector."""
+    def unit(x):
+        y = silu(x)
+        n = np.sqrt(np.sum(y * y, axis=-1, keepdims=True))
+        return np.divide(y, n, out=np.zeros_like(y), where=n > 0)
+    b = 1.0 / (1.0 + np.exp(-np.asarray(beta_raw, dtype=np.float64)))
+    if beta_map == "2sigmoid":
+        b = 2.0 * b
+    elif beta_map != "sigmoid":
+        raise ValueError(f"beta_map {beta_map!r} is not 'sigmoid' or '2sigmoid'")
+    return unit(q_raw), unit(k_raw), b
