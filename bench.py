@@ -569,6 +569,49 @@ def measure_diagnostics(wr, dev, args):
     return out
 
 
+def measure_prologue(wr, dev, args, peaks):
+    """The input prologue on the headline workload's shapes, timed with CUDA
+    events: raw q and k ~ N(0, 1) (bf16) and raw beta ~ N(0, 1) through
+    SiLU + L2 norm and sigmoid on their own (``delta_prologue``, one pass over
+    HBM), and the forward on raw inputs (``delta_fwd_prologue``) beside the
+    forward on the same tensors taken as already normalised (``delta_fwd``)."""
+    stream = torch.cuda.current_stream(dev)
+    w = synth.WORKLOADS[HEADLINE]
+    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 11)
+    rn = lambda *shape: torch.randn(shape, generator=gen, device=dev)
+    q, k, v = (rn(B, T, H, d).to(torch.bfloat16) for d in (dk, dk, dv))
+    beta = rn(B, T, H)
+    g = torch.sigmoid(rn(B, T, H) * 2.0 + 3.0)
+    h0 = rn(B, H, dk, dv) * w.h0_std
+    out = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=dev)
+    hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+
+    pro_us = timed(lambda: wr.delta_prologue(q, k, beta))
+    fwdp_us = timed(lambda: wr.delta_fwd_prologue(q, k, v, beta, g, h0, out, hT))
+    fwd_us = timed(lambda: wr.delta_fwd(q, k, v, beta, g, h0, out, hT))
+    nbytes = 2 * (q.numel() * 2 + k.numel() * 2 + beta.numel() * 4)  # read once, write once
+    hbm = float(peaks["hbm_gbs"])
+    return {"workload": w.name, "input": "raw q, k ~ N(0,1) bf16, raw beta ~ N(0,1), sigmoid",
+            "prologue_us": pro_us, "bytes_per_call": nbytes,
+            "gbs": nbytes / (pro_us * 1e-6) / 1e9,
+            "frac_of_measured_hbm": nbytes / (pro_us * 1e-6) / 1e9 / hbm,
+            "fwd_prologue_ms": fwdp_us / 1e3, "fwd_ms": fwd_us / 1e3}
+
+
 def run_ours(args, dist):
     import weight_rnn_gb300 as wr
 
@@ -593,6 +636,8 @@ def run_ours(args, dist):
     head_id = ids[0]
     head = recs[head_id]
     diagnostics = measure_diagnostics(wr, dev, args) if args.workload == "all" else None
+    prologue = (measure_prologue(wr, dev, args, peaks)
+                if args.workload == "all" and not args.batch else None)
     w = synth.WORKLOADS[head_id]
     if args.batch:
         w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
@@ -613,6 +658,7 @@ def run_ours(args, dist):
         "gpu_launches": head["gpu_launches"],
         "gpu": torch.cuda.get_device_name(dev),
         "diagnostics": diagnostics,
+        "prologue": prologue,
         "per_workload": {
             recs[i]["workload"]: {
                 "value": recs[i]["value"], "unit": UNIT,

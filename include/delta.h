@@ -73,6 +73,12 @@ typedef enum {
     DELTA_BF16 = 1  /* q, k, v, out are bfloat16 (outputs rounded to nearest even) */
 } delta_dtype;
 
+/* phi of "DeltaProduct" §2.2, the map from a raw projection to beta */
+typedef enum {
+    DELTA_BETA_SIGMOID = 0,  /* beta = sigmoid(x), in (0, 1) */
+    DELTA_BETA_2SIGMOID = 1  /* beta = 2 sigmoid(x), in (0, 2): reflections allowed */
+} delta_beta_map;
+
 /*
  * delta_fwd -- chunked forward over a whole sequence.
  *
@@ -102,6 +108,54 @@ int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
               const float *g, const float *h0, void *out, float *hT,
               int B, int H, int T, int dk, int dv, int n_h, int chunk,
               delta_dtype dtype, struct CUstream_st *stream);
+
+/*
+ * delta_prologue -- the input prologue on its own: the keys of "DeltaProduct"
+ * §2.2, k = psi(x) / ||psi(x)||_2 over the key dimension with psi = SiLU,
+ * the queries likewise (the query path of the layer design in "08 · linear
+ * 路线（三）" §3: SiLU, then L2 norm), and beta = phi(x), phi = sigmoid or
+ * 2 sigmoid.  A vector whose SiLU is all zero becomes the zero vector.
+ *
+ *   q_raw    [B, T, H, dk]       dtype   in    q_out    same shape, dtype   out
+ *   k_raw    [B, T, n_h, H, dk]  dtype   in    k_out    same shape, dtype   out
+ *   beta_raw [B, T, n_h, H]      float32 in    beta_out same shape, float32 out
+ *
+ * One kernel, one read of each input and one write of each output, float32
+ * arithmetic (outputs rounded to dtype, nearest even).  All buffers are
+ * caller-owned device memory, 16-byte aligned; no output may overlap an input
+ * or another output (DELTA_ERR_INVALID).  dk must be in {16, 32, 64, 128}.
+ */
+int delta_prologue(const void *q_raw, const void *k_raw, const float *beta_raw,
+                   void *q_out, void *k_out, float *beta_out, int B, int H, int T, int dk,
+                   int n_h, delta_dtype dtype, delta_beta_map beta_map,
+                   struct CUstream_st *stream);
+
+/*
+ * delta_fwd_prologue -- delta_fwd on raw projections: first the input
+ * prologue of "DeltaProduct" §2.2 (each key k = psi(x) / ||psi(x)||_2 over
+ * the key dimension with psi = SiLU, beta = phi(x) with phi = sigmoid or
+ * 2 sigmoid) with the query path of the layer design in "08 · linear 路线
+ * （三）" §3 (SiLU, then the same L2 norm), then delta_fwd on the results.
+ *
+ *   q_raw    [B, T, H, dk]       dtype   raw query projections
+ *   k_raw    [B, T, n_h, H, dk]  dtype   raw key projections
+ *   beta_raw [B, T, n_h, H]      float32 raw beta projections
+ *   beta_map                      DELTA_BETA_SIGMOID or DELTA_BETA_2SIGMOID
+ *   everything else               as in delta_fwd
+ *
+ * A key or query whose SiLU is all zero is used as the zero vector.  The
+ * prologue is delta_prologue's kernel: a single read of q_raw, k_raw and
+ * beta_raw and a single write of the normalised q and k (in dtype) and of
+ * beta (float32) into stream-ordered scratch from the pool delta_fwd uses (B*H*(T + n_h*T)
+ * *dk*sizeof(dtype) + B*H*n_h*T*4 bytes, 256-byte rounded per part),
+ * released before the call returns.  Errors as in delta_fwd, plus
+ * DELTA_ERR_INVALID for an unknown beta_map.
+ */
+int delta_fwd_prologue(const void *q_raw, const void *k_raw, const void *v,
+                       const float *beta_raw, const float *g, const float *h0, void *out,
+                       float *hT, int B, int H, int T, int dk, int dv, int n_h, int chunk,
+                       delta_dtype dtype, delta_beta_map beta_map,
+                       struct CUstream_st *stream);
 
 /*
  * delta_fwd_static_scratch -- delta_fwd for callers that cannot allocate
@@ -192,6 +246,19 @@ int delta_step(const void *q, const void *k, const void *v, const float *beta,
                delta_dtype dtype, struct CUstream_st *stream);
 
 /*
+ * delta_step_prologue -- delta_step on raw projections, with the input
+ * prologue of delta_fwd_prologue ("DeltaProduct" §2.2; "08 · linear 路线
+ * （三）" §3) applied inside the decode kernel: q_raw, k_raw and beta_raw
+ * take the places of q, k and beta (same shapes and types), beta_map picks
+ * phi.  No extra pass over memory and no scratch.  Errors as in delta_step,
+ * plus DELTA_ERR_INVALID for an unknown beta_map.
+ */
+int delta_step_prologue(const void *q_raw, const void *k_raw, const void *v,
+                        const float *beta_raw, const float *g, float *state, void *out,
+                        int B, int H, int dk, int dv, int n_h, delta_dtype dtype,
+                        delta_beta_map beta_map, struct CUstream_st *stream);
+
+/*
  * delta_state_erank -- the effective rank of each state matrix, the spectral
  * diagnostic of "DeltaProduct" §4.6:
  *
@@ -266,8 +333,9 @@ int delta_version(void);
 
 /*
  * delta_inject_failure -- test hook: the next `count` calls of delta_fwd,
- * delta_ut_transform, delta_fwd_with_ut, delta_step, delta_state_erank and
- * delta_attention_map (together) return DELTA_ERR_CUDA, with "injected failure" in
+ * delta_prologue, delta_fwd_prologue, delta_ut_transform, delta_fwd_with_ut, delta_step,
+ * delta_step_prologue, delta_state_erank and delta_attention_map (together)
+ * return DELTA_ERR_CUDA, with "injected failure" in
  * delta_last_error(), right after their arguments pass validation and before
  * anything is enqueued.  count = 0 clears a pending injection; count < 0 is
  * DELTA_ERR_INVALID.  The counter is process-wide.

@@ -237,3 +237,86 @@ def test_attention_map_rejects_bad_arguments(lib):
     assert call(None, P[1], P[2], None, P[4], 1, 1, 8, 128, wr.DELTA_BF16, None) == wr.DELTA_ERR_INVALID
     assert call(P[0], P[1], P[2], None, P[0], 1, 1, 8, 128, wr.DELTA_BF16, None) == wr.DELTA_ERR_INVALID
     assert call(P[0], P[1], P[2], None, P[4], 1, 1, 0, 128, wr.DELTA_BF16, None) == wr.DELTA_OK
+
+
+def fwd_prologue(lib, beta_map=0, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, beta=FAKE * 4, g=None, h0=None,
+             out=FAKE * 5, hT=None, B=1, H=1, T=4, dk=16, dv=16, n_h=1, chunk=16,
+             dtype=wr.DELTA_F32)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_fwd_prologue(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["beta"]), vp(a["g"]),
+                                  vp(a["h0"]), vp(a["out"]), vp(a["hT"]), a["B"], a["H"], a["T"],
+                                  a["dk"], a["dv"], a["n_h"], a["chunk"], a["dtype"], beta_map,
+                                  None)
+
+
+def step_prologue(lib, beta_map=0, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, beta=FAKE * 4, g=None, state=FAKE * 5,
+             out=FAKE * 6, B=1, H=1, dk=16, dv=16, n_h=1, dtype=wr.DELTA_F32)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_step_prologue(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["beta"]),
+                                   vp(a["g"]), vp(a["state"]), vp(a["out"]), a["B"], a["H"],
+                                   a["dk"], a["dv"], a["n_h"], a["dtype"], beta_map, None)
+
+
+@pytest.mark.parametrize("beta_map,kw,status", [
+    (2, {}, wr.DELTA_ERR_INVALID),                       # unknown beta map
+    (-1, {}, wr.DELTA_ERR_INVALID),
+    (0, dict(dk=48), wr.DELTA_ERR_UNSUPPORTED),
+    (1, dict(k=FAKE + 8), wr.DELTA_ERR_ALIGN),
+    (1, dict(out=FAKE + 16), wr.DELTA_ERR_INVALID),      # out overlaps q_raw
+    (0, dict(beta=None), wr.DELTA_ERR_INVALID),
+])
+def test_prologue_entry_points_reject_before_launch(lib, beta_map, kw, status):
+    assert fwd_prologue(lib, beta_map, **kw) == status
+    step_kw = {k: v for k, v in kw.items() if k in ("dk", "k", "beta")}
+    if "out" in kw:
+        step_kw["out"] = FAKE + 32
+    assert step_prologue(lib, beta_map, **step_kw) == status
+
+
+def test_prologue_empty_problems_are_ok_without_gpu(lib):
+    assert fwd_prologue(lib, 1, B=0) == wr.DELTA_OK
+    assert step_prologue(lib, 1, H=0) == wr.DELTA_OK
+
+
+def test_binding_rejects_unknown_beta_map():
+    import torch
+    q = torch.zeros(1, 4, 1, 16)
+    with pytest.raises(ValueError):
+        wr.delta_fwd_prologue(q, q, q, torch.zeros(1, 4, 1), beta_map="tanh")
+    with pytest.raises(ValueError):
+        wr.delta_step_prologue(q[:, 0], q[:, :1], q[:, :1], torch.zeros(1, 1, 1), None,
+                               torch.zeros(1, 1, 16, 16), beta_map="relu")
+
+
+def prologue(lib, beta_map=0, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, beta=FAKE * 3, qo=FAKE * 4, ko=FAKE * 5, bo=FAKE * 6,
+             B=1, H=1, T=4, dk=16, n_h=1, dtype=wr.DELTA_F32)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_prologue(vp(a["q"]), vp(a["k"]), vp(a["beta"]), vp(a["qo"]), vp(a["ko"]),
+                              vp(a["bo"]), a["B"], a["H"], a["T"], a["dk"], a["n_h"], a["dtype"],
+                              beta_map, None)
+
+
+@pytest.mark.parametrize("beta_map,kw,status", [
+    (5, {}, wr.DELTA_ERR_INVALID),
+    (0, dict(dk=24), wr.DELTA_ERR_UNSUPPORTED),
+    (0, dict(n_h=0), wr.DELTA_ERR_UNSUPPORTED),
+    (1, dict(T=-1), wr.DELTA_ERR_INVALID),
+    (1, dict(dtype=3), wr.DELTA_ERR_INVALID),
+    (0, dict(ko=None), wr.DELTA_ERR_INVALID),
+    (0, dict(bo=FAKE * 6 + 4), wr.DELTA_ERR_ALIGN),
+    (0, dict(qo=FAKE * 2 + 32), wr.DELTA_ERR_INVALID),   # q_out overlaps k_raw
+    (1, dict(ko=FAKE * 4 + 16), wr.DELTA_ERR_INVALID),   # k_out overlaps q_out
+])
+def test_prologue_rejects_before_launch(lib, beta_map, kw, status):
+    assert prologue(lib, beta_map, **kw) == status
+
+
+def test_prologue_empty_is_ok_without_gpu(lib):
+    assert prologue(lib, 0, T=0) == wr.DELTA_OK
+    assert prologue(lib, 1, B=0, q=None, k=None) == wr.DELTA_OK

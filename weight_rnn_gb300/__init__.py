@@ -15,14 +15,15 @@ import threading
 
 import torch
 
-__all__ = ["delta_fwd", "delta_fwd_static_scratch", "delta_state_erank",
+__all__ = ["delta_fwd", "delta_prologue", "delta_fwd_prologue", "delta_step_prologue",
+           "delta_fwd_static_scratch", "delta_state_erank",
            "delta_attention_map", "delta_ut_transform", "delta_fwd_with_ut", "delta_step",
            "fwd_launches", "delta_status_string", "delta_last_error",
            "delta_check_device", "delta_inject_failure", "delta_selftest_wait",
            "delta_version", "DeltaError", "library_path", "load_library",
            "DELTA_OK", "DELTA_ERR_INVALID", "DELTA_ERR_UNSUPPORTED",
            "DELTA_ERR_ALIGN", "DELTA_ERR_CUDA", "DELTA_F32", "DELTA_BF16",
-           "EXPORTED_SYMBOLS"]
+           "DELTA_BETA_SIGMOID", "DELTA_BETA_2SIGMOID", "EXPORTED_SYMBOLS"]
 
 DELTA_OK = 0
 DELTA_ERR_INVALID = -1
@@ -31,11 +32,15 @@ DELTA_ERR_ALIGN = -3
 DELTA_ERR_CUDA = -4
 DELTA_F32 = 0
 DELTA_BF16 = 1
+DELTA_BETA_SIGMOID = 0
+DELTA_BETA_2SIGMOID = 1
+_BETA_MAPS = {"sigmoid": DELTA_BETA_SIGMOID, "2sigmoid": DELTA_BETA_2SIGMOID}
 
 #: every extern "C" entry point include/delta.h declares
-EXPORTED_SYMBOLS = ("delta_fwd", "delta_fwd_static_scratch", "delta_ut_transform",
-                    "delta_fwd_with_ut",
-                    "delta_fwd_kernel_count", "delta_step", "delta_status_string",
+EXPORTED_SYMBOLS = ("delta_fwd", "delta_prologue", "delta_fwd_prologue", "delta_fwd_static_scratch",
+                    "delta_ut_transform", "delta_fwd_with_ut",
+                    "delta_fwd_kernel_count", "delta_step", "delta_step_prologue",
+                    "delta_status_string",
                     "delta_last_error", "delta_check_device", "delta_version",
                     "delta_inject_failure", "delta_selftest_wait", "delta_state_erank",
                     "delta_attention_map")
@@ -72,6 +77,10 @@ def load_library():
         p, i = ctypes.c_void_p, ctypes.c_int
         lib.delta_fwd.restype = i
         lib.delta_fwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.delta_prologue.restype = i
+        lib.delta_prologue.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, p]
+        lib.delta_fwd_prologue.restype = i
+        lib.delta_fwd_prologue.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, i, p]
         lib.delta_fwd_static_scratch.restype = i
         lib.delta_fwd_static_scratch.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
         lib.delta_state_erank.restype = i
@@ -86,6 +95,8 @@ def load_library():
         lib.delta_fwd_kernel_count.argtypes = [i, i, i, i, i, i, i, i]
         lib.delta_step.restype = i
         lib.delta_step.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, p]
+        lib.delta_step_prologue.restype = i
+        lib.delta_step_prologue.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, p]
         lib.delta_status_string.restype = ctypes.c_char_p
         lib.delta_status_string.argtypes = [i]
         lib.delta_last_error.restype = ctypes.c_char_p
@@ -211,6 +222,82 @@ def delta_fwd(q, k, v, beta, g=None, h0=None, out=None, hT=None, *, n_h=1,
     st = lib.delta_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
                        _ptr(out), _ptr(hT), B, H, T, dk, dv, n_h, chunk, code,
                        _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return out, hT
+
+
+def _beta_map(beta_map):
+    if beta_map not in _BETA_MAPS:
+        raise ValueError(f"beta_map {beta_map!r} is not 'sigmoid' or '2sigmoid'")
+    return _BETA_MAPS[beta_map]
+
+
+def delta_prologue(q_raw, k_raw, beta_raw, *, n_h=1, beta_map="sigmoid", stream=None):
+    """The input prologue on its own (``delta_prologue``): returns
+    ``(q, k, beta)`` with q and k through SiLU and an L2 norm over the key
+    dimension (in the input dtype) and beta through ``beta_map`` (float32).
+    q_raw [B,T,H,dk]; k_raw [B,T,n_h,H,dk] (or [B,T,H,dk] when n_h = 1);
+    beta_raw [B,T,n_h,H] (or [B,T,H]) float32."""
+    lib = load_library()
+    code_map = _beta_map(beta_map)
+    B, T, H, dk = q_raw.shape
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise ValueError("delta_prologue needs CUDA tensors")
+    dt = q_raw.dtype
+    code = _dtype_code(dt)
+    if n_h == 1 and k_raw.dim() == 4:
+        kshape, bshape = (B, T, H, dk), (B, T, H)
+    else:
+        kshape, bshape = (B, T, n_h, H, dk), (B, T, n_h, H)
+    _check(q_raw, "q_raw", (B, T, H, dk), dt, dev)
+    _check(k_raw, "k_raw", kshape, dt, dev)
+    _check(beta_raw, "beta_raw", bshape, torch.float32, dev)
+    q = torch.empty_like(q_raw)
+    k = torch.empty_like(k_raw)
+    beta = torch.empty_like(beta_raw)
+    st = lib.delta_prologue(_ptr(q_raw), _ptr(k_raw), _ptr(beta_raw), _ptr(q), _ptr(k), _ptr(beta),
+                            B, H, T, dk, n_h, code, code_map, _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return q, k, beta
+
+
+def delta_fwd_prologue(q_raw, k_raw, v, beta_raw, g=None, h0=None, out=None, hT=None, *,
+                       n_h=1, chunk=64, beta_map="sigmoid", want_state=True, stream=None):
+    """``delta_fwd`` on raw projections (``delta_fwd_prologue``): q and k go
+    through SiLU and an L2 norm over the key dimension, beta through
+    ``beta_map`` ('sigmoid' or '2sigmoid'), then the forward.  Shapes and
+    results as in ``delta_fwd``."""
+    lib = load_library()
+    code_map = _beta_map(beta_map)
+    B, T, H, dk = q_raw.shape
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise ValueError("delta_fwd_prologue needs CUDA tensors")
+    dt = q_raw.dtype
+    code = _dtype_code(dt)
+    if n_h == 1 and k_raw.dim() == 4:
+        kshape, vshape, bshape = (B, T, H, dk), (B, T, H, v.shape[-1]), (B, T, H)
+    else:
+        kshape, vshape, bshape = (B, T, n_h, H, dk), (B, T, n_h, H, v.shape[-1]), (B, T, n_h, H)
+    dv = v.shape[-1]
+    _check(q_raw, "q_raw", (B, T, H, dk), dt, dev)
+    _check(k_raw, "k_raw", kshape, dt, dev)
+    _check(v, "v", vshape, dt, dev)
+    _check(beta_raw, "beta_raw", bshape, torch.float32, dev)
+    _check(g, "g", (B, T, H), torch.float32, dev)
+    _check(h0, "h0", (B, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=dt, device=dev)
+    _check(out, "out", (B, T, H, dv), dt, dev)
+    if hT is None and want_state:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(hT, "hT", (B, H, dk, dv), torch.float32, dev)
+    st = lib.delta_fwd_prologue(_ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(beta_raw), _ptr(g),
+                                _ptr(h0), _ptr(out), _ptr(hT), B, H, T, dk, dv, n_h, chunk,
+                                code, code_map, _stream(dev, stream))
     if st != DELTA_OK:
         raise DeltaError(st, delta_last_error())
     return out, hT
@@ -402,6 +489,37 @@ def delta_step(q, k, v, beta, g, state, out=None, *, n_h=1, stream=None):
     _check(out, "out", (B, H, dv), dt, dev)
     st = lib.delta_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(state),
                         _ptr(out), B, H, dk, dv, n_h, code, _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return out
+
+
+def delta_step_prologue(q_raw, k_raw, v, beta_raw, g, state, out=None, *, n_h=1,
+                        beta_map="sigmoid", stream=None):
+    """``delta_step`` on raw projections (``delta_step_prologue``): the input
+    prologue of ``delta_fwd_prologue`` runs inside the decode kernel.  Shapes
+    and results as in ``delta_step``."""
+    lib = load_library()
+    code_map = _beta_map(beta_map)
+    B, H, dk = q_raw.shape
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise ValueError("delta_step_prologue needs CUDA tensors")
+    dt = q_raw.dtype
+    code = _dtype_code(dt)
+    dv = v.shape[-1]
+    _check(q_raw, "q_raw", (B, H, dk), dt, dev)
+    _check(k_raw, "k_raw", (B, n_h, H, dk), dt, dev)
+    _check(v, "v", (B, n_h, H, dv), dt, dev)
+    _check(beta_raw, "beta_raw", (B, n_h, H), torch.float32, dev)
+    _check(g, "g", (B, H), torch.float32, dev)
+    _check(state, "state", (B, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=dt, device=dev)
+    _check(out, "out", (B, H, dv), dt, dev)
+    st = lib.delta_step_prologue(_ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(beta_raw), _ptr(g),
+                                 _ptr(state), _ptr(out), B, H, dk, dv, n_h, code, code_map,
+                                 _stream(dev, stream))
     if st != DELTA_OK:
         raise DeltaError(st, delta_last_error())
     return out

@@ -185,6 +185,133 @@ int validate_t_mat(const delta::FwdArgs &a, const void *t_mat, bool with_outputs
   return DELTA_OK;
 }
 
+// The forward of a validated call (B*H > 0): the tensor-core path with its
+// T-tile scratch, the state pass-through for T = 0, or the generic kernel.
+int run_fwd(const delta::FwdArgs &a, cudaStream_t s) {
+  cudaError_t err;
+  if (a.T == 0) {
+    err = delta::launch_state_passthrough(a, s);
+    return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "state passthrough launch");
+  }
+  if (delta::chunk_tc_supports(a)) {
+    // the T tiles of every chunk live in stream-ordered scratch between the
+    // two passes and are released (stream-ordered) after the second
+    cudaMemPool_t pool;
+    if ((err = scratch_pool(&pool)) != cudaSuccess) return cuda_fail(err, "scratch pool");
+    void *t_mat = nullptr;
+    err = cudaMallocFromPoolAsync(&t_mat, (size_t)delta::ut_workspace_bytes(a), pool, s);
+    if (err != cudaSuccess) return cuda_fail(err, "scratch allocation");
+    err = delta::launch_ut(a, t_mat, s);
+    const char *what = "UT-pass kernel launch";
+    if (err == cudaSuccess) {
+      err = delta::launch_chunk_tc(a, t_mat, s);
+      what = "tensor-core chunk kernel launch";
+    }
+    const cudaError_t ef = cudaFreeAsync(t_mat, s);
+    if (err != cudaSuccess) return cuda_fail(err, what);
+    return ef == cudaSuccess ? DELTA_OK : cuda_fail(ef, "scratch release");
+  }
+  err = delta::launch_chunk_generic(a, s);
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "generic chunk kernel launch");
+}
+
+// Checks of delta_prologue's arguments (rows of q and k, betas).
+int validate_prologue(const void *q_raw, const void *k_raw, const float *beta_raw, void *q_out,
+                      void *k_out, float *beta_out, int B, int H, int T, int dk, int n_h,
+                      delta_dtype dtype, delta_beta_map beta_map) {
+  if (beta_map != DELTA_BETA_SIGMOID && beta_map != DELTA_BETA_2SIGMOID)
+    return fail(DELTA_ERR_INVALID, "unknown beta_map %d", (int)beta_map);
+  if (B < 0 || H < 0 || T < 0)
+    return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d T=%d", B, H, T);
+  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
+    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (!supported_dim(dk)) return fail(DELTA_ERR_UNSUPPORTED, "dk=%d not in {16,32,64,128}", dk);
+  if (n_h < 1 || n_h > 4) return fail(DELTA_ERR_UNSUPPORTED, "n_h=%d not in [1,4]", n_h);
+  const int64_t BH = (int64_t)B * H, esz = dtype == DELTA_BF16 ? 2 : 4;
+  if (BH * T == 0) return DELTA_OK;
+  if (!q_raw || !k_raw || !beta_raw || !q_out || !k_out || !beta_out)
+    return fail(DELTA_ERR_INVALID, "every pointer must be non-NULL");
+  if (!aligned16(q_raw) || !aligned16(k_raw) || !aligned16(beta_raw) || !aligned16(q_out) ||
+      !aligned16(k_out) || !aligned16(beta_out))
+    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+  const int64_t L = (int64_t)T * n_h;
+  const Range outs[] = {range(q_out, BH * T * dk * esz), range(k_out, BH * L * dk * esz),
+                        range(beta_out, BH * L * 4)};
+  const Range ins[] = {range(q_raw, BH * T * dk * esz), range(k_raw, BH * L * dk * esz),
+                       range(beta_raw, BH * L * 4)};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlap(outs[i], ins[j])) return fail(DELTA_ERR_INVALID, "an output overlaps an input");
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i], outs[j])) return fail(DELTA_ERR_INVALID, "two outputs overlap");
+  }
+  return DELTA_OK;
+}
+
+delta::PrologueArgs prologue_args(const void *q_raw, const void *k_raw, const float *beta_raw,
+                                  void *q_out, void *k_out, float *beta_out, int64_t BH, int64_t T,
+                                  int dk, int n_h, bool bf16, delta_beta_map beta_map) {
+  delta::PrologueArgs p;
+  p.q = q_raw; p.k = k_raw; p.beta = beta_raw;
+  p.q_out = q_out; p.k_out = k_out; p.beta_out = beta_out;
+  p.rows_q = BH * T; p.rows_k = BH * T * n_h; p.n_beta = BH * T * n_h;
+  p.dk = dk; p.beta_map = beta_map == DELTA_BETA_2SIGMOID ? 1 : 0; p.bf16 = bf16;
+  return p;
+}
+
+// Checks of delta_step's arguments.
+int validate_step(const void *q, const void *k, const void *v, const float *beta,
+                  const float *g, float *state, void *out, int B, int H, int dk, int dv,
+                  int n_h, delta_dtype dtype) {
+  if (B < 0 || H < 0) return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d", B, H);
+  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
+    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (!supported_dim(dk) || !supported_dim(dv))
+    return fail(DELTA_ERR_UNSUPPORTED, "dk=%d dv=%d not in {16,32,64,128}", dk, dv);
+  if (n_h < 1 || n_h > 4) return fail(DELTA_ERR_UNSUPPORTED, "n_h=%d not in [1,4]", n_h);
+  if ((int64_t)B * H >= (int64_t(1) << 31))
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
+  const int64_t BH = (int64_t)B * H;
+  if (BH == 0) return DELTA_OK;
+  // one CTA per (b, h) and 32-column slab of the state: the grid must fit
+  // gridDim.x
+  if (BH * (dv < 32 ? 1 : dv / 32) > INT32_MAX)
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H*(dv/32)=%lld blocks exceed 2^31-1",
+                (long long)(BH * (dv < 32 ? 1 : dv / 32)));
+  if (!q || !k || !v || !beta || !state || !out)
+    return fail(DELTA_ERR_INVALID, "q, k, v, beta, state and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) ||
+      !aligned16(g) || !aligned16(state) || !aligned16(out))
+    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+  const int64_t esz = dtype == DELTA_BF16 ? 2 : 4;
+  const Range r_state = range(state, BH * dk * dv * 4);
+  const Range r_out = range(out, BH * dv * esz);
+  const Range inputs[] = {range(q, BH * dk * esz), range(k, BH * n_h * dk * esz),
+                          range(v, BH * n_h * dv * esz), range(beta, BH * n_h * 4),
+                          range(g, g ? BH * 4 : 0)};
+  for (const Range &r : inputs) {
+    if (overlap(r_out, r)) return fail(DELTA_ERR_INVALID, "out overlaps an input");
+    if (overlap(r_state, r)) return fail(DELTA_ERR_INVALID, "state overlaps an input");
+  }
+  if (overlap(r_state, r_out)) return fail(DELTA_ERR_INVALID, "state overlaps out");
+  return DELTA_OK;
+}
+
+int run_step(const void *q, const void *k, const void *v, const float *beta, const float *g,
+             float *state, void *out, int B, int H, int dk, int dv, int n_h, delta_dtype dtype,
+             int beta_map, struct CUstream_st *stream) {
+  const int st = validate_step(q, k, v, beta, g, state, out, B, H, dk, dv, n_h, dtype);
+  if (st != DELTA_OK || (int64_t)B * H == 0) return st;
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+  delta::StepArgs a;
+  a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.state = state; a.out = out;
+  a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.n_h = n_h;
+  a.bf16 = dtype == DELTA_BF16;
+  a.beta_map = beta_map;
+  const cudaError_t err = delta::launch_step(a, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "decode step launch");
+}
+
 }  // namespace
 
 extern "C" {
@@ -240,33 +367,62 @@ int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
   const int st = validate_fwd(q, k, v, beta, g, h0, out, hT, B, H, T, dk, dv, n_h, chunk, dtype, a);
   if (st != DELTA_OK || a.B * a.H == 0) return st;
   if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return run_fwd(a, reinterpret_cast<cudaStream_t>(stream));
+}
 
-  cudaError_t err;
-  if (T == 0) {
-    err = delta::launch_state_passthrough(a, s);
-    return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "state passthrough launch");
+int delta_fwd_prologue(const void *q_raw, const void *k_raw, const void *v, const float *beta_raw,
+                       const float *g, const float *h0, void *out, float *hT, int B, int H,
+                       int T, int dk, int dv, int n_h, int chunk, delta_dtype dtype,
+                       delta_beta_map beta_map, struct CUstream_st *stream) {
+  if (beta_map != DELTA_BETA_SIGMOID && beta_map != DELTA_BETA_2SIGMOID)
+    return fail(DELTA_ERR_INVALID, "unknown beta_map %d", (int)beta_map);
+  delta::FwdArgs a;
+  const int st = validate_fwd(q_raw, k_raw, v, beta_raw, g, h0, out, hT, B, H, T, dk, dv, n_h,
+                              chunk, dtype, a);
+  if (st != DELTA_OK || a.B * a.H == 0) return st;
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) return run_fwd(a, s);
+  // the normalised q and k and the mapped beta, in stream-ordered scratch
+  // (one allocation, 256-byte aligned parts), released after the forward
+  const int64_t BH = a.B * a.H, esz = a.bf16 ? 2 : 4;
+  const auto up = [](int64_t n) { return (n + 255) & ~int64_t(255); };
+  const int64_t bq = up(BH * a.T * dk * esz), bk = up(BH * a.L * dk * esz), bb = up(BH * a.L * 4);
+  cudaMemPool_t pool;
+  cudaError_t err = scratch_pool(&pool);
+  if (err != cudaSuccess) return cuda_fail(err, "scratch pool");
+  void *scratch = nullptr;
+  err = cudaMallocFromPoolAsync(&scratch, (size_t)(bq + bk + bb), pool, s);
+  if (err != cudaSuccess) return cuda_fail(err, "scratch allocation");
+  uint8_t *base = static_cast<uint8_t *>(scratch);
+  const delta::PrologueArgs p =
+      prologue_args(q_raw, k_raw, beta_raw, base, base + bq,
+                    reinterpret_cast<float *>(base + bq + bk), BH, a.T, dk, n_h, a.bf16, beta_map);
+  err = delta::launch_prologue(p, s);
+  int rc = DELTA_OK;
+  if (err != cudaSuccess) {
+    rc = cuda_fail(err, "prologue kernel launch");
+  } else {
+    a.q = p.q_out; a.k = p.k_out; a.beta = p.beta_out;
+    rc = run_fwd(a, s);
   }
-  if (delta::chunk_tc_supports(a)) {
-    // the T tiles of every chunk live in stream-ordered scratch between the
-    // two passes and are released (stream-ordered) after the second
-    cudaMemPool_t pool;
-    if ((err = scratch_pool(&pool)) != cudaSuccess) return cuda_fail(err, "scratch pool");
-    void *t_mat = nullptr;
-    err = cudaMallocFromPoolAsync(&t_mat, (size_t)delta::ut_workspace_bytes(a), pool, s);
-    if (err != cudaSuccess) return cuda_fail(err, "scratch allocation");
-    err = delta::launch_ut(a, t_mat, s);
-    const char *what = "UT-pass kernel launch";
-    if (err == cudaSuccess) {
-      err = delta::launch_chunk_tc(a, t_mat, s);
-      what = "tensor-core chunk kernel launch";
-    }
-    const cudaError_t ef = cudaFreeAsync(t_mat, s);
-    if (err != cudaSuccess) return cuda_fail(err, what);
-    return ef == cudaSuccess ? DELTA_OK : cuda_fail(ef, "scratch release");
-  }
-  err = delta::launch_chunk_generic(a, s);
-  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "generic chunk kernel launch");
+  const cudaError_t ef = cudaFreeAsync(scratch, s);
+  if (rc != DELTA_OK) return rc;
+  return ef == cudaSuccess ? DELTA_OK : cuda_fail(ef, "scratch release");
+}
+
+int delta_prologue(const void *q_raw, const void *k_raw, const float *beta_raw, void *q_out,
+                   void *k_out, float *beta_out, int B, int H, int T, int dk, int n_h,
+                   delta_dtype dtype, delta_beta_map beta_map, struct CUstream_st *stream) {
+  const int st = validate_prologue(q_raw, k_raw, beta_raw, q_out, k_out, beta_out, B, H, T, dk,
+                                   n_h, dtype, beta_map);
+  if (st != DELTA_OK || (int64_t)B * H * T == 0) return st;
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+  const delta::PrologueArgs p = prologue_args(q_raw, k_raw, beta_raw, q_out, k_out, beta_out,
+                                              (int64_t)B * H, T, dk, n_h, dtype == DELTA_BF16,
+                                              beta_map);
+  const cudaError_t err = delta::launch_prologue(p, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "prologue kernel launch");
 }
 
 int delta_fwd_static_scratch(const void *q, const void *k, const void *v, const float *beta,
@@ -409,46 +565,17 @@ int delta_fwd_kernel_count(int B, int H, int T, int dk, int dv, int n_h, int chu
 int delta_step(const void *q, const void *k, const void *v, const float *beta,
                const float *g, float *state, void *out, int B, int H, int dk, int dv,
                int n_h, delta_dtype dtype, struct CUstream_st *stream) {
-  if (B < 0 || H < 0) return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d", B, H);
-  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
-    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
-  if (!supported_dim(dk) || !supported_dim(dv))
-    return fail(DELTA_ERR_UNSUPPORTED, "dk=%d dv=%d not in {16,32,64,128}", dk, dv);
-  if (n_h < 1 || n_h > 4) return fail(DELTA_ERR_UNSUPPORTED, "n_h=%d not in [1,4]", n_h);
-  if ((int64_t)B * H >= (int64_t(1) << 31))
-    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
-  const int64_t BH = (int64_t)B * H;
-  if (BH == 0) return DELTA_OK;
-  // one CTA per (b, h) and 32-column slab of the state: the grid must fit
-  // gridDim.x
-  if (BH * (dv < 32 ? 1 : dv / 32) > INT32_MAX)
-    return fail(DELTA_ERR_UNSUPPORTED, "B*H*(dv/32)=%lld blocks exceed 2^31-1",
-                (long long)(BH * (dv < 32 ? 1 : dv / 32)));
-  if (!q || !k || !v || !beta || !state || !out)
-    return fail(DELTA_ERR_INVALID, "q, k, v, beta, state and out must be non-NULL");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) ||
-      !aligned16(g) || !aligned16(state) || !aligned16(out))
-    return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
-  const int64_t esz = dtype == DELTA_BF16 ? 2 : 4;
-  const Range r_state = range(state, BH * dk * dv * 4);
-  const Range r_out = range(out, BH * dv * esz);
-  const Range inputs[] = {range(q, BH * dk * esz), range(k, BH * n_h * dk * esz),
-                          range(v, BH * n_h * dv * esz), range(beta, BH * n_h * 4),
-                          range(g, g ? BH * 4 : 0)};
-  for (const Range &r : inputs) {
-    if (overlap(r_out, r)) return fail(DELTA_ERR_INVALID, "out overlaps an input");
-    if (overlap(r_state, r)) return fail(DELTA_ERR_INVALID, "state overlaps an input");
-  }
-  if (overlap(r_state, r_out)) return fail(DELTA_ERR_INVALID, "state overlaps out");
+  return run_step(q, k, v, beta, g, state, out, B, H, dk, dv, n_h, dtype, -1, stream);
+}
 
-  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
-
-  delta::StepArgs a;
-  a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.state = state; a.out = out;
-  a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.n_h = n_h;
-  a.bf16 = dtype == DELTA_BF16;
-  const cudaError_t err = delta::launch_step(a, reinterpret_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "decode step launch");
+int delta_step_prologue(const void *q_raw, const void *k_raw, const void *v, const float *beta_raw,
+                        const float *g, float *state, void *out, int B, int H, int dk, int dv,
+                        int n_h, delta_dtype dtype, delta_beta_map beta_map,
+                        struct CUstream_st *stream) {
+  if (beta_map != DELTA_BETA_SIGMOID && beta_map != DELTA_BETA_2SIGMOID)
+    return fail(DELTA_ERR_INVALID, "unknown beta_map %d", (int)beta_map);
+  return run_step(q_raw, k_raw, v, beta_raw, g, state, out, B, H, dk, dv, n_h, dtype,
+                  beta_map == DELTA_BETA_2SIGMOID ? 1 : 0, stream);
 }
 
 }  // extern "C"

@@ -27,7 +27,25 @@ struct StepArgs {
   int64_t B, H;
   int dk, dv, n_h;
   bool bf16;
+  // input prologue applied in the kernel: -1 none (q, k, beta as given);
+  // 0: q, k -> SiLU -> L2 norm, beta -> sigmoid; 1: the same, beta -> 2 sigmoid
+  int beta_map = -1;
 };
+
+// The input prologue as one pass over raw inputs: rows of dk elements
+// (rows_q query rows, then rows_k key rows) -> SiLU -> L2 norm, written to
+// q_out / k_out in the input dtype; n_beta betas -> sigmoid (beta_map 0) or
+// 2 sigmoid (beta_map 1), float32.
+struct PrologueArgs {
+  const void *q, *k;
+  const float *beta;
+  void *q_out, *k_out;
+  float *beta_out;
+  int64_t rows_q, rows_k, n_beta;
+  int dk, beta_map;
+  bool bf16;
+};
+cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t s);
 
 // Generic chunked forward on CUDA cores, float32 arithmetic, any supported
 // shape.  Returns the launch error (cudaSuccess if enqueued).

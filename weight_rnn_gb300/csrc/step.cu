@@ -25,6 +25,12 @@
 // several slices per SM be in their load phase while others compute and
 // store.  Loads and stores use the streaming cache hint: every byte of the
 // state is touched once per call.
+//
+// With the input prologue on (delta_step_prologue), the raw q and k of the
+// token go through SiLU and an L2 norm over the key index and beta through
+// sigmoid or 2 sigmoid ("DeltaProduct" §2.2; the query path of the layer
+// design in "08 · linear 路线（三）" §3) in shared memory, before any of the
+// above: no extra pass over HBM.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -49,6 +55,8 @@ __device__ __forceinline__ void store_io(void *p, int64_t i, float x, bool bf16)
     static_cast<float *>(p)[i] = x;
 }
 
+__device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
+
 template <int NH>
 __global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
   __shared__ float s_k[NH][kMaxD];
@@ -58,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
   __shared__ float s_r[NH + 1][kSlab];
   __shared__ float s_beta[NH];
   __shared__ float s_dot[NH + 1][NH];  // [i][j] = k_i.k_j (i<j); [NH][j] = k_j.q
+  __shared__ float s_inv[NH + 1];      // prologue: 1 / ||SiLU(k_j)||, 1 / ||SiLU(q)||
   // partial sums per row group: (NH + 1) x RG x SW floats, RG * SW == 4 * kThreads
   // (written as float4: 16-byte alignment)
   __shared__ __align__(16) float s_part[(NH + 1) * 4 * kThreads];
@@ -93,9 +102,36 @@ __global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
     const int j = i / SW, c = i % SW;
     s_v[j][c] = load_io(a.v, ((b * NH + j) * H + h) * dv + cbase + c, a.bf16);
   }
-  if (tid < NH) s_beta[tid] = a.beta[(b * NH + tid) * H + h];
+  if (tid < NH) {
+    const float x = a.beta[(b * NH + tid) * H + h];
+    s_beta[tid] = a.beta_map < 0 ? x : (a.beta_map == 1 ? 2.f : 1.f) / (1.f + __expf(-x));
+  }
   const float gate = a.g ? a.g[bh] : 1.0f;
   __syncthreads();  // token inputs visible
+  if (a.beta_map >= 0) {
+    // ---- prologue: q, k_j <- SiLU(.) / ||SiLU(.)||_2 (0 for a zero vector) ----
+    for (int i = tid; i < (NH + 1) * dk; i += kThreads) {
+      float *p = i < NH * dk ? &s_k[i / dk][i % dk] : &s_q[i - NH * dk];
+      *p = silu(*p);
+    }
+    __syncthreads();
+    for (int j = warp; j <= NH; j += kThreads / 32) {
+      const float *p = j < NH ? s_k[j] : s_q;
+      float ss = 0.f;
+      for (int d = lane; d < dk; d += 32) ss = fmaf(p[d], p[d], ss);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s_inv[j] = ss > 0.f ? rsqrtf(ss) : 0.f;
+    }
+    __syncthreads();
+    for (int i = tid; i < (NH + 1) * dk; i += kThreads) {
+      if (i < NH * dk)
+        s_k[i / dk][i % dk] *= s_inv[i / dk];
+      else
+        s_q[i - NH * dk] *= s_inv[NH];
+    }
+    __syncthreads();
+  }
 
   // ---- the small dot products k_i.k_j and k_j.q, one warp each ----
   {
