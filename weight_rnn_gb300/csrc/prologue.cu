@@ -17,9 +17,21 @@ namespace delta {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kRows = 4;  // rows in flight per lane group
 
-__device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
-__device__ __forceinline__ float sigmoid(float x) { return 1.f / (1.f + __expf(-x)); }
+// SiLU with two MUFU operations (exp and reciprocal, relative error ~2^-21):
+// for float32 outputs
+__device__ __forceinline__ float silu_f32(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+// SiLU with one, x sigmoid(x) = h + h tanh(h) with h = x / 2 (tanh.approx,
+// relative error ~2^-11, below the bf16 rounding of the result): for bf16
+// outputs, where the MUFU rate would otherwise bound the kernel
+__device__ __forceinline__ float silu_bf16(float x) {
+  const float h = 0.5f * x;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
+}
+__device__ __forceinline__ float sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 template <typename In>
 __device__ __forceinline__ void unpack(const uint4 &u, float (&x)[16 / sizeof(In)]) {
@@ -61,33 +73,43 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(PrologueArgs a) {
   const int lane = threadIdx.x & 31;
   const int sub = lane % lpr;
   const int64_t rows = a.rows_q + a.rows_k;
-  const int64_t rows_per_warp = 32 / lpr;
+  const int64_t rpw = 32 / lpr;  // rows per warp and load
   const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
   const int64_t gw = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-  for (int64_t base = gw * rows_per_warp; base < rows; base += warps * rows_per_warp) {
-    const int64_t row = base + lane / lpr;
-    const bool live = row < rows;
-    const bool isq = row < a.rows_q;
-    const int64_t r = isq ? row : row - a.rows_q;
-    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const In *>(isq ? a.q : a.k) + r * a.dk) + sub;
-    float x[V];
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (live) u = __ldcs(src);
-    unpack<In>(u, x);
-    float ss = 0.f;
+  // kRows rows per lane group per round, their loads issued before any use
+  // so that enough bytes are in flight to keep HBM busy
+  for (int64_t base = gw * rpw * kRows; base < rows; base += warps * rpw * kRows) {
+    uint4 u[kRows];
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-      x[i] = silu(x[i]);
-      ss = fmaf(x[i], x[i], ss);
+    for (int j = 0; j < kRows; ++j) {
+      const int64_t row = base + j * rpw + lane / lpr;
+      const bool isq = row < a.rows_q;
+      const int64_t r = isq ? row : row - a.rows_q;
+      u[j] = make_uint4(0, 0, 0, 0);
+      if (row < rows)
+        u[j] = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const In *>(isq ? a.q : a.k) + r * a.dk) + sub);
     }
-    // sum over the row's lane group (xor offsets below lpr stay inside it)
-    for (int o = lpr >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
 #pragma unroll
-    for (int i = 0; i < V; ++i) x[i] *= inv;
-    if (live) {
-      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<In *>(isq ? a.q_out : a.k_out) + r * a.dk) + sub;
-      __stcs(dst, pack<In>(x));
+    for (int j = 0; j < kRows; ++j) {
+      const int64_t row = base + j * rpw + lane / lpr;
+      const bool isq = row < a.rows_q;
+      const int64_t r = isq ? row : row - a.rows_q;
+      float x[V];
+      unpack<In>(u[j], x);
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        x[i] = sizeof(In) == 2 ? silu_bf16(x[i]) : silu_f32(x[i]);
+        ss = fmaf(x[i], x[i], ss);
+      }
+      // sum over the row's lane group (xor offsets below lpr stay inside it)
+      for (int o = lpr >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) x[i] *= inv;
+      if (row < rows)
+        __stcs(reinterpret_cast<uint4 *>(static_cast<In *>(isq ? a.q_out : a.k_out) + r * a.dk) + sub,
+               pack<In>(x));
     }
   }
   const float scale = a.beta_map == 1 ? 2.f : 1.f;
@@ -101,20 +123,22 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(PrologueArgs a) {
 cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t s) {
   const int64_t rows = a.rows_q + a.rows_k;
   const int lpr = a.dk / (a.bf16 ? 8 : 4);
-  const int64_t rows_per_block = (int64_t)(kThreads / 32) * (32 / lpr);
+  const int64_t rows_per_block = (int64_t)(kThreads / 32) * (32 / lpr) * kRows;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // enough blocks to cover every row once, at most 8 per SM (grid-stride)
+  // enough blocks to cover every row once, at most as many as are resident
+  // at a time (grid-stride beyond that)
+  auto kern = a.bf16 ? prologue_kernel<__nv_bfloat16> : prologue_kernel<float>;
+  int per_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0)) != cudaSuccess)
+    return e;
   int64_t grid = (rows + rows_per_block - 1) / rows_per_block;
-  const int64_t cap = (int64_t)sms * 8;
+  const int64_t cap = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  if (a.bf16)
-    prologue_kernel<__nv_bfloat16><<<(unsigned)grid, kThreads, 0, s>>>(a);
-  else
-    prologue_kernel<float><<<(unsigned)grid, kThreads, 0, s>>>(a);
+  kern<<<(unsigned)grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
