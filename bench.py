@@ -577,6 +577,8 @@ def measure_prologue(wr, dev, args, peaks):
     forward on the same tensors taken as already normalised (``delta_fwd``)."""
     stream = torch.cuda.current_stream(dev)
     w = synth.WORKLOADS[HEADLINE]
+    if args.batch:
+        w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
     B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
     gen = torch.Generator(device=dev).manual_seed(w.seed + 11)
     rn = lambda *shape: torch.randn(shape, generator=gen, device=dev)
@@ -636,8 +638,7 @@ def run_ours(args, dist):
     head_id = ids[0]
     head = recs[head_id]
     diagnostics = measure_diagnostics(wr, dev, args) if args.workload == "all" else None
-    prologue = (measure_prologue(wr, dev, args, peaks)
-                if args.workload == "all" and not args.batch else None)
+    prologue = measure_prologue(wr, dev, args, peaks) if args.workload == "all" else None
     w = synth.WORKLOADS[head_id]
     if args.batch:
         w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
