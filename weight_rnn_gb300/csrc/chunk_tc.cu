@@ -727,12 +727,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         st_chunk(ws + sw128_offset(L, 8 * q, 128), {pw_[4 * q], pw_[4 * q + 1], pw_[4 * q + 2], pw_[4 * q + 3]});
       if (GATED) {
         // ---- the readout factor exp(gc) at each readout row's sub-step
-        //      (published by prep warp 2 with the chunk's plan).  Ratio regime (the chunk's decay stays above
-        //      2^-100; P' = Q K^T * 2^-gc_j): the output rows are scaled by
-        //      it at write-out.  Exact regime: Q exp(gc) in place (rows past
-        //      the readouts zeroed) and no output scaling.  The G product
-        //      (which read Q) completed before P and W; the output product
-        //      that reads Q waits for the S W product, which waits for WCVT ----
+        //      (published by prep warp 2 with the chunk's plan).  Ratio
+        //      regime (the chunk's decay stays above 2^-100; P' = Q K^T *
+        //      2^-gc_j): the output rows are scaled by it at write-out.
+        //      Exact regime: Q exp(gc) in place (rows past the readouts
+        //      zeroed) and no output scaling.  The G product (which read Q)
+        //      completed before P and W; the output product that reads Q
+        //      waits for the S W product, which waits for WCVT ----
         // (the plan of chunk m + 4 needs this thread's W^T of chunk m + 2)
         wait_bar(sm, B_PLAN + (m & 3), (m >> 2) & 1, 3);
         if (!sm.plan(m)->ratio) {
