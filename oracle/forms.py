@@ -335,3 +335,35 @@ def prologue(q_raw, k_raw, beta_raw, beta_map="sigmoid"):
     elif beta_map != "sigmoid":
         raise ValueError(f"beta_map {beta_map!r} is not 'sigmoid' or '2sigmoid'")
     return unit(q_raw), unit(k_raw), b
+
+
+# --------------------------------------------------------------------------
+# channel-wise gate (KDA; [DR] §1.4 family table and §5 DPLR reductions)
+# --------------------------------------------------------------------------
+def kda_recurrent(q, k, v, beta, alpha, S0=None, n_h=1):
+    """The KDA recurrence of [DR] §1.4 with a per-channel gate, for one head:
+        S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+        o_t = S_t^T q_t,
+    the decay applied first, then the delta update on the decayed state.
+    alpha_t (a vector over the key dimension) decays the rows of S.  With
+    n_h > 1 ([DP] §2.6) the gate acts once per token, before its n_h
+    sub-steps, and the readout follows the last one.
+    Shapes: q [T, dk]; k [T, n_h, dk]; v [T, n_h, dv]; beta [T, n_h];
+    alpha [T, dk]; S0 [dk, dv] or None."""
+    q = np.asarray(q, float)
+    k = np.asarray(k, float).reshape(q.shape[0], n_h, q.shape[1])
+    v = np.asarray(v, float)
+    v = v.reshape(q.shape[0], n_h, v.shape[-1])
+    beta = np.asarray(beta, float).reshape(q.shape[0], n_h)
+    alpha = np.asarray(alpha, float)
+    T, dk = q.shape
+    dv = v.shape[-1]
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((T, dv))
+    for t in range(T):
+        S = alpha[t][:, None] * S
+        for j in range(n_h):
+            kk = k[t, j]
+            S = S + beta[t, j] * np.outer(kk, v[t, j] - S.T @ kk)
+        o[t] = S.T @ q[t]
+    return o, S
