@@ -614,6 +614,46 @@ def measure_prologue(wr, dev, args, peaks):
             "fwd_prologue_ms": fwdp_us / 1e3, "fwd_ms": fwd_us / 1e3}
 
 
+def measure_kda(wr, dev, args, peaks):
+    """The channel-wise gate (``delta_fwd_kda``, the CUDA-core kernel) on the
+    headline workload's shapes: q, k, v bf16 from the headline recipe (unit
+    keys), per-channel alpha = sigmoid(N(0,1) * 2 + 3) float32, timed with CUDA
+    events; bytes = the headline's algorithmic bytes + alpha (4 B per key
+    channel per token)."""
+    stream = torch.cuda.current_stream(dev)
+    w = synth.WORKLOADS[HEADLINE]
+    if args.batch:
+        w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
+    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 13)
+    rn = lambda *shape: torch.randn(shape, generator=gen, device=dev)
+    k = rn(B, T, H, dk)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    q, v = rn(B, T, H, dk).to(torch.bfloat16), rn(B, T, H, dv).to(torch.bfloat16)
+    beta = torch.sigmoid(rn(B, T, H))
+    alpha = torch.sigmoid(rn(B, T, H, dk) * 2.0 + 3.0)
+    h0 = rn(B, H, dk, dv) * w.h0_std
+    out = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=dev)
+    hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    fn = lambda: wr.delta_fwd_kda(q, k, v, beta, alpha, h0, out, hT)
+    fn()
+    torch.cuda.synchronize(dev)
+    steps = max(2, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = algorithmic_bytes(w) + alpha.numel() * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "input": "headline shapes, per-channel alpha = sigmoid(2 N(0,1) + 3)",
+            "kernel": "chunk_generic_kernel (float32, CUDA cores)", "ms_per_step": ms,
+            "value": w.tokens / (ms * 1e-3), "unit": UNIT, "steps": steps,
+            "bytes_per_step": nbytes, "gbs": gbs, "frac_of_measured_hbm": gbs / float(peaks["hbm_gbs"])}
+
+
 def run_ours(args, dist):
     import weight_rnn_gb300 as wr
 
@@ -639,6 +679,7 @@ def run_ours(args, dist):
     head = recs[head_id]
     diagnostics = measure_diagnostics(wr, dev, args) if args.workload == "all" else None
     prologue = measure_prologue(wr, dev, args, peaks) if args.workload == "all" else None
+    kda = measure_kda(wr, dev, args, peaks) if args.workload == "all" else None
     w = synth.WORKLOADS[head_id]
     if args.batch:
         w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
@@ -660,6 +701,7 @@ def run_ours(args, dist):
         "gpu": torch.cuda.get_device_name(dev),
         "diagnostics": diagnostics,
         "prologue": prologue,
+        "kda": kda,
         "per_workload": {
             recs[i]["workload"]: {
                 "value": recs[i]["value"], "unit": UNIT,

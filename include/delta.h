@@ -110,6 +110,32 @@ int delta_fwd(const void *q, const void *k, const void *v, const float *beta,
               delta_dtype dtype, struct CUstream_st *stream);
 
 /*
+ * delta_fwd_kda -- delta_fwd with a channel-wise gate instead of the scalar
+ * one: the KDA row of the family table in "08 · linear 路线（三）" §1.4,
+ *
+ *   S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *   o_t = S_t^T q_t,
+ *
+ * the decay of each key row of the state first, then the delta update on the
+ * decayed state (§5 of the same page gives it as the DPLR form with w =
+ * alpha_t, a = -beta k, b = alpha_t * k).  With n_h > 1 the gate acts once per
+ * token, before its sub-steps, as g does in delta_fwd.
+ *
+ *   alpha [B, T, H, dk]  float32  per-channel linear gate in [0, 1]
+ *                                 (log alpha is clamped at -80 inside)
+ *   everything else      as in delta_fwd (without g)
+ *
+ * Runs the float32 CUDA-core chunk kernel for every shape (the tensor-core
+ * path takes the scalar gate only): a correctness path, several hundred times
+ * slower than delta_fwd's fast path.  Errors as in delta_fwd; alpha must be
+ * 16-byte aligned and must not overlap out or hT.
+ */
+int delta_fwd_kda(const void *q, const void *k, const void *v, const float *beta,
+                  const float *alpha, const float *h0, void *out, float *hT,
+                  int B, int H, int T, int dk, int dv, int n_h, int chunk,
+                  delta_dtype dtype, struct CUstream_st *stream);
+
+/*
  * delta_prologue -- the input prologue on its own: the keys of "DeltaProduct"
  * §2.2, k = psi(x) / ||psi(x)||_2 over the key dimension with psi = SiLU,
  * the queries likewise (the query path of the layer design in "08 · linear
@@ -246,6 +272,18 @@ int delta_step(const void *q, const void *k, const void *v, const float *beta,
                delta_dtype dtype, struct CUstream_st *stream);
 
 /*
+ * delta_step_kda -- delta_step with the channel-wise gate of delta_fwd_kda:
+ * alpha [B, H, dk] float32 in place of g.  The decayed state Diag(alpha) S
+ * is formed in the same single read of the state; HBM-bound like delta_step.
+ * Errors as in delta_step; alpha must be 16-byte aligned and overlap neither
+ * state nor out.
+ */
+int delta_step_kda(const void *q, const void *k, const void *v, const float *beta,
+                   const float *alpha, float *state, void *out,
+                   int B, int H, int dk, int dv, int n_h,
+                   delta_dtype dtype, struct CUstream_st *stream);
+
+/*
  * delta_step_prologue -- delta_step on raw projections, with the input
  * prologue of delta_fwd_prologue ("DeltaProduct" §2.2; "08 · linear 路线
  * （三）" §3) applied inside the decode kernel: q_raw, k_raw and beta_raw
@@ -333,7 +371,7 @@ int delta_version(void);
 
 /*
  * delta_inject_failure -- test hook: the next `count` calls of delta_fwd,
- * delta_prologue, delta_fwd_prologue, delta_ut_transform, delta_fwd_with_ut, delta_step,
+ * delta_fwd_kda, delta_step_kda, delta_prologue, delta_fwd_prologue, delta_ut_transform, delta_fwd_with_ut, delta_step,
  * delta_step_prologue, delta_state_erank and delta_attention_map (together)
  * return DELTA_ERR_CUDA, with "injected failure" in
  * delta_last_error(), right after their arguments pass validation and before

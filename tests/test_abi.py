@@ -320,3 +320,44 @@ def test_prologue_rejects_before_launch(lib, beta_map, kw, status):
 def test_prologue_empty_is_ok_without_gpu(lib):
     assert prologue(lib, 0, T=0) == wr.DELTA_OK
     assert prologue(lib, 1, B=0, q=None, k=None) == wr.DELTA_OK
+
+
+def fwd_kda(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, beta=FAKE * 4, alpha=FAKE * 9, h0=None,
+             out=FAKE * 5, hT=None, B=1, H=1, T=4, dk=16, dv=16, n_h=1, chunk=16,
+             dtype=wr.DELTA_F32)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_fwd_kda(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["beta"]), vp(a["alpha"]),
+                             vp(a["h0"]), vp(a["out"]), vp(a["hT"]), a["B"], a["H"], a["T"],
+                             a["dk"], a["dv"], a["n_h"], a["chunk"], a["dtype"], None)
+
+
+def step_kda(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, beta=FAKE * 4, alpha=FAKE * 9, state=FAKE * 5,
+             out=FAKE * 6, B=1, H=1, dk=16, dv=16, n_h=1, dtype=wr.DELTA_F32)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_step_kda(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["beta"]), vp(a["alpha"]),
+                              vp(a["state"]), vp(a["out"]), a["B"], a["H"], a["dk"], a["dv"],
+                              a["n_h"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(alpha=None), wr.DELTA_ERR_INVALID),
+    (dict(alpha=FAKE * 9 + 4), wr.DELTA_ERR_ALIGN),
+    (dict(out=FAKE * 9 + 16), wr.DELTA_ERR_INVALID),     # out overlaps alpha
+    (dict(dk=24), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(q=None), wr.DELTA_ERR_INVALID),
+])
+def test_kda_entry_points_reject_before_launch(lib, kw, status):
+    assert fwd_kda(lib, **kw) == status
+    skw = dict(kw)
+    if "out" in skw:
+        skw = dict(state=FAKE * 9 + 16)                  # state overlaps alpha
+    assert step_kda(lib, **skw) == status
+
+
+def test_kda_empty_problems_are_ok_without_gpu(lib):
+    assert fwd_kda(lib, B=0) == wr.DELTA_OK
+    assert step_kda(lib, H=0) == wr.DELTA_OK

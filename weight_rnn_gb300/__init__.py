@@ -15,7 +15,8 @@ import threading
 
 import torch
 
-__all__ = ["delta_fwd", "delta_prologue", "delta_fwd_prologue", "delta_step_prologue",
+__all__ = ["delta_fwd", "delta_fwd_kda", "delta_step_kda", "delta_prologue",
+           "delta_fwd_prologue", "delta_step_prologue",
            "delta_fwd_static_scratch", "delta_state_erank",
            "delta_attention_map", "delta_ut_transform", "delta_fwd_with_ut", "delta_step",
            "fwd_launches", "delta_status_string", "delta_last_error",
@@ -37,7 +38,8 @@ DELTA_BETA_2SIGMOID = 1
 _BETA_MAPS = {"sigmoid": DELTA_BETA_SIGMOID, "2sigmoid": DELTA_BETA_2SIGMOID}
 
 #: every extern "C" entry point include/delta.h declares
-EXPORTED_SYMBOLS = ("delta_fwd", "delta_prologue", "delta_fwd_prologue", "delta_fwd_static_scratch",
+EXPORTED_SYMBOLS = ("delta_fwd", "delta_fwd_kda", "delta_step_kda", "delta_prologue",
+                    "delta_fwd_prologue", "delta_fwd_static_scratch",
                     "delta_ut_transform", "delta_fwd_with_ut",
                     "delta_fwd_kernel_count", "delta_step", "delta_step_prologue",
                     "delta_status_string",
@@ -77,6 +79,10 @@ def load_library():
         p, i = ctypes.c_void_p, ctypes.c_int
         lib.delta_fwd.restype = i
         lib.delta_fwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.delta_fwd_kda.restype = i
+        lib.delta_fwd_kda.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.delta_step_kda.restype = i
+        lib.delta_step_kda.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, p]
         lib.delta_prologue.restype = i
         lib.delta_prologue.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, p]
         lib.delta_fwd_prologue.restype = i
@@ -225,6 +231,70 @@ def delta_fwd(q, k, v, beta, g=None, h0=None, out=None, hT=None, *, n_h=1,
     if st != DELTA_OK:
         raise DeltaError(st, delta_last_error())
     return out, hT
+
+
+def delta_fwd_kda(q, k, v, beta, alpha, h0=None, out=None, hT=None, *, n_h=1, chunk=64,
+                  want_state=True, stream=None):
+    """Chunked forward with a channel-wise gate (``delta_fwd_kda``): alpha
+    [B,T,H,dk] float32 decays each key row of the state, in place of g.
+    Other shapes and results as in ``delta_fwd``."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("delta_fwd_kda needs CUDA tensors")
+    dt = q.dtype
+    code = _dtype_code(dt)
+    if n_h == 1 and k.dim() == 4:
+        kshape, vshape, bshape = (B, T, H, dk), (B, T, H, v.shape[-1]), (B, T, H)
+    else:
+        kshape, vshape, bshape = (B, T, n_h, H, dk), (B, T, n_h, H, v.shape[-1]), (B, T, n_h, H)
+    dv = v.shape[-1]
+    _check(q, "q", (B, T, H, dk), dt, dev)
+    _check(k, "k", kshape, dt, dev)
+    _check(v, "v", vshape, dt, dev)
+    _check(beta, "beta", bshape, torch.float32, dev)
+    _check(alpha, "alpha", (B, T, H, dk), torch.float32, dev)
+    _check(h0, "h0", (B, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=dt, device=dev)
+    _check(out, "out", (B, T, H, dv), dt, dev)
+    if hT is None and want_state:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(hT, "hT", (B, H, dk, dv), torch.float32, dev)
+    st = lib.delta_fwd_kda(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(h0),
+                           _ptr(out), _ptr(hT), B, H, T, dk, dv, n_h, chunk, code,
+                           _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return out, hT
+
+
+def delta_step_kda(q, k, v, beta, alpha, state, out=None, *, n_h=1, stream=None):
+    """One decode token with a channel-wise gate (``delta_step_kda``): alpha
+    [B,H,dk] float32 in place of g; ``state`` is updated in place."""
+    lib = load_library()
+    B, H, dk = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("delta_step_kda needs CUDA tensors")
+    dt = q.dtype
+    code = _dtype_code(dt)
+    dv = v.shape[-1]
+    _check(q, "q", (B, H, dk), dt, dev)
+    _check(k, "k", (B, n_h, H, dk), dt, dev)
+    _check(v, "v", (B, n_h, H, dv), dt, dev)
+    _check(beta, "beta", (B, n_h, H), torch.float32, dev)
+    _check(alpha, "alpha", (B, H, dk), torch.float32, dev)
+    _check(state, "state", (B, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=dt, device=dev)
+    _check(out, "out", (B, H, dv), dt, dev)
+    st = lib.delta_step_kda(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(state),
+                            _ptr(out), B, H, dk, dv, n_h, code, _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return out
 
 
 def _beta_map(beta_map):

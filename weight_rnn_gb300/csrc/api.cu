@@ -299,15 +299,26 @@ int validate_step(const void *q, const void *k, const void *v, const float *beta
 
 int run_step(const void *q, const void *k, const void *v, const float *beta, const float *g,
              float *state, void *out, int B, int H, int dk, int dv, int n_h, delta_dtype dtype,
-             int beta_map, struct CUstream_st *stream) {
+             int beta_map, struct CUstream_st *stream, const float *alpha = nullptr,
+             bool kda = false) {
   const int st = validate_step(q, k, v, beta, g, state, out, B, H, dk, dv, n_h, dtype);
   if (st != DELTA_OK || (int64_t)B * H == 0) return st;
+  if (kda) {
+    if (!alpha) return fail(DELTA_ERR_INVALID, "alpha must be non-NULL");
+    if (!aligned16(alpha)) return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+    const int64_t BH = (int64_t)B * H, esz = dtype == DELTA_BF16 ? 2 : 4;
+    const Range r_a = range(alpha, BH * dk * 4);
+    if (overlap(r_a, range(state, BH * dk * dv * 4)))
+      return fail(DELTA_ERR_INVALID, "state overlaps alpha");
+    if (overlap(r_a, range(out, BH * dv * esz))) return fail(DELTA_ERR_INVALID, "out overlaps alpha");
+  }
   if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
   delta::StepArgs a;
   a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.state = state; a.out = out;
   a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.n_h = n_h;
   a.bf16 = dtype == DELTA_BF16;
   a.beta_map = beta_map;
+  a.alpha = alpha;
   const cudaError_t err = delta::launch_step(a, reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? DELTA_OK : cuda_fail(err, "decode step launch");
 }
@@ -409,6 +420,29 @@ int delta_fwd_prologue(const void *q_raw, const void *k_raw, const void *v, cons
   const cudaError_t ef = cudaFreeAsync(scratch, s);
   if (rc != DELTA_OK) return rc;
   return ef == cudaSuccess ? DELTA_OK : cuda_fail(ef, "scratch release");
+}
+
+int delta_fwd_kda(const void *q, const void *k, const void *v, const float *beta,
+                  const float *alpha, const float *h0, void *out, float *hT, int B, int H, int T,
+                  int dk, int dv, int n_h, int chunk, delta_dtype dtype,
+                  struct CUstream_st *stream) {
+  delta::FwdArgs a;
+  const int st = validate_fwd(q, k, v, beta, nullptr, h0, out, hT, B, H, T, dk, dv, n_h, chunk,
+                              dtype, a);
+  if (st != DELTA_OK || a.B * a.H == 0) return st;
+  if (T > 0) {
+    if (!alpha) return fail(DELTA_ERR_INVALID, "alpha must be non-NULL");
+    if (!aligned16(alpha)) return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+    const int64_t esz = a.bf16 ? 2 : 4, BH = a.B * a.H;
+    const Range r_a = range(alpha, BH * a.T * dk * 4);
+    if (overlap(r_a, range(out, BH * a.T * dv * esz)))
+      return fail(DELTA_ERR_INVALID, "out overlaps alpha");
+    if (overlap(r_a, range(hT, BH * dk * dv * 4)))
+      return fail(DELTA_ERR_INVALID, "hT overlaps alpha");
+  }
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+  a.alpha = alpha;
+  return run_fwd(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int delta_prologue(const void *q_raw, const void *k_raw, const float *beta_raw, void *q_out,
@@ -566,6 +600,13 @@ int delta_step(const void *q, const void *k, const void *v, const float *beta,
                const float *g, float *state, void *out, int B, int H, int dk, int dv,
                int n_h, delta_dtype dtype, struct CUstream_st *stream) {
   return run_step(q, k, v, beta, g, state, out, B, H, dk, dv, n_h, dtype, -1, stream);
+}
+
+int delta_step_kda(const void *q, const void *k, const void *v, const float *beta,
+                   const float *alpha, float *state, void *out, int B, int H, int dk, int dv,
+                   int n_h, delta_dtype dtype, struct CUstream_st *stream) {
+  return run_step(q, k, v, beta, nullptr, state, out, B, H, dk, dv, n_h, dtype, -1, stream, alpha,
+                  true);
 }
 
 int delta_step_prologue(const void *q_raw, const void *k_raw, const void *v, const float *beta_raw,

@@ -14,6 +14,15 @@
 //   O   = (Q * exp(gc)) S + (Q K^T * Gam) Vt      readout rows only
 //   S  <- exp(gc_C) S + (K * exp(gc_C - gc))^T Vt
 //
+// With a channel-wise gate (the KDA row of the family table in §1.4: S_t =
+// (I - beta k k^T) Diag(alpha_t) S_{t-1} + beta k v^T), gc is a vector per row
+// (the cumulative log alpha of each key channel) and every Gam factor above
+// becomes the per-channel ratio inside the key dimension's sum:
+//
+//   A_rj = beta_r sum_d k_rd k_jd exp(gc_rd - gc_jd),  P_rj likewise with q_r
+//   W    = T (K * exp(gc)),  O = (Q * exp(gc)) S + P Vt
+//   S   <- Diag(exp(gc_C)) S + (K * exp(gc_C - gc))^T Vt
+//
 // A ragged tail is padded with identity steps (k = v = 0, beta = 0, log g = 0).
 // log g is clamped at -80 so that g = 0 (a reset) stays finite: exp(-80) is
 // far below float32 resolution relative to the state.
@@ -45,10 +54,10 @@ __device__ __forceinline__ void store_io(void *p, int64_t i, float x, bool bf16)
 }
 
 struct Smem {
-  float *S, *K, *Q, *V, *A, *X, *P, *W, *U, *beta, *gc;
-  static __host__ __device__ size_t floats(int C, int dk, int BV) {
+  float *S, *K, *Q, *V, *A, *X, *P, *W, *U, *beta, *gc, *gcd;
+  static __host__ __device__ size_t floats(int C, int dk, int BV, bool kda) {
     return (size_t)dk * BV + 3 * (size_t)C * dk + 2 * (size_t)C * BV +
-           3 * (size_t)C * C + 2 * (size_t)C;
+           3 * (size_t)C * C + 2 * (size_t)C + (kda ? (size_t)C * dk : 0);
   }
   __device__ Smem(float *base, int C, int dk, int BV) {
     S = base;
@@ -62,9 +71,11 @@ struct Smem {
     P = X + C * C;
     beta = P + C * C;
     gc = beta + C;
+    gcd = gc + C;  // [C][dk], channel-wise gate only
   }
 };
 
+template <bool KDA>
 __global__ void __launch_bounds__(kThreads)
 chunk_generic_kernel(FwdArgs a, int BV) {
   extern __shared__ float smem_raw[];
@@ -75,6 +86,7 @@ chunk_generic_kernel(FwdArgs a, int BV) {
   const int64_t b = bh / a.H, h = bh % a.H;
   const int v0 = blockIdx.y * BV;
   const int64_t L = a.L, T = a.T, H = a.H;
+  constexpr bool kda = KDA;  // channel-wise gate a.alpha (else the scalar a.g)
 
   // initial state slab
   for (int i = tid; i < dk * BV; i += kThreads) {
@@ -116,12 +128,25 @@ chunk_generic_kernel(FwdArgs a, int BV) {
       sm.gc[r] = lg;
     }
     __syncthreads();
-    // inclusive cumulative log gate (C <= 64: one thread)
-    if (tid == 0) {
-      float acc = 0.0f;
-      for (int r = 0; r < C; ++r) {
-        acc += sm.gc[r];
-        sm.gc[r] = acc;
+    // inclusive cumulative log gate (C <= 64: one thread; channel-wise: one
+    // thread per key channel)
+    if (!kda) {
+      if (tid == 0) {
+        float acc = 0.0f;
+        for (int r = 0; r < C; ++r) {
+          acc += sm.gc[r];
+          sm.gc[r] = acc;
+        }
+      }
+    } else {
+      for (int d = tid; d < dk; d += kThreads) {
+        float acc = 0.0f;
+        for (int r = 0; r < C; ++r) {
+          const int64_t e = e0 + r;
+          if (e < L && (e % n_h) == 0)
+            acc += fmaxf(logf(a.alpha[((b * T + e / n_h) * H + h) * dk + d]), kLogGateFloor);
+          sm.gcd[r * dk + d] = acc;
+        }
       }
     }
     __syncthreads();
@@ -129,7 +154,7 @@ chunk_generic_kernel(FwdArgs a, int BV) {
     for (int i = tid; i < C * C; i += kThreads) {
       const int r = i / C, j = i % C;
       float av = 0.0f, pv = 0.0f, xv = (r == j) ? 1.0f : 0.0f;
-      if (j <= r) {
+      if (j <= r && !kda) {
         const float gam = expf(sm.gc[r] - sm.gc[j]);
         float kk = 0.0f, qk = 0.0f;
         for (int d = 0; d < dk; ++d) {
@@ -139,6 +164,16 @@ chunk_generic_kernel(FwdArgs a, int BV) {
         }
         pv = qk * gam;
         if (j < r) av = sm.beta[r] * kk * gam;
+      } else if (j <= r) {
+        // the ratio of each channel's decay inside the sum (exponent <= 0)
+        float kk = 0.0f, qk = 0.0f;
+        for (int d = 0; d < dk; ++d) {
+          const float kj = sm.K[j * dk + d] * expf(sm.gcd[r * dk + d] - sm.gcd[j * dk + d]);
+          kk = fmaf(sm.K[r * dk + d], kj, kk);
+          qk = fmaf(sm.Q[r * dk + d], kj, qk);
+        }
+        pv = qk;
+        if (j < r) av = sm.beta[r] * kk;
       }
       sm.A[i] = av;
       sm.P[i] = pv;
@@ -162,7 +197,7 @@ chunk_generic_kernel(FwdArgs a, int BV) {
       const int r = i / dk, d = i % dk;
       float acc = 0.0f;
       for (int j = 0; j <= r; ++j)
-        acc = fmaf(sm.A[r * C + j], sm.K[j * dk + d] * expf(sm.gc[j]), acc);
+        acc = fmaf(sm.A[r * C + j], sm.K[j * dk + d] * expf(kda ? sm.gcd[j * dk + d] : sm.gc[j]), acc);
       sm.W[i] = acc;
     }
     for (int i = tid; i < C * BV; i += kThreads) {
@@ -186,20 +221,27 @@ chunk_generic_kernel(FwdArgs a, int BV) {
       const int64_t e = e0 + r;
       if (e >= L || (int)(e % n_h) != n_h - 1) continue;
       float qs = 0.0f;
-      for (int d = 0; d < dk; ++d) qs = fmaf(sm.Q[r * dk + d], sm.S[d * BV + c], qs);
-      float acc = qs * expf(sm.gc[r]);
+      if (kda) {
+        for (int d = 0; d < dk; ++d)
+          qs = fmaf(sm.Q[r * dk + d] * expf(sm.gcd[r * dk + d]), sm.S[d * BV + c], qs);
+      } else {
+        for (int d = 0; d < dk; ++d) qs = fmaf(sm.Q[r * dk + d], sm.S[d * BV + c], qs);
+        qs *= expf(sm.gc[r]);
+      }
+      float acc = qs;
       for (int j = 0; j <= r; ++j) acc = fmaf(sm.P[r * C + j], sm.U[j * BV + c], acc);
       store_io(a.out, ((b * T + e / n_h) * H + h) * a.dv + v0 + c, acc, a.bf16);
     }
     __syncthreads();
     // ---- S <- exp(gc_C) S + (K * exp(gc_C - gc))^T Vt ----
-    const float gl = sm.gc[C - 1];
-    const float decay = expf(gl);
     for (int i = tid; i < dk * BV; i += kThreads) {
       const int d = i / BV, c = i % BV;
-      float acc = sm.S[i] * decay;
+      const float *g = kda ? sm.gcd + d : sm.gc;  // this row's cumulative log gate
+      const int gs = kda ? dk : 1;
+      const float gl = g[(C - 1) * gs];
+      float acc = sm.S[i] * expf(gl);
       for (int j = 0; j < C; ++j)
-        acc = fmaf(sm.K[j * dk + d] * expf(gl - sm.gc[j]), sm.U[j * BV + c], acc);
+        acc = fmaf(sm.K[j * dk + d] * expf(gl - g[j * gs]), sm.U[j * BV + c], acc);
       sm.S[i] = acc;
     }
   }
@@ -222,12 +264,13 @@ __global__ void state_passthrough_kernel(const float *h0, float *hT, int64_t n) 
 
 cudaError_t launch_chunk_generic(const FwdArgs &a, cudaStream_t s) {
   const int BV = a.dv < 32 ? a.dv : 32;
-  const size_t bytes = Smem::floats(a.chunk, a.dk, BV) * sizeof(float);
-  cudaError_t err = cudaFuncSetAttribute(
-      chunk_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  const bool kda = a.alpha != nullptr;
+  const size_t bytes = Smem::floats(a.chunk, a.dk, BV, kda) * sizeof(float);
+  auto kern = kda ? chunk_generic_kernel<true> : chunk_generic_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (err != cudaSuccess) return err;
   dim3 grid((unsigned)(a.B * a.H), (unsigned)(a.dv / BV));
-  chunk_generic_kernel<<<grid, kThreads, bytes, s>>>(a, BV);
+  kern<<<grid, kThreads, bytes, s>>>(a, BV);
   return cudaGetLastError();
 }
 

@@ -957,7 +957,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 }  // namespace
 
 bool chunk_tc_supports(const FwdArgs &a) {
-  return a.bf16 && a.dk == D && a.dv == D && a.chunk == C && a.T > 0 && ut_supports(a);
+  return a.bf16 && a.dk == D && a.dv == D && a.chunk == C && a.T > 0 && !a.alpha && ut_supports(a);
 }
 
 namespace {

@@ -17,6 +17,8 @@ struct FwdArgs {
   int64_t B, H, T, L;
   int dk, dv, n_h, chunk;
   bool bf16;
+  // channel-wise gate [B, T, H, dk] (KDA), instead of g; nullptr: none
+  const float *alpha = nullptr;
 };
 
 struct StepArgs {
@@ -27,6 +29,8 @@ struct StepArgs {
   int64_t B, H;
   int dk, dv, n_h;
   bool bf16;
+  // channel-wise gate [B, H, dk] (KDA), instead of g; nullptr: none
+  const float *alpha = nullptr;
   // input prologue applied in the kernel: -1 none (q, k, beta as given);
   // 0: q, k -> SiLU -> L2 norm, beta -> sigmoid; 1: the same, beta -> 2 sigmoid
   int beta_map = -1;

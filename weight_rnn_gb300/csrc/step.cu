@@ -26,6 +26,11 @@
 // store.  Loads and stores use the streaming cache hint: every byte of the
 // state is touched once per call.
 //
+// With a channel-wise gate alpha (KDA, the family table of "08 · linear
+// 路线（三）" §1.4: S <- (I - beta k k^T) Diag(alpha) S + beta k v^T), the
+// decayed state Diag(alpha) S0 takes the place of g S0: r_j = S0^T (alpha *
+// k_j), r_q = S0^T (alpha * q), S' = Diag(alpha) S0 + sum_j beta_j k_j e_j^T.
+//
 // With the input prologue on (delta_step_prologue), the raw q and k of the
 // token go through SiLU and an L2 norm over the key index and beta through
 // sigmoid or 2 sigmoid ("DeltaProduct" §2.2; the query path of the layer
@@ -57,7 +62,7 @@ __device__ __forceinline__ void store_io(void *p, int64_t i, float x, bool bf16)
 
 __device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
 
-template <int NH>
+template <int NH, bool KDA>
 __global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
   __shared__ float s_k[NH][kMaxD];
   __shared__ float s_q[kMaxD];
@@ -67,6 +72,7 @@ __global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
   __shared__ float s_beta[NH];
   __shared__ float s_dot[NH + 1][NH];  // [i][j] = k_i.k_j (i<j); [NH][j] = k_j.q
   __shared__ float s_inv[NH + 1];      // prologue: 1 / ||SiLU(k_j)||, 1 / ||SiLU(q)||
+  __shared__ float s_alpha[kMaxD];     // channel-wise gate (KDA)
   // partial sums per row group: (NH + 1) x RG x SW floats, RG * SW == 4 * kThreads
   // (written as float4: 16-byte alignment)
   __shared__ __align__(16) float s_part[(NH + 1) * 4 * kThreads];
@@ -106,7 +112,10 @@ __global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
     const float x = a.beta[(b * NH + tid) * H + h];
     s_beta[tid] = a.beta_map < 0 ? x : (a.beta_map == 1 ? 2.f : 1.f) / (1.f + __expf(-x));
   }
-  const float gate = a.g ? a.g[bh] : 1.0f;
+  constexpr bool kda = KDA;  // channel-wise gate a.alpha (else the scalar a.g)
+  if (kda)
+    for (int i = tid; i < dk; i += kThreads) s_alpha[i] = a.alpha[bh * dk + i];
+  const float gate = kda ? 1.0f : (a.g ? a.g[bh] : 1.0f);
   __syncthreads();  // token inputs visible
   if (a.beta_map >= 0) {
     // ---- prologue: q, k_j <- SiLU(.) / ||SiLU(.)||_2 (0 for a zero vector) ----
@@ -164,9 +173,10 @@ __global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
   for (int i = 0; i < kMaxRows; ++i) {
     const int d = rg + i * RG;
     if (d < dk) {
+      const float ad = kda ? s_alpha[d] : 1.0f;  // the row's decay (KDA)
 #pragma unroll
       for (int j = 0; j <= NH; ++j) {
-        const float w = (j < NH) ? s_k[j][d] : s_q[d];
+        const float w = ((j < NH) ? s_k[j][d] : s_q[d]) * ad;
         part[j].x = fmaf(S[i].x, w, part[j].x);
         part[j].y = fmaf(S[i].y, w, part[j].y);
         part[j].z = fmaf(S[i].z, w, part[j].z);
@@ -215,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
   for (int i = 0; i < kMaxRows; ++i) {
     const int d = rg + i * RG;
     if (d < dk) {
-      float4 x = make_float4(S[i].x * gate, S[i].y * gate, S[i].z * gate, S[i].w * gate);
+      const float gd = kda ? s_alpha[d] : gate;
+      float4 x = make_float4(S[i].x * gd, S[i].y * gd, S[i].z * gd, S[i].w * gd);
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
         const float kd = s_k[j][d];
@@ -234,11 +245,12 @@ __global__ void __launch_bounds__(kThreads, 6) step_kernel(StepArgs a) {
 cudaError_t launch_step(const StepArgs &a, cudaStream_t s) {
   const int sw = a.dv < kSlab ? a.dv : kSlab;
   const unsigned grid = (unsigned)(a.B * a.H * (a.dv / sw));
+  const bool kda = a.alpha != nullptr;
   switch (a.n_h) {
-    case 1: step_kernel<1><<<grid, kThreads, 0, s>>>(a); break;
-    case 2: step_kernel<2><<<grid, kThreads, 0, s>>>(a); break;
-    case 3: step_kernel<3><<<grid, kThreads, 0, s>>>(a); break;
-    case 4: step_kernel<4><<<grid, kThreads, 0, s>>>(a); break;
+    case 1: (kda ? step_kernel<1, true> : step_kernel<1, false>)<<<grid, kThreads, 0, s>>>(a); break;
+    case 2: (kda ? step_kernel<2, true> : step_kernel<2, false>)<<<grid, kThreads, 0, s>>>(a); break;
+    case 3: (kda ? step_kernel<3, true> : step_kernel<3, false>)<<<grid, kThreads, 0, s>>>(a); break;
+    case 4: (kda ? step_kernel<4, true> : step_kernel<4, false>)<<<grid, kThreads, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
