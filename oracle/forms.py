@@ -367,3 +367,42 @@ def kda_recurrent(q, k, v, beta, alpha, S0=None, n_h=1):
             S = S + beta[t, j] * np.outer(kk, v[t, j] - S.T @ kk)
         o[t] = S.T @ q[t]
     return o, S
+
+
+# --------------------------------------------------------------------------
+# gradients of the recurrence (no page gives them: float64 autograd)
+# --------------------------------------------------------------------------
+def recurrent_grad(q, k, v, beta, g, S0, dout, dST=None, n_h=1):
+    """Gradients of L = <dout, o> + <dST, S_T> through the recurrence of
+    [DP] §2.6 (gate once per token, then n_h delta sub-steps, readout after
+    the last), for one head, by float64 reverse-mode autograd of a plain
+    loop (the pages state no backward formulas).
+    Shapes: q [T, dk]; k [T, n_h, dk]; v [T, n_h, dv]; beta [T, n_h];
+    g [T] or None; S0 [dk, dv] or None; dout [T, dv]; dST [dk, dv] or None.
+    Returns dq, dk, dv, dbeta, dg (None without g), dS0 as NumPy arrays."""
+    import torch
+    f64 = lambda x: torch.tensor(np.asarray(x, dtype=np.float64), requires_grad=True)
+    T, dk = np.asarray(q).shape
+    dv = np.asarray(v).shape[-1]
+    tq = f64(q)
+    tk = f64(np.asarray(k, float).reshape(T, n_h, dk))
+    tv = f64(np.asarray(v, float).reshape(T, n_h, dv))
+    tb = f64(np.asarray(beta, float).reshape(T, n_h))
+    tg = None if g is None else f64(g)
+    tS0 = f64(np.zeros((dk, dv)) if S0 is None else S0)
+    S = tS0
+    outs = []
+    for t in range(T):
+        if tg is not None:
+            S = tg[t] * S
+        for j in range(n_h):
+            kk = tk[t, j]
+            S = S + tb[t, j] * torch.outer(kk, tv[t, j] - S.T @ kk)
+        outs.append(S.T @ tq[t])
+    o = torch.stack(outs)
+    loss = (o * torch.as_tensor(np.asarray(dout, dtype=np.float64))).sum()
+    if dST is not None:
+        loss = loss + (S * torch.as_tensor(np.asarray(dST, dtype=np.float64))).sum()
+    loss.backward()
+    grad = lambda x: None if x is None else x.grad.detach().numpy().copy()
+    return grad(tq), grad(tk), grad(tv), grad(tb), grad(tg), grad(tS0)

@@ -1,0 +1,93 @@
+"""Pins of the oracle's gradients of the recurrence (``oracle.forms.
+recurrent_grad``; no page states backward formulas), CPU only: central finite
+differences of the forward loss through the independent float64 forms, on
+tiny inputs, for every argument, and planted mistakes these pins catch."""
+import numpy as np
+import pytest
+
+from oracle import forms
+from pins import unit
+
+
+def loss(q, k, v, beta, g, S0, dout, dST, n_h):
+    # <dout, o> + <dST, S_T>, the forward written once more as a plain loop
+    T = q.shape[0]
+    S = np.array(S0, float)
+    L = 0.0
+    for t in range(T):
+        if g is not None:
+            S = g[t] * S
+        for j in range(n_h):
+            kk = k[t, j]
+            S = S + beta[t, j] * np.outer(kk, v[t, j] - S.T @ kk)
+        L += dout[t] @ (S.T @ q[t])
+    return L + np.sum(dST * S)
+
+
+def fd(f, x, eps=1e-6):
+    gr = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        x0 = x[i]
+        x[i] = x0 + eps
+        lp = f()
+        x[i] = x0 - eps
+        lm = f()
+        x[i] = x0
+        gr[i] = (lp - lm) / (2 * eps)
+    return gr
+
+
+@pytest.mark.parametrize("n_h,gated", [(1, False), (1, True), (2, True), (3, False)])
+def test_gradients_match_finite_differences(n_h, gated):
+    rng = np.random.default_rng(40 + n_h + 3 * gated)
+    T, dk, dv = 4, 3, 2
+    q = rng.standard_normal((T, dk))
+    k = unit(rng.standard_normal((T, n_h, dk)))
+    v = rng.standard_normal((T, n_h, dv))
+    beta = rng.uniform(0.1, 1.8, (T, n_h))
+    g = rng.uniform(0.4, 1.0, T) if gated else None
+    S0 = rng.standard_normal((dk, dv)) * 0.5
+    dout = rng.standard_normal((T, dv))
+    dST = rng.standard_normal((dk, dv))
+    got = forms.recurrent_grad(q, k, v, beta, g, S0, dout, dST, n_h=n_h)
+    f = lambda: loss(q, k, v, beta, g, S0, dout, dST, n_h)
+    for name, x, gx in (("q", q, got[0]), ("k", k, got[1]), ("v", v, got[2]),
+                        ("beta", beta, got[3]), ("S0", S0, got[5])):
+        np.testing.assert_allclose(gx, fd(f, x), rtol=1e-6, atol=1e-7, err_msg=name)
+    if gated:
+        np.testing.assert_allclose(got[4], fd(f, g), rtol=1e-6, atol=1e-7, err_msg="g")
+    else:
+        assert got[4] is None
+
+
+def test_no_state_gradient_without_a_state_loss_term_keeps_the_output_path():
+    # dST = None: only the outputs carry loss; dS0 still flows through them
+    rng = np.random.default_rng(47)
+    T, dk, dv = 3, 2, 2
+    q, k, v = rng.standard_normal((T, dk)), unit(rng.standard_normal((T, 1, dk))), rng.standard_normal((T, 1, dv))
+    beta, S0, dout = rng.uniform(0, 1, (T, 1)), rng.standard_normal((dk, dv)), rng.standard_normal((T, dv))
+    got = forms.recurrent_grad(q, k, v, beta, None, S0, dout, None)
+    f = lambda: loss(q, k, v, beta, None, S0, dout, np.zeros((dk, dv)), 1)
+    np.testing.assert_allclose(got[5], fd(f, S0), rtol=1e-6, atol=1e-7)
+
+
+def _wrong_sign(*a, **kw):
+    out = list(forms._recurrent_grad_ok(*a, **kw))
+    out[1] = -out[1]  # dk with the wrong sign
+    return tuple(out)
+
+
+def _dropped_beta(*a, **kw):
+    out = list(forms._recurrent_grad_ok(*a, **kw))
+    out[3] = np.zeros_like(out[3])
+    return tuple(out)
+
+
+@pytest.mark.parametrize("mutant", [_wrong_sign, _dropped_beta])
+def test_pins_catch_planted_mistakes(monkeypatch, mutant):
+    monkeypatch.setattr(forms, "_recurrent_grad_ok", forms.recurrent_grad, raising=False)
+    monkeypatch.setattr(forms, "recurrent_grad", mutant)
+    with pytest.raises(AssertionError):
+        test_gradients_match_finite_differences(2, True)
