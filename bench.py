@@ -654,6 +654,44 @@ def measure_kda(wr, dev, args, peaks):
             "bytes_per_step": nbytes, "gbs": gbs, "frac_of_measured_hbm": gbs / float(peaks["hbm_gbs"])}
 
 
+def measure_bwd(wr, dev, args, peaks):
+    """The gradients (``delta_bwd``, float32 CUDA-core kernel) on the headline
+    workload's shapes, timed with CUDA events: q, k, v, dout bf16, beta, g,
+    h0 and dhT float32; bytes = every input read once and every gradient
+    written once (float32)."""
+    stream = torch.cuda.current_stream(dev)
+    w = synth.WORKLOADS[HEADLINE]
+    if args.batch:
+        w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
+    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 17)
+    rn = lambda *shape: torch.randn(shape, generator=gen, device=dev)
+    k = rn(B, T, H, dk)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    q, v, dout = (rn(B, T, H, d).to(torch.bfloat16) for d in (dk, dv, dv))
+    beta = torch.sigmoid(rn(B, T, H))
+    g = torch.sigmoid(rn(B, T, H) * 2.0 + 3.0)
+    h0, dhT = rn(B, H, dk, dv) * w.h0_std, rn(B, H, dk, dv)
+    fn = lambda: wr.delta_bwd(q, k, v, beta, g, h0, dout, dhT)
+    fn()
+    torch.cuda.synchronize(dev)
+    steps = 2
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    tok = B * T * H
+    nbytes = tok * ((dk * 2 + dv * 2) * 2 + 2 * 4) + 2 * B * H * dk * dv * 4  # inputs
+    nbytes += tok * ((dk + dv) * 4 * 2 + 2 * 4) + B * H * dk * dv * 4          # gradients
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "kernel": "bwd_kernel (float32, CUDA cores)", "ms_per_step": ms,
+            "value": tok / (ms * 1e-3), "unit": UNIT, "steps": steps, "bytes_per_step": nbytes,
+            "gbs": gbs, "frac_of_measured_hbm": gbs / float(peaks["hbm_gbs"])}
+
+
 def run_ours(args, dist):
     import weight_rnn_gb300 as wr
 
@@ -680,6 +718,7 @@ def run_ours(args, dist):
     diagnostics = measure_diagnostics(wr, dev, args) if args.workload == "all" else None
     prologue = measure_prologue(wr, dev, args, peaks) if args.workload == "all" else None
     kda = measure_kda(wr, dev, args, peaks) if args.workload == "all" else None
+    bwd = measure_bwd(wr, dev, args, peaks) if args.workload == "all" else None
     w = synth.WORKLOADS[head_id]
     if args.batch:
         w = w.with_(B=args.batch, name=f"{w.name}_batch{args.batch}")
@@ -702,6 +741,7 @@ def run_ours(args, dist):
         "diagnostics": diagnostics,
         "prologue": prologue,
         "kda": kda,
+        "backward": bwd,
         "per_workload": {
             recs[i]["workload"]: {
                 "value": recs[i]["value"], "unit": UNIT,

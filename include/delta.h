@@ -136,6 +136,38 @@ int delta_fwd_kda(const void *q, const void *k, const void *v, const float *beta
                   delta_dtype dtype, struct CUstream_st *stream);
 
 /*
+ * delta_bwd -- gradients of delta_fwd's outputs and final state with
+ * respect to every input, for training.  The pages state no backward
+ * formulas: these are the reverse-mode derivatives of the recurrence of
+ * "DeltaProduct" §2.6 (gate once per token, then the n_h delta sub-steps,
+ * readout after the last), taken one sub-step at a time in float32.
+ *
+ *   q, k, v, beta, g, h0   as in delta_fwd (g and h0 may be NULL)
+ *   dout  [B, T, H, dv]    dtype    gradient of the loss w.r.t. out
+ *   dhT   [B, H, dk, dv]   float32  gradient w.r.t. hT, or NULL (=> 0)
+ *   grad_q    [B, T, H, dk]       float32  out
+ *   grad_k    [B, T, n_h, H, dk]  float32  out
+ *   grad_v    [B, T, n_h, H, dv]  float32  out
+ *   grad_beta [B, T, n_h, H]      float32  out
+ *   grad_g    [B, T, H]           float32  out, required when g is given (else unused)
+ *   grad_h0   [B, H, dk, dv]      float32  out, or NULL (=> not written)
+ *
+ * One CTA per (b, h) on the CUDA cores keeps the state and its gradient in
+ * shared memory; it runs the forward once storing the state every 64
+ * sub-steps, then walks the sequence backwards, recomputing 64 states at a
+ * time.  Scratch: B*H*(ceil(n_h*T/64) + 1 + 64)*dk*dv*4 bytes, stream-ordered
+ * from the pool delta_fwd uses, released before returning.  A correctness
+ * path (float32 throughout; no tensor cores).  dk, dv in {16, 32, 64, 128},
+ * n_h in [1, 4], any dtype; the grad_ outputs must overlap no input and no other
+ * output (DELTA_ERR_INVALID); every pointer 16-byte aligned.
+ */
+int delta_bwd(const void *q, const void *k, const void *v, const float *beta,
+              const float *g, const float *h0, const void *dout, const float *dhT,
+              float *grad_q, float *grad_k, float *grad_v, float *grad_beta,
+              float *grad_g, float *grad_h0, int B, int H, int T, int dk, int dv, int n_h,
+              delta_dtype dtype, struct CUstream_st *stream);
+
+/*
  * delta_prologue -- the input prologue on its own: the keys of "DeltaProduct"
  * §2.2, k = psi(x) / ||psi(x)||_2 over the key dimension with psi = SiLU,
  * the queries likewise (the query path of the layer design in "08 · linear
@@ -371,10 +403,11 @@ int delta_version(void);
 
 /*
  * delta_inject_failure -- test hook: the next `count` calls of delta_fwd,
- * delta_fwd_kda, delta_step_kda, delta_prologue, delta_fwd_prologue, delta_ut_transform, delta_fwd_with_ut, delta_step,
+ * delta_bwd, delta_fwd_kda, delta_step_kda, delta_prologue,
+ * delta_fwd_prologue, delta_ut_transform, delta_fwd_with_ut, delta_step,
  * delta_step_prologue, delta_state_erank and delta_attention_map (together)
- * return DELTA_ERR_CUDA, with "injected failure" in
- * delta_last_error(), right after their arguments pass validation and before
+ * return DELTA_ERR_CUDA, with "injected failure" in delta_last_error(),
+ * right after their arguments pass validation and before
  * anything is enqueued.  count = 0 clears a pending injection; count < 0 is
  * DELTA_ERR_INVALID.  The counter is process-wide.
  */

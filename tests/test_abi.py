@@ -361,3 +361,34 @@ def test_kda_entry_points_reject_before_launch(lib, kw, status):
 def test_kda_empty_problems_are_ok_without_gpu(lib):
     assert fwd_kda(lib, B=0) == wr.DELTA_OK
     assert step_kda(lib, H=0) == wr.DELTA_OK
+
+
+def bwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, beta=FAKE * 4, g=None, h0=None, dout=FAKE * 5,
+             dhT=None, gq=FAKE * 6, gk=FAKE * 7, gv=FAKE * 8, gb=FAKE * 9, gg=None, gh0=None,
+             B=1, H=1, T=4, dk=16, dv=16, n_h=1, dtype=wr.DELTA_F32)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.delta_bwd(*(vp(a[n]) for n in ("q", "k", "v", "beta", "g", "h0", "dout", "dhT",
+                                             "gq", "gk", "gv", "gb", "gg", "gh0")),
+                         a["B"], a["H"], a["T"], a["dk"], a["dv"], a["n_h"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=48), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(n_h=5), wr.DELTA_ERR_UNSUPPORTED),
+    (dict(T=-1), wr.DELTA_ERR_INVALID),
+    (dict(dtype=9), wr.DELTA_ERR_INVALID),
+    (dict(dout=None), wr.DELTA_ERR_INVALID),
+    (dict(gk=None), wr.DELTA_ERR_INVALID),
+    (dict(g=FAKE * 10), wr.DELTA_ERR_INVALID),          # g given without its gradient
+    (dict(gq=FAKE * 6 + 8), wr.DELTA_ERR_ALIGN),
+    (dict(gq=FAKE * 5 + 16), wr.DELTA_ERR_INVALID),     # grad_q overlaps dout
+    (dict(gv=FAKE * 7 + 16), wr.DELTA_ERR_INVALID),     # grad_v overlaps grad_k
+])
+def test_bwd_rejects_before_launch(lib, kw, status):
+    assert bwd(lib, **kw) == status
+
+
+def test_bwd_empty_batch_is_ok_without_gpu(lib):
+    assert bwd(lib, B=0) == wr.DELTA_OK

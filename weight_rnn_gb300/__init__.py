@@ -15,7 +15,7 @@ import threading
 
 import torch
 
-__all__ = ["delta_fwd", "delta_fwd_kda", "delta_step_kda", "delta_prologue",
+__all__ = ["delta_fwd", "delta_bwd", "delta_fwd_kda", "delta_step_kda", "delta_prologue",
            "delta_fwd_prologue", "delta_step_prologue",
            "delta_fwd_static_scratch", "delta_state_erank",
            "delta_attention_map", "delta_ut_transform", "delta_fwd_with_ut", "delta_step",
@@ -38,7 +38,7 @@ DELTA_BETA_2SIGMOID = 1
 _BETA_MAPS = {"sigmoid": DELTA_BETA_SIGMOID, "2sigmoid": DELTA_BETA_2SIGMOID}
 
 #: every extern "C" entry point include/delta.h declares
-EXPORTED_SYMBOLS = ("delta_fwd", "delta_fwd_kda", "delta_step_kda", "delta_prologue",
+EXPORTED_SYMBOLS = ("delta_fwd", "delta_bwd", "delta_fwd_kda", "delta_step_kda", "delta_prologue",
                     "delta_fwd_prologue", "delta_fwd_static_scratch",
                     "delta_ut_transform", "delta_fwd_with_ut",
                     "delta_fwd_kernel_count", "delta_step", "delta_step_prologue",
@@ -79,6 +79,8 @@ def load_library():
         p, i = ctypes.c_void_p, ctypes.c_int
         lib.delta_fwd.restype = i
         lib.delta_fwd.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.delta_bwd.restype = i
+        lib.delta_bwd.argtypes = [p] * 14 + [i] * 7 + [p]
         lib.delta_fwd_kda.restype = i
         lib.delta_fwd_kda.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p]
         lib.delta_step_kda.restype = i
@@ -231,6 +233,44 @@ def delta_fwd(q, k, v, beta, g=None, h0=None, out=None, hT=None, *, n_h=1,
     if st != DELTA_OK:
         raise DeltaError(st, delta_last_error())
     return out, hT
+
+
+def delta_bwd(q, k, v, beta, g, h0, dout, dhT=None, *, n_h=1, want_dh0=True, stream=None):
+    """Gradients of ``delta_fwd``'s out and hT (``delta_bwd``): given dout
+    [B,T,H,dv] (q's dtype) and dhT [B,H,dk,dv] float32 or None, returns
+    ``(dq, dk, dv, dbeta, dg, dh0)`` in float32 with the shapes of q, k, v,
+    beta, g (None without g) and h0 (None unless ``want_dh0``)."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("delta_bwd needs CUDA tensors")
+    dt = q.dtype
+    code = _dtype_code(dt)
+    if n_h == 1 and k.dim() == 4:
+        kshape, vshape, bshape = (B, T, H, dk), (B, T, H, v.shape[-1]), (B, T, H)
+    else:
+        kshape, vshape, bshape = (B, T, n_h, H, dk), (B, T, n_h, H, v.shape[-1]), (B, T, n_h, H)
+    dv = v.shape[-1]
+    _check(q, "q", (B, T, H, dk), dt, dev)
+    _check(k, "k", kshape, dt, dev)
+    _check(v, "v", vshape, dt, dev)
+    _check(beta, "beta", bshape, torch.float32, dev)
+    _check(g, "g", (B, T, H), torch.float32, dev)
+    _check(h0, "h0", (B, H, dk, dv), torch.float32, dev)
+    _check(dout, "dout", (B, T, H, dv), dt, dev)
+    _check(dhT, "dhT", (B, H, dk, dv), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    gq, gk, gv = torch.empty((B, T, H, dk), **f32), torch.empty(kshape, **f32), torch.empty(vshape, **f32)
+    gb = torch.empty(bshape, **f32)
+    gg = None if g is None else torch.empty((B, T, H), **f32)
+    gh0 = torch.empty((B, H, dk, dv), **f32) if want_dh0 else None
+    st = lib.delta_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(dout), _ptr(dhT),
+                       _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(gg), _ptr(gh0),
+                       B, H, T, dk, dv, n_h, code, _stream(dev, stream))
+    if st != DELTA_OK:
+        raise DeltaError(st, delta_last_error())
+    return gq, gk, gv, gb, gg, gh0
 
 
 def delta_fwd_kda(q, k, v, beta, alpha, h0=None, out=None, hT=None, *, n_h=1, chunk=64,

@@ -445,6 +445,72 @@ int delta_fwd_kda(const void *q, const void *k, const void *v, const float *beta
   return run_fwd(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int delta_bwd(const void *q, const void *k, const void *v, const float *beta, const float *g,
+              const float *h0, const void *dout, const float *dhT, float *dq, float *dk,
+              float *dv, float *dbeta, float *dg, float *dh0, int B, int H, int T, int dk_,
+              int dv_, int n_h, delta_dtype dtype, struct CUstream_st *stream) {
+  if (B < 0 || H < 0 || T < 0)
+    return fail(DELTA_ERR_INVALID, "negative size B=%d H=%d T=%d", B, H, T);
+  if (dtype != DELTA_F32 && dtype != DELTA_BF16)
+    return fail(DELTA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (!supported_dim(dk_) || !supported_dim(dv_))
+    return fail(DELTA_ERR_UNSUPPORTED, "dk=%d dv=%d not in {16,32,64,128}", dk_, dv_);
+  if (n_h < 1 || n_h > 4) return fail(DELTA_ERR_UNSUPPORTED, "n_h=%d not in [1,4]", n_h);
+  if ((int64_t)B * H >= (int64_t(1) << 31))
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large", (long long)B * H);
+  const int64_t BH = (int64_t)B * H, L = (int64_t)T * n_h, esz = dtype == DELTA_BF16 ? 2 : 4;
+  if (BH == 0) return DELTA_OK;
+  if (T > 0 && (!q || !k || !v || !beta || !dout || !dq || !dk || !dv || !dbeta))
+    return fail(DELTA_ERR_INVALID, "q, k, v, beta, dout, dq, dk, dv and dbeta must be non-NULL");
+  if (T > 0 && g && !dg) return fail(DELTA_ERR_INVALID, "dg must be non-NULL when g is given");
+  const void *ptrs[] = {q, k, v, beta, g, h0, dout, dhT, dq, dk, dv, dbeta, dg, dh0};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return fail(DELTA_ERR_ALIGN, "every pointer must be 16-byte aligned");
+  const int64_t DD = (int64_t)dk_ * dv_;
+  const Range ins[] = {range(q, BH * T * dk_ * esz), range(k, BH * L * dk_ * esz),
+                       range(v, BH * L * dv_ * esz), range(beta, BH * L * 4),
+                       range(g, g ? BH * T * 4 : 0), range(h0, h0 ? BH * DD * 4 : 0),
+                       range(dout, BH * T * dv_ * esz), range(dhT, dhT ? BH * DD * 4 : 0)};
+  const Range outs[] = {range(dq, BH * T * dk_ * 4), range(dk, BH * L * dk_ * 4),
+                        range(dv, BH * L * dv_ * 4), range(dbeta, BH * L * 4),
+                        range(g ? dg : nullptr, BH * T * 4), range(dh0, dh0 ? BH * DD * 4 : 0)};
+  for (int i = 0; i < 6; ++i) {
+    for (const Range &r : ins)
+      if (overlap(outs[i], r)) return fail(DELTA_ERR_INVALID, "an output overlaps an input");
+    for (int j = i + 1; j < 6; ++j)
+      if (overlap(outs[i], outs[j])) return fail(DELTA_ERR_INVALID, "two outputs overlap");
+  }
+  if (take_injection()) return fail(DELTA_ERR_CUDA, "injected failure (delta_inject_failure)");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    // no step: dh0 = dhT
+    if (!dh0) return DELTA_OK;
+    const cudaError_t e = dhT ? cudaMemcpyAsync(dh0, dhT, (size_t)(BH * DD * 4), cudaMemcpyDeviceToDevice, s)
+                              : cudaMemsetAsync(dh0, 0, (size_t)(BH * DD * 4), s);
+    return e == cudaSuccess ? DELTA_OK : cuda_fail(e, "dh0 copy");
+  }
+  delta::BwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.dout = dout;
+  a.beta = beta; a.g = g; a.h0 = h0; a.dhT = dhT;
+  a.gq = dq; a.gk = dk; a.gv = dv; a.gbeta = dbeta; a.gg = g ? dg : nullptr; a.gh0 = dh0;
+  a.B = B; a.H = H; a.T = T; a.dk = dk_; a.dv = dv_; a.n_h = n_h;
+  a.bf16 = dtype == DELTA_BF16;
+  int64_t second = 0;
+  const int64_t first = delta::bwd_scratch_floats(a, &second);
+  cudaMemPool_t pool;
+  cudaError_t err = scratch_pool(&pool);
+  if (err != cudaSuccess) return cuda_fail(err, "scratch pool");
+  void *scr = nullptr;
+  err = cudaMallocFromPoolAsync(&scr, (size_t)((first + second) * 4), pool, s);
+  if (err != cudaSuccess) return cuda_fail(err, "scratch allocation");
+  a.scratch = static_cast<float *>(scr);
+  a.scratch2 = a.scratch + first;
+  err = delta::launch_bwd(a, s);
+  const cudaError_t ef = cudaFreeAsync(scr, s);
+  if (err != cudaSuccess) return cuda_fail(err, "backward kernel launch");
+  return ef == cudaSuccess ? DELTA_OK : cuda_fail(ef, "scratch release");
+}
+
 int delta_prologue(const void *q_raw, const void *k_raw, const float *beta_raw, void *q_out,
                    void *k_out, float *beta_out, int B, int H, int T, int dk, int n_h,
                    delta_dtype dtype, delta_beta_map beta_map, struct CUstream_st *stream) {

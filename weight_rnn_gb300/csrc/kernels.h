@@ -51,6 +51,24 @@ struct PrologueArgs {
 };
 cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t s);
 
+// Gradients of the forward (float32, CUDA cores): inputs as FwdArgs plus the
+// loss gradients dout (dtype) and dhT (float32, or nullptr); outputs, all
+// float32: gq [B,T,H,dk], gk [B,L,H,dk], gv [B,L,H,dv], gbeta [B,L,H], gg
+// [B,T,H] (when g is set) and gh0 [B,H,dk,dv] (or nullptr).  scratch holds
+// bwd_scratch_floats() floats (block-start states), scratch2 `second` floats
+// (the states inside one block, per head).
+struct BwdArgs {
+  const void *q, *k, *v, *dout;
+  const float *beta, *g, *h0, *dhT;
+  float *gq, *gk, *gv, *gbeta, *gg, *gh0;
+  float *scratch, *scratch2;
+  int64_t B, H, T;
+  int dk, dv, n_h;
+  bool bf16;
+};
+int64_t bwd_scratch_floats(const BwdArgs &a, int64_t *second);
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t s);
+
 // Generic chunked forward on CUDA cores, float32 arithmetic, any supported
 // shape.  Returns the launch error (cudaSuccess if enqueued).
 cudaError_t launch_chunk_generic(const FwdArgs &a, cudaStream_t s);
