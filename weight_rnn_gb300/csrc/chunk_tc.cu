@@ -35,9 +35,9 @@
 // once per head.
 //
 // Warp roles (512 threads; one CTA per (b, h) head):
-//   warp 0       TMA producer: K/Q/V tiles (128-byte swizzle, 3 stages, the
-//                chunk after them prefetched into L2), the T tile (2-slot
-//                ring), beta / log-gate rows
+//   warp 0       TMA producer: K/Q/V tiles (128-byte swizzle, 3 stages)
+//                and the T tile (2-slot ring); beta is inside T, and the
+//                prep warps read the gate
 //   warps 1, 14, 15  MMA issuers (one thread each): the recurrence (U, V~,
 //                the state update); the outputs; the look-ahead G, W.
 //                Warp 1 owns the TMEM allocation.
