@@ -152,12 +152,18 @@ int delta_fwd_kda(const void *q, const void *k, const void *v, const float *beta
  *   grad_g    [B, T, H]           float32  out, required when g is given (else unused)
  *   grad_h0   [B, H, dk, dv]      float32  out, or NULL (=> not written)
  *
- * One CTA per (b, h) on the CUDA cores keeps the state and its gradient in
- * shared memory; it runs the forward once storing the state every 64
- * sub-steps, then walks the sequence backwards, recomputing 64 states at a
- * time.  Scratch: B*H*(ceil(n_h*T/64) + 1 + 64)*dk*dv*4 bytes, stream-ordered
- * from the pool delta_fwd uses, released before returning.  A correctness
- * path (float32 throughout; no tensor cores).  dk, dv in {16, 32, 64, 128},
+ * The update and its reverse act on each value column of the state alone,
+ * so every (b, h) is split into groups of 32 value columns (one group when
+ * dv <= 32), one CTA per group on the CUDA cores, holding its columns of the
+ * state and of its gradient in shared memory.  A CTA runs the forward once
+ * storing the state every 64 sub-steps, then walks the sequence backwards,
+ * recomputing 64 states at a time.  grad_q, grad_k, grad_beta and grad_g sum
+ * over the columns: with several groups each CTA writes partial sums, which a
+ * second kernel adds in group order, so results are deterministic.  Scratch:
+ * B*H*(ceil(n_h*T/64) + 1 + 64)*dk*dv*4 bytes, plus, when dv > 32, dv/32
+ * times the sizes of grad_q, grad_k, grad_beta and grad_g (each rounded up to
+ * 16 bytes); stream-ordered from the pool delta_fwd uses, released before
+ * returning.  A correctness path (float32 throughout; no tensor cores).  dk, dv in {16, 32, 64, 128},
  * n_h in [1, 4], any dtype; the grad_ outputs must overlap no input and no other
  * output (DELTA_ERR_INVALID); every pointer 16-byte aligned.
  */

@@ -51,6 +51,8 @@ def oracle_grads(inp, n_h):
     (torch.float32, 32, 16, 2, 70, True, False),
     (torch.float32, 64, 32, 3, 25, False, True),
     (torch.float32, 128, 128, 1, 150, True, True),   # more than two blocks of 64 sub-steps
+    (torch.float32, 128, 64, 1, 70, True, True),     # two groups of 32 value columns
+    (torch.float32, 16, 128, 2, 33, True, False),    # four groups, narrow keys
     (torch.bfloat16, 128, 128, 1, 66, True, True),
 ])
 def test_bwd_matches_oracle(dtype, dk, dv, n_h, T, gated, h0):

@@ -495,16 +495,19 @@ int delta_bwd(const void *q, const void *k, const void *v, const float *beta, co
   a.gq = dq; a.gk = dk; a.gv = dv; a.gbeta = dbeta; a.gg = g ? dg : nullptr; a.gh0 = dh0;
   a.B = B; a.H = H; a.T = T; a.dk = dk_; a.dv = dv_; a.n_h = n_h;
   a.bf16 = dtype == DELTA_BF16;
-  int64_t second = 0;
-  const int64_t first = delta::bwd_scratch_floats(a, &second);
+  if (delta::bwd_ctas(a) > INT32_MAX)
+    return fail(DELTA_ERR_UNSUPPORTED, "B*H=%lld too large for the backward grid", (long long)BH);
+  int64_t second = 0, third = 0;
+  const int64_t first = delta::bwd_scratch_floats(a, &second, &third);
   cudaMemPool_t pool;
   cudaError_t err = scratch_pool(&pool);
   if (err != cudaSuccess) return cuda_fail(err, "scratch pool");
   void *scr = nullptr;
-  err = cudaMallocFromPoolAsync(&scr, (size_t)((first + second) * 4), pool, s);
+  err = cudaMallocFromPoolAsync(&scr, (size_t)((first + second + third) * 4), pool, s);
   if (err != cudaSuccess) return cuda_fail(err, "scratch allocation");
   a.scratch = static_cast<float *>(scr);
   a.scratch2 = a.scratch + first;
+  a.scratch3 = a.scratch2 + second;
   err = delta::launch_bwd(a, s);
   const cudaError_t ef = cudaFreeAsync(scr, s);
   if (err != cudaSuccess) return cuda_fail(err, "backward kernel launch");

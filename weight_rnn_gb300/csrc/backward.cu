@@ -10,16 +10,22 @@
 //   dv = beta dS^T k;  dbeta = k^T dS r;  dk = beta (dS r - P dS^T k)
 //   dP = dS - beta k (k^T dS);  at a gate: dg = <dP, S_prev>, dS_prev = g dP
 //
-// One CTA per (b, h) keeps S, dS and the state a sub-step reads, P, [dk][dv]
-// in shared memory.  A first sweep runs the forward and stores the state at
+// The delta update acts on every column of the state alone (S[:, c] depends
+// only on k, beta and v_c), and so does its reverse: dS[:, c] needs nothing
+// from the other columns.  So each (b, h) is split into groups of kCols
+// value columns, one CTA per group, which keeps its columns of S, dS and of
+// the state a sub-step reads, P, in shared memory.  The gradients that sum
+// over the value columns (dq, dk, dbeta, dg) leave each CTA as partial sums,
+// which a second kernel adds up in group order (deterministic); dv and dh0
+// are per column.  A first sweep runs the forward and stores the state at
 // the start of every block of kBlk sub-steps in scratch; the backward sweep
 // walks the blocks in reverse, recomputes the block's states from its start
-// (stored per sub-step in scratch) and runs the reverse recurrence over them.
-// A correctness path: every step is a few dependent matrix-vector products
-// over the state.  The dims are powers of two (16 ... 128), so every index
-// below is a shift or a mask; each thread owns one column of the elementwise
-// passes, and both kinds of matrix-vector product split their sum over
-// kThreads / dim parts that meet in `part`.
+// (stored per sub-step in scratch) and runs the reverse recurrence over
+// them.  A correctness path: every step is a few dependent matrix-vector
+// products over the state.  The dims are powers of two (16 ... 128), so every
+// index below is a shift or a mask; each thread owns one column of the
+// elementwise passes, and both kinds of matrix-vector product split their
+// sum over several parts that meet in `part`.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -28,7 +34,10 @@ namespace delta {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBlk = 64;  // sub-steps per recomputed block
+constexpr int kBlk = 64;   // sub-steps per recomputed block
+constexpr int kCols = 32;  // value columns per CTA
+
+__host__ __device__ inline int col_groups(int dv) { return dv > kCols ? dv / kCols : 1; }
 
 __device__ __forceinline__ float ld(const void *p, int64_t i, bool bf16) {
   return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i])
@@ -48,47 +57,77 @@ __device__ __forceinline__ float block_sum(float x, float *red) {
   return t;
 }
 
+// sizes of the four summed gradients, each rounded up to 4 floats so that
+// every partial array starts 16-byte aligned
+struct PartSizes {
+  int64_t q, k, b, g;
+  __host__ __device__ PartSizes(const BwdArgs &a) {
+    const int64_t L = a.T * a.n_h;
+    q = (a.B * a.T * a.H * a.dk + 3) & ~int64_t(3);
+    k = (a.B * L * a.H * a.dk + 3) & ~int64_t(3);
+    b = (a.B * L * a.H + 3) & ~int64_t(3);
+    g = a.g ? (a.B * a.T * a.H + 3) & ~int64_t(3) : 0;
+  }
+  __host__ __device__ int64_t total() const { return q + k + b + g; }
+};
+
 __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdArgs a) {
   extern __shared__ float sm[];
   const int dk = a.dk, dv = a.dv, n_h = a.n_h, tid = threadIdx.x;
+  const int ng = col_groups(dv), dvs = dv / ng;  // this CTA's columns: cb .. cb + dvs - 1
   const int64_t T = a.T, H = a.H, L = a.T * a.n_h;
-  const int64_t bh = blockIdx.x, b = bh / H, h = bh % H;
-  const int DD = dk * dv;
-  const int lgv = __ffs(dv) - 1, lgk = __ffs(dk) - 1;
-  float *S = sm;              // [dk][dv]
-  float *dS = S + DD;         // [dk][dv]
-  float *Ps = dS + DD;        // [dk][dv]: the state the current sub-step read
+  const int64_t cta = blockIdx.x, bh = cta / ng, b = bh / H, h = bh % H;
+  const int grp = (int)(cta % ng), cb = grp * dvs;
+  const int DD = dk * dvs;
+  const int lgv = __ffs(dvs) - 1, lgk = __ffs(dk) - 1;
+  float *S = sm;              // [dk][dvs]
+  float *dS = S + DD;         // [dk][dvs]
+  float *Ps = dS + DD;        // [dk][dvs]: the state the current sub-step read
   float *kk = Ps + DD;        // [dk]
   float *qq = kk + dk;        // [dk]
   float *w = qq + dk;         // [dk]: dS r
-  float *vec = w + dk;        // [dv]: v, then r
-  float *u = vec + dv;        // [dv]: P^T k, dS^T k, do, ...
-  float *red = u + dv;        // [kThreads / 32]
+  float *vec = w + dk;        // [dvs]: v, then r
+  float *u = vec + dvs;       // [dvs]: dS^T k, do, ...
+  float *red = u + dvs;       // [kThreads / 32]
   float *part = red + kThreads / 32;  // [kThreads]
   const int64_t nblk = (L + kBlk - 1) / kBlk;
-  float *ckpt = a.scratch + bh * (nblk + 1) * (int64_t)DD;  // block starts
-  float *steps = a.scratch2 + bh * (int64_t)kBlk * DD;      // the states inside one block
+  float *ckpt = a.scratch + cta * (nblk + 1) * (int64_t)DD;  // block starts
+  float *steps = a.scratch2 + cta * (int64_t)kBlk * DD;      // the states inside one block
+  // the summed gradients: straight to the outputs with one group, else into
+  // this group's partial arrays
+  float *oq = a.gq, *ok = a.gk, *ob = a.gbeta, *og = a.gg;
+  if (ng > 1) {
+    const PartSizes ps(a);
+    float *base = a.scratch3 + grp * ps.total();
+    oq = base;
+    ok = base + ps.q;
+    ob = ok + ps.k;
+    og = a.g ? ob + ps.b : nullptr;
+  }
 
   // elementwise passes: this thread's column ec, rows er0, er0 + estep, ...
-  const int ec = tid & (dv - 1), er0 = tid >> lgv, estep = kThreads >> lgv;
-  // y[c] = sum_d M[d][c] x[d]; `out(c, y)` runs on threads c < dv
+  const int ec = tid & (dvs - 1), er0 = tid >> lgv, estep = kThreads >> lgv;
+  // state element (r, c) of this group in a [dk][dv] float32 array
+  auto gidx = [&](int r, int c) { return (int64_t)r * dv + cb + c; };
+  // y[c] = sum_d M[d][c] x[d]; `out(c, y)` runs on threads c < dvs
   auto col_product = [&](const float *M, const float *x, auto out) {
     const int np = kThreads >> lgv, len = dk / np, d0 = (tid >> lgv) * len;
     float acc = 0.f;
     for (int d = d0; d < d0 + len; ++d) acc = fmaf(M[(d << lgv) + ec], x[d], acc);
     part[tid] = acc;
     __syncthreads();
-    if (tid < dv) {
+    if (tid < dvs) {
       float y = 0.f;
       for (int q = 0; q < np; ++q) y += part[(q << lgv) + tid];
       out(tid, y);
     }
     __syncthreads();
   };
-  // y[r] = sum_c M[r][c] x[c]; each part walks its columns from a row-skewed
-  // start, so the lanes of a warp (consecutive rows) hit distinct banks
+  // y[r] = sum_c M[r][c] x[c] over this group's columns; each part walks its
+  // columns from a row-skewed start, so that the lanes of a warp
+  // (consecutive rows) hit distinct banks
   auto row_product = [&](const float *M, const float *x, auto out) {
-    const int r = tid & (dk - 1), np = kThreads >> lgk, len = dv / np, c0 = (tid >> lgk) * len;
+    const int r = tid & (dk - 1), np = kThreads >> lgk, len = dvs / np, c0 = (tid >> lgk) * len;
     float acc = 0.f;
     for (int j = 0; j < len; ++j) {
       const int c = c0 + ((j + r) & (len - 1));
@@ -105,7 +144,8 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdArgs a) {
   };
   auto load_kv = [&](int64_t e) {
     for (int d = tid; d < dk; d += kThreads) kk[d] = ld(a.k, ((b * L + e) * H + h) * dk + d, a.bf16);
-    for (int c = tid; c < dv; c += kThreads) vec[c] = ld(a.v, ((b * L + e) * H + h) * dv + c, a.bf16);
+    for (int c = tid; c < dvs; c += kThreads)
+      vec[c] = ld(a.v, ((b * L + e) * H + h) * dv + cb + c, a.bf16);
   };
   // r = v - M^T k into vec (vec holds v, kk holds k)
   auto residual = [&](const float *M) {
@@ -136,10 +176,8 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdArgs a) {
   };
 
   // ---- forward sweep: block starts into ckpt ----
-  for (int r = er0; r < dk; r += estep) {
-    const int i = (r << lgv) + ec;
-    S[i] = a.h0 ? a.h0[bh * DD + i] : 0.f;
-  }
+  for (int r = er0; r < dk; r += estep)
+    S[(r << lgv) + ec] = a.h0 ? a.h0[bh * dk * dv + gidx(r, ec)] : 0.f;
   __syncthreads();
   for (int64_t blk = 0; blk < nblk; ++blk) {
     float *dst = ckpt + blk * DD;
@@ -147,10 +185,8 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdArgs a) {
     for (int64_t e = blk * kBlk; e < L && e < (blk + 1) * kBlk; ++e) fwd_step(e, nullptr);
   }
   // ---- backward sweep ----
-  for (int r = er0; r < dk; r += estep) {
-    const int i = (r << lgv) + ec;
-    dS[i] = a.dhT ? a.dhT[bh * DD + i] : 0.f;
-  }
+  for (int r = er0; r < dk; r += estep)
+    dS[(r << lgv) + ec] = a.dhT ? a.dhT[bh * dk * dv + gidx(r, ec)] : 0.f;
   __syncthreads();
   bool preloaded = false;  // Ps already holds the state the next sub-step read
   for (int64_t blk = nblk - 1; blk >= 0; --blk) {
@@ -185,9 +221,10 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdArgs a) {
       // readout at the token's last sub-step: dq = S do, dS += q do^T
       if ((int)(e % n_h) == n_h - 1) {
         for (int d = tid; d < dk; d += kThreads) qq[d] = ld(a.q, ((b * T + t) * H + h) * dk + d, a.bf16);
-        for (int c = tid; c < dv; c += kThreads) u[c] = ld(a.dout, ((b * T + t) * H + h) * dv + c, a.bf16);
+        for (int c = tid; c < dvs; c += kThreads)
+          u[c] = ld(a.dout, ((b * T + t) * H + h) * dv + cb + c, a.bf16);
         __syncthreads();
-        float *gq = a.gq + ((b * T + t) * H + h) * dk;
+        float *gq = oq + ((b * T + t) * H + h) * dk;
         row_product(S, u, [&](int d, float y) { gq[d] = y; });
         const float uo = u[ec];
         for (int r = er0; r < dk; r += estep) {
@@ -197,7 +234,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdArgs a) {
         __syncthreads();
       }
       // u = dS^T k, dv = beta u
-      float *gv = a.gv + ((b * L + e) * H + h) * dv;
+      float *gv = a.gv + ((b * L + e) * H + h) * dv + cb;
       col_product(dS, kk, [&](int c, float y) {
         u[c] = y;
         gv[c] = bt * y;
@@ -208,9 +245,9 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdArgs a) {
       float pk = 0.f;
       for (int d = tid; d < dk; d += kThreads) pk = fmaf(kk[d], w[d], pk);
       const float dbeta = block_sum(pk, red);
-      if (tid == 0) a.gbeta[(b * L + e) * H + h] = dbeta;
+      if (tid == 0) ob[(b * L + e) * H + h] = dbeta;
       // dk = beta (dS r - P dS^T k)
-      float *gk = a.gk + ((b * L + e) * H + h) * dk;
+      float *gk = ok + ((b * L + e) * H + h) * dk;
       row_product(Ps, u, [&](int d, float y) { gk[d] = bt * (w[d] - y); });
       // dP = dS - beta k (k^T dS) = dS - beta k u^T
       {
@@ -250,35 +287,83 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(BwdArgs a) {
           }
         }
         const float dg = block_sum(pdot, red);
-        if (tid == 0) a.gg[(b * T + t) * H + h] = dg;
+        if (tid == 0) og[(b * T + t) * H + h] = dg;
         for (int r = er0; r < dk; r += estep) dS[(r << lgv) + ec] *= gt;
         __syncthreads();
       }
     }
   }
   if (a.gh0)
-    for (int r = er0; r < dk; r += estep) {
-      const int i = (r << lgv) + ec;
-      a.gh0[bh * DD + i] = dS[i];
+    for (int r = er0; r < dk; r += estep) a.gh0[bh * dk * dv + gidx(r, ec)] = dS[(r << lgv) + ec];
+}
+
+// out[i] = sum over the groups g = 0, 1, ... of part[g * stride + i], in
+// group order; n floats (16-byte aligned arrays, float4 where n allows)
+__global__ void __launch_bounds__(256) bwd_sum_kernel(const float *__restrict__ part, int64_t stride,
+                                                      int ng, float *__restrict__ out, int64_t n) {
+  const int64_t n4 = n >> 2;
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += step) {
+    float4 acc = reinterpret_cast<const float4 *>(part)[i];
+    for (int g = 1; g < ng; ++g) {
+      const float4 x = reinterpret_cast<const float4 *>(part + g * stride)[i];
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
     }
+    reinterpret_cast<float4 *>(out)[i] = acc;
+  }
+  for (int64_t i = 4 * n4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += step) {
+    float acc = part[i];
+    for (int g = 1; g < ng; ++g) acc += part[g * stride + i];
+    out[i] = acc;
+  }
 }
 
 }  // namespace
 
-int64_t bwd_scratch_floats(const BwdArgs &a, int64_t *second) {
+int64_t bwd_ctas(const BwdArgs &a) { return a.B * a.H * col_groups(a.dv); }
+
+int64_t bwd_scratch_floats(const BwdArgs &a, int64_t *second, int64_t *third) {
   const int64_t DD = (int64_t)a.dk * a.dv, L = a.T * a.n_h;
   const int64_t nblk = (L + kBlk - 1) / kBlk;
+  const int ng = col_groups(a.dv);
   *second = a.B * a.H * (int64_t)kBlk * DD;
+  *third = ng > 1 ? ng * PartSizes(a).total() : 0;
   return a.B * a.H * (nblk + 1) * DD;
 }
 
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t s) {
+  const int ng = col_groups(a.dv), dvs = a.dv / ng;
   const size_t smem =
-      (size_t)(3 * a.dk * a.dv + 3 * a.dk + 2 * a.dv + kThreads / 32 + kThreads) * sizeof(float);
+      (size_t)(3 * a.dk * dvs + 3 * a.dk + 2 * dvs + kThreads / 32 + kThreads) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  bwd_kernel<<<(unsigned)(a.B * a.H), kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  bwd_kernel<<<(unsigned)(a.B * a.H * ng), kThreads, smem, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess || ng == 1) return e;
+  // add up the groups' partial sums of the gradients that sum over columns
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const PartSizes ps(a);
+  const int64_t L = a.T * a.n_h;
+  struct {
+    int64_t off, n;
+    float *out;
+  } parts[4] = {{0, a.B * a.T * a.H * a.dk, a.gq},
+                {ps.q, a.B * L * a.H * a.dk, a.gk},
+                {ps.q + ps.k, a.B * L * a.H, a.gbeta},
+                {ps.q + ps.k + ps.b, a.g ? a.B * a.T * a.H : 0, a.gg}};
+  for (const auto &p : parts) {
+    if (p.n == 0) continue;
+    int64_t blocks = (p.n / 4 + 255) / 256;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    if (blocks < 1) blocks = 1;
+    bwd_sum_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.scratch3 + p.off, ps.total(), ng, p.out, p.n);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace delta

@@ -56,17 +56,19 @@ cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t s);
 // float32: gq [B,T,H,dk], gk [B,L,H,dk], gv [B,L,H,dv], gbeta [B,L,H], gg
 // [B,T,H] (when g is set) and gh0 [B,H,dk,dv] (or nullptr).  scratch holds
 // bwd_scratch_floats() floats (block-start states), scratch2 `second` floats
-// (the states inside one block, per head).
+// (the states inside one block), scratch3 `third` floats (the per-column-group
+// partial sums of gq, gk, gbeta and gg; none when one group covers dv).
 struct BwdArgs {
   const void *q, *k, *v, *dout;
   const float *beta, *g, *h0, *dhT;
   float *gq, *gk, *gv, *gbeta, *gg, *gh0;
-  float *scratch, *scratch2;
+  float *scratch, *scratch2, *scratch3;
   int64_t B, H, T;
   int dk, dv, n_h;
   bool bf16;
 };
-int64_t bwd_scratch_floats(const BwdArgs &a, int64_t *second);
+int64_t bwd_scratch_floats(const BwdArgs &a, int64_t *second, int64_t *third);
+int64_t bwd_ctas(const BwdArgs &a);  // the grid of the backward kernel
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t s);
 
 // Generic chunked forward on CUDA cores, float32 arithmetic, any supported
