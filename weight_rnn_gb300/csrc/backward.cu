@@ -71,7 +71,7 @@ struct PartSizes {
   __host__ __device__ int64_t total() const { return q + k + b + g; }
 };
 
-__global__ void __launch_bounds__(kThreads) bwd_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) bwd_kernel(BwdArgs a) {
   extern __shared__ float sm[];
   const int dk = a.dk, dv = a.dv, n_h = a.n_h, tid = threadIdx.x;
   const int ng = col_groups(dv), dvs = dv / ng;  // this CTA's columns: cb .. cb + dvs - 1
