@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(BwdArgs a) {
 
 // out[i] = sum over the groups g = 0, 1, ... of part[g * stride + i], in
 // group order; n floats (16-byte aligned arrays, float4 where n allows)
-__global__ void __launch_bounds__(256) bwd_sum_kernel(const float *__restrict__ part, int64_t stride,
+__global__ void __launch_bounds__(256, 4) bwd_sum_kernel(const float *__restrict__ part, int64_t stride,
                                                       int ng, float *__restrict__ out, int64_t n) {
   const int64_t n4 = n >> 2;
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
