@@ -30,7 +30,10 @@
 // This kernel serves every supported shape and both I/O dtypes; it is the
 // float32 path (accurate to ~1e-6) and the fallback for shapes the
 // tensor-core kernel does not take.  One CTA handles one (b, h) head and a
-// slab of BV value columns; every array lives in shared memory.
+// slab of BV value columns; every array lives in shared memory.  The rows of
+// K (and of the channel-wise cumulative gate) are padded to dk + 1 floats:
+// forming A and P, the lanes of a warp read one key channel of 32 different
+// rows, which an unpadded stride of dk floats would put in one bank.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -54,15 +57,15 @@ __device__ __forceinline__ void store_io(void *p, int64_t i, float x, bool bf16)
 }
 
 struct Smem {
-  float *S, *K, *Q, *V, *A, *X, *P, *W, *U, *beta, *gc, *gcd;
+  float *S, *K, *Q, *V, *A, *X, *P, *W, *U, *beta, *gc, *eg, *ed, *gcd;
   static __host__ __device__ size_t floats(int C, int dk, int BV, bool kda) {
-    return (size_t)dk * BV + 3 * (size_t)C * dk + 2 * (size_t)C * BV +
-           3 * (size_t)C * C + 2 * (size_t)C + (kda ? (size_t)C * dk : 0);
+    return (size_t)dk * BV + (size_t)C * (dk + 1) + 2 * (size_t)C * dk + 2 * (size_t)C * BV +
+           3 * (size_t)C * C + 4 * (size_t)C + (kda ? (size_t)C * (dk + 1) : 0);
   }
   __device__ Smem(float *base, int C, int dk, int BV) {
     S = base;
-    K = S + dk * BV;
-    Q = K + C * dk;
+    K = S + dk * BV;        // [C][dk + 1]
+    Q = K + C * (dk + 1);
     W = Q + C * dk;
     V = W + C * dk;
     U = V + C * BV;
@@ -71,7 +74,9 @@ struct Smem {
     P = X + C * C;
     beta = P + C * C;
     gc = beta + C;
-    gcd = gc + C;  // [C][dk], channel-wise gate only
+    eg = gc + C;   // exp(gc_j), scalar gate
+    ed = eg + C;   // exp(gc_C - gc_j), scalar gate
+    gcd = ed + C;  // [C][dk + 1], channel-wise gate only
   }
 };
 
@@ -85,6 +90,7 @@ chunk_generic_kernel(FwdArgs a, int BV) {
   const int64_t bh = blockIdx.x;
   const int64_t b = bh / a.H, h = bh % a.H;
   const int v0 = blockIdx.y * BV;
+  const int ks = dk + 1;  // row stride of K and gcd
   const int64_t L = a.L, T = a.T, H = a.H;
   constexpr bool kda = KDA;  // channel-wise gate a.alpha (else the scalar a.g)
 
@@ -108,7 +114,7 @@ chunk_generic_kernel(FwdArgs a, int BV) {
         if ((int)(e % n_h) == n_h - 1)
           qv = load_io(a.q, ((b * T + e / n_h) * H + h) * dk + d, a.bf16);
       }
-      sm.K[i] = kv;
+      sm.K[r * ks + d] = kv;
       sm.Q[i] = qv;
     }
     for (int i = tid; i < C * BV; i += kThreads) {
@@ -138,6 +144,11 @@ chunk_generic_kernel(FwdArgs a, int BV) {
           sm.gc[r] = acc;
         }
       }
+      __syncthreads();
+      for (int j = tid; j < C; j += kThreads) {
+        sm.eg[j] = expf(sm.gc[j]);
+        sm.ed[j] = expf(sm.gc[C - 1] - sm.gc[j]);
+      }
     } else {
       for (int d = tid; d < dk; d += kThreads) {
         float acc = 0.0f;
@@ -145,7 +156,7 @@ chunk_generic_kernel(FwdArgs a, int BV) {
           const int64_t e = e0 + r;
           if (e < L && (e % n_h) == 0)
             acc += fmaxf(logf(a.alpha[((b * T + e / n_h) * H + h) * dk + d]), kLogGateFloor);
-          sm.gcd[r * dk + d] = acc;
+          sm.gcd[r * ks + d] = acc;
         }
       }
     }
@@ -158,8 +169,8 @@ chunk_generic_kernel(FwdArgs a, int BV) {
         const float gam = expf(sm.gc[r] - sm.gc[j]);
         float kk = 0.0f, qk = 0.0f;
         for (int d = 0; d < dk; ++d) {
-          const float kj = sm.K[j * dk + d];
-          kk = fmaf(sm.K[r * dk + d], kj, kk);
+          const float kj = sm.K[j * ks + d];
+          kk = fmaf(sm.K[r * ks + d], kj, kk);
           qk = fmaf(sm.Q[r * dk + d], kj, qk);
         }
         pv = qk * gam;
@@ -168,8 +179,8 @@ chunk_generic_kernel(FwdArgs a, int BV) {
         // the ratio of each channel's decay inside the sum (exponent <= 0)
         float kk = 0.0f, qk = 0.0f;
         for (int d = 0; d < dk; ++d) {
-          const float kj = sm.K[j * dk + d] * expf(sm.gcd[r * dk + d] - sm.gcd[j * dk + d]);
-          kk = fmaf(sm.K[r * dk + d], kj, kk);
+          const float kj = sm.K[j * ks + d] * expf(sm.gcd[r * ks + d] - sm.gcd[j * ks + d]);
+          kk = fmaf(sm.K[r * ks + d], kj, kk);
           qk = fmaf(sm.Q[r * dk + d], kj, qk);
         }
         pv = qk;
@@ -197,7 +208,7 @@ chunk_generic_kernel(FwdArgs a, int BV) {
       const int r = i / dk, d = i % dk;
       float acc = 0.0f;
       for (int j = 0; j <= r; ++j)
-        acc = fmaf(sm.A[r * C + j], sm.K[j * dk + d] * expf(kda ? sm.gcd[j * dk + d] : sm.gc[j]), acc);
+        acc = fmaf(sm.A[r * C + j], sm.K[j * ks + d] * (kda ? expf(sm.gcd[j * ks + d]) : sm.eg[j]), acc);
       sm.W[i] = acc;
     }
     for (int i = tid; i < C * BV; i += kThreads) {
@@ -223,10 +234,10 @@ chunk_generic_kernel(FwdArgs a, int BV) {
       float qs = 0.0f;
       if (kda) {
         for (int d = 0; d < dk; ++d)
-          qs = fmaf(sm.Q[r * dk + d] * expf(sm.gcd[r * dk + d]), sm.S[d * BV + c], qs);
+          qs = fmaf(sm.Q[r * dk + d] * expf(sm.gcd[r * ks + d]), sm.S[d * BV + c], qs);
       } else {
         for (int d = 0; d < dk; ++d) qs = fmaf(sm.Q[r * dk + d], sm.S[d * BV + c], qs);
-        qs *= expf(sm.gc[r]);
+        qs *= sm.eg[r];
       }
       float acc = qs;
       for (int j = 0; j <= r; ++j) acc = fmaf(sm.P[r * C + j], sm.U[j * BV + c], acc);
@@ -236,12 +247,17 @@ chunk_generic_kernel(FwdArgs a, int BV) {
     // ---- S <- exp(gc_C) S + (K * exp(gc_C - gc))^T Vt ----
     for (int i = tid; i < dk * BV; i += kThreads) {
       const int d = i / BV, c = i % BV;
-      const float *g = kda ? sm.gcd + d : sm.gc;  // this row's cumulative log gate
-      const int gs = kda ? dk : 1;
-      const float gl = g[(C - 1) * gs];
-      float acc = sm.S[i] * expf(gl);
-      for (int j = 0; j < C; ++j)
-        acc = fmaf(sm.K[j * dk + d] * expf(gl - g[j * gs]), sm.U[j * BV + c], acc);
+      float acc;
+      if (kda) {
+        const float *g = sm.gcd + d;  // this row's cumulative log gate
+        const float gl = g[(C - 1) * ks];
+        acc = sm.S[i] * expf(gl);
+        for (int j = 0; j < C; ++j)
+          acc = fmaf(sm.K[j * ks + d] * expf(gl - g[j * ks]), sm.U[j * BV + c], acc);
+      } else {
+        acc = sm.S[i] * sm.eg[C - 1];
+        for (int j = 0; j < C; ++j) acc = fmaf(sm.K[j * ks + d] * sm.ed[j], sm.U[j * BV + c], acc);
+      }
       sm.S[i] = acc;
     }
   }
