@@ -48,7 +48,7 @@ def test_decode_bytes_per_call():
 
 def test_code_hash_ignores_comments_and_blank_lines():
     a = "int f(int x) {\n  return x + 1;  // one more\n}\n"
-    b = "// a header comment\nint f(int x) {\n\n  /* the\n     result */ return x + 1;\n}\n"
+    b = "// a header comment\n/* spanning\n   lines */\nint f(int x) {\n\n  return x + 1;\n}\n"
     c = "int f(int x) {\n  return x + 2;\n}\n"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
