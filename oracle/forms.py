@@ -406,3 +406,114 @@ def recurrent_grad(q, k, v, beta, g, S0, dout, dST=None, n_h=1):
     loss.backward()
     grad = lambda x: None if x is None else x.grad.detach().numpy().copy()
     return grad(tq), grad(tk), grad(tv), grad(tb), grad(tg), grad(tS0)
+
+
+def ut_chunk_grad(q, k, v, beta, log_g=None, S0=None, dout=None, dST=None, C=16):
+    """The chunked backward: gradients of L = <dout, o> + <dST, S_T> through
+    ut_chunk ([DR] §2.2-§2.3 with the §3 gate), one chunk at a time in
+    reverse, by differentiating each chunk's matrix products (the pages state
+    no backward formulas; this is the chain rule applied to the chunkwise
+    form, written out by hand).  With the forward quantities of a chunk
+    (gamma = exp(gc), gamma_C its last entry, Qg = Q * gamma, Kg = K * gamma,
+    Kd = K * gamma_C / gamma, P = (Q K^T) * Gam * M, X = (I + A)^{-1},
+    T = X diag(beta), W = T Kg, U = T V, Vt = U - W S) and dS the gradient
+    arriving at the chunk's end state:
+        dVt = Kd dS + P^T dO;   dKd = Vt dS^T;   d gamma_C = <S, dS>
+        dS_prev = gamma_C dS + Qg^T dO - W^T dVt
+        dQg = dO S^T;  dP = (dO Vt^T) * M
+        dT = dVt V^T - dVt S^T Kg^T;  dV = T^T dVt;  dKg = -T^T dVt S^T
+        dX = dT diag(beta);  dbeta_j = sum_i X_ij dT_ij;  dA = -(X^T dX X^T) * M_strict
+    then A, P, Qg, Kg and Kd give dK, dQ, dbeta and the gradient of every
+    exponential of gc, and d log_g is the reverse cumulative sum of dgc within
+    the chunk.  Shapes and padding as ut_chunk (n_h = 1: every row is read
+    out).  Returns dq, dk, dv, dbeta, dlog_g, dS0 (float64)."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    L, dk = k.shape
+    dv = v.shape[1]
+    log_g = np.zeros(L) if log_g is None else np.asarray(log_g, dtype=np.float64)
+    dout = np.zeros((L, dv)) if dout is None else np.asarray(dout, dtype=np.float64)
+    NT = -(-L // C)
+    Lp = NT * C
+    pad = Lp - L
+
+    def padrows(x):
+        return np.concatenate([x, np.zeros((pad,) + x.shape[1:])]) if pad else x
+
+    Q, K, V, dO = padrows(q), padrows(k), padrows(v), padrows(dout)
+    bt, lg = padrows(np.asarray(beta, dtype=np.float64)), padrows(log_g)
+    strict = np.tril(np.ones((C, C), dtype=bool), -1)
+    incl = np.tril(np.ones((C, C), dtype=bool))
+    # forward: the state at the start of every chunk
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    starts = []
+    Ts = ut_transform(K, bt, lg, C)
+    for n in range(NT):
+        sl = slice(n * C, (n + 1) * C)
+        starts.append(S)
+        gc = np.cumsum(lg[sl])
+        Kc, Vc = K[sl], V[sl]
+        Vt = Ts[n] @ Vc - (Ts[n] @ (Kc * np.exp(gc)[:, None])) @ S
+        S = np.exp(gc[-1]) * S + (Kc * np.exp(gc[-1] - gc)[:, None]).T @ Vt
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    dB, dLG = np.zeros(Lp), np.zeros(Lp)
+    dS = np.zeros((dk, dv)) if dST is None else np.array(dST, dtype=np.float64)
+    for n in reversed(range(NT)):
+        sl = slice(n * C, (n + 1) * C)
+        S = starts[n]
+        Qc, Kc, Vc, dOc, bc = Q[sl], K[sl], V[sl], dO[sl], bt[sl]
+        gc = np.cumsum(lg[sl])
+        gam, gC = np.exp(gc), np.exp(gc[-1])
+        dec = np.exp(gc[-1] - gc)
+        Gam = np.exp(np.where(incl, gc[:, None] - gc[None, :], -np.inf))
+        KK, QK = Kc @ Kc.T, Qc @ Kc.T
+        A = np.where(strict, bc[:, None] * Gam * KK, 0.0)
+        X = solve_triangular(np.eye(C) + A, np.eye(C), lower=True, unit_diagonal=True)
+        Tm = X * bc[None, :]
+        Qg, Kg, Kd = Qc * gam[:, None], Kc * gam[:, None], Kc * dec[:, None]
+        W = Tm @ Kg
+        Vt = Tm @ Vc - W @ S
+        P = QK * Gam
+        # state update S' = gamma_C S + Kd^T Vt
+        dgC = np.sum(S * dS)
+        dKd = Vt @ dS.T
+        dVt = Kd @ dS
+        dSp = gC * dS
+        # readout O = Qg S + P Vt
+        dQg = dOc @ S.T
+        dSp += Qg.T @ dOc
+        dP = np.where(incl, dOc @ Vt.T, 0.0)
+        dVt += P.T @ dOc
+        # Vt = U - W S, U = T V, W = T Kg
+        dW = -dVt @ S.T
+        dSp -= W.T @ dVt
+        dT = dVt @ Vc.T + dW @ Kg.T
+        dV[sl] = Tm.T @ dVt
+        dKg = Tm.T @ dW
+        # T = X diag(beta), X = (I + A)^{-1}
+        dX = dT * bc[None, :]
+        dbeta = np.sum(X * dT, axis=0)
+        dA = np.where(strict, -(X.T @ dX @ X.T), 0.0)
+        # A_ij = beta_i Gam_ij (k_i . k_j), i > j
+        dbeta += np.sum(dA * Gam * KK, axis=1)
+        E = dA * Gam * bc[:, None]
+        dKc = E @ Kc + E.T @ Kc
+        dGam = dA * bc[:, None] * KK
+        # P_ij = (q_i . k_j) Gam_ij, j <= i
+        F = dP * Gam
+        dQc = F @ Kc
+        dKc += F.T @ Qc
+        dGam += dP * QK
+        # the scaled copies of Q and K
+        dQc += dQg * gam[:, None]
+        dKc += dKg * gam[:, None] + dKd * dec[:, None]
+        dgam = np.sum(dQg * Qc, axis=1) + np.sum(dKg * Kc, axis=1)
+        ddec = np.sum(dKd * Kc, axis=1)
+        # every exponential of gc
+        dgc = dgam * gam - ddec * dec
+        dgc[-1] += dgC * gC + np.sum(ddec * dec)
+        Z = np.where(incl, dGam * Gam, 0.0)
+        dgc += Z.sum(axis=1) - Z.sum(axis=0)
+        dLG[sl] = np.cumsum(dgc[::-1])[::-1]
+        dQ[sl], dK[sl], dB[sl] = dQc, dKc, dbeta
+        dS = dSp
+    return dQ[:L], dK[:L], dV[:L], dB[:L], dLG[:L], dS

@@ -91,3 +91,67 @@ def test_pins_catch_planted_mistakes(monkeypatch, mutant):
     monkeypatch.setattr(forms, "recurrent_grad", mutant)
     with pytest.raises(AssertionError):
         test_gradients_match_finite_differences(2, True)
+
+
+# ---- the chunked backward (forms.ut_chunk_grad) ----
+
+def _chunk_case(seed, L, dk, dv, gated):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((L, dk))
+    k = unit(rng.standard_normal((L, dk)))
+    v = rng.standard_normal((L, dv))
+    beta = rng.uniform(0.1, 1.8, L)
+    lg = np.log(rng.uniform(0.4, 1.0, L)) if gated else None
+    S0 = rng.standard_normal((dk, dv)) * 0.5
+    dout = rng.standard_normal((L, dv))
+    dST = rng.standard_normal((dk, dv))
+    return q, k, v, beta, lg, S0, dout, dST
+
+
+@pytest.mark.parametrize("L,C,gated", [(7, 4, True), (8, 4, False), (5, 8, True)])
+def test_chunked_backward_matches_finite_differences(L, C, gated):
+    # several chunks and a ragged tail (L = 7, C = 4), one chunk, a part chunk
+    dk, dv = 3, 2
+    q, k, v, beta, lg, S0, dout, dST = _chunk_case(60 + L + C, L, dk, dv, gated)
+    got = forms.ut_chunk_grad(q, k, v, beta, lg, S0, dout, dST, C=C)
+    f = lambda: loss(q, k[:, None], v[:, None], beta[:, None],
+                     None if lg is None else np.exp(lg), S0, dout, dST, 1)
+    for name, x, gx in (("q", q, got[0]), ("k", k, got[1]), ("v", v, got[2]),
+                        ("beta", beta, got[3]), ("S0", S0, got[5])):
+        np.testing.assert_allclose(gx, fd(f, x), rtol=1e-6, atol=1e-7, err_msg=name)
+    if gated:
+        # the gradient with respect to log g
+        np.testing.assert_allclose(got[4], fd(f, lg), rtol=1e-6, atol=1e-7, err_msg="log g")
+
+
+@pytest.mark.parametrize("L,C", [(37, 8), (33, 16), (16, 16)])
+def test_chunked_backward_agrees_with_the_recurrent_gradients(L, C):
+    dk, dv = 8, 6
+    q, k, v, beta, lg, S0, dout, dST = _chunk_case(70 + L, L, dk, dv, True)
+    g = np.exp(lg)
+    ref = forms.recurrent_grad(q, k[:, None], v[:, None], beta[:, None], g, S0, dout, dST)
+    got = forms.ut_chunk_grad(q, k, v, beta, lg, S0, dout, dST, C=C)
+    pairs = ((got[0], ref[0]), (got[1], ref[1][:, 0]), (got[2], ref[2][:, 0]),
+             (got[3], ref[3][:, 0]), (got[4], ref[4] * g), (got[5], ref[5]))
+    for x, r in pairs:
+        np.testing.assert_allclose(x, r, rtol=1e-10, atol=1e-12)
+
+
+def _index_slip(*a, **kw):
+    out = list(forms._ut_chunk_grad_ok(*a, **kw))
+    out[4] = np.roll(out[4], 1)  # d log g one row off
+    return tuple(out)
+
+
+def _swapped_operands(*a, **kw):
+    out = list(forms._ut_chunk_grad_ok(*a, **kw))
+    out[0], out[1] = out[1], out[0]  # dq and dk exchanged
+    return tuple(out)
+
+
+@pytest.mark.parametrize("mutant", [_index_slip, _swapped_operands])
+def test_chunked_pins_catch_planted_mistakes(monkeypatch, mutant):
+    monkeypatch.setattr(forms, "_ut_chunk_grad_ok", forms.ut_chunk_grad, raising=False)
+    monkeypatch.setattr(forms, "ut_chunk_grad", mutant)
+    with pytest.raises(AssertionError):
+        test_chunked_backward_matches_finite_differences(7, 4, True)
