@@ -148,8 +148,87 @@ def cpu_model() -> str:
     return "unknown"
 
 
+class NvmlPoller:
+    """Read-only clock, power and clock-event-reason queries through the
+    driver's NVML library (ctypes), polled about every millisecond from a
+    thread, each sample tagged with whether the timed region was running.
+    Any failure (no library, no device, a query error) leaves `ok` False or
+    ends the polling; nothing here changes a GPU setting."""
+
+    CLOCK_SM = 1  # nvmlClockType_t: the SM clock
+    # nvmlClocksEventReasons bits that the timing rules name
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, bus_id, lib=None):
+        import ctypes
+        self.ct = ctypes
+        self.ok = False
+        self.samples = []  # (sm_mhz, max_mhz, watts, reason_bits, in_region)
+        self.in_region = False
+        self._stop = threading.Event()
+        self.thread = None
+        try:
+            self.lib = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.h)) != 0:
+                return
+            self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = self.sample() is not None
+        except Exception:
+            self.ok = False
+
+    def sample(self):
+        ct = self.ct
+        mhz, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if (self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(mhz)) != 0 or
+                self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ct.byref(mx)) != 0):
+            return None
+        if self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw)) != 0:
+            mw.value = 0
+        if self._reasons(self.h, ct.byref(rs)) != 0:
+            rs.value = 0
+        return (float(mhz.value), float(mx.value), mw.value / 1000.0, int(rs.value))
+
+    def _run(self):
+        try:
+            while not self._stop.is_set():
+                smp = self.sample()
+                if smp is None:
+                    return
+                self.samples.append(smp + (self.in_region,))
+                time.sleep(0.0005)
+        except Exception:
+            return
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        try:
+            self.lib.nvmlShutdown()
+        except Exception:
+            pass
+        loaded = [x for x in self.samples if x[4]]
+        use = loaded or self.samples
+        reasons = sorted({name for x in use for bit, name in self.REASONS.items() if x[3] & bit})
+        return {"sm_mhz": statistics.median(x[0] for x in use) if use else None,
+                "sm_max_mhz": max(x[1] for x in self.samples) if self.samples else None,
+                "reasons": reasons, "samples": len(self.samples),
+                "samples_under_load": len(loaded), "source": "nvml, timed region"}
+
+
 class ClockSampler:
-    """nvidia-smi clock/throttle samples while the timed region runs."""
+    """Clock/throttle samples while the timed region runs: NVML polled about
+    every millisecond (samples inside the timed region count as under load),
+    else nvidia-smi at 100 ms (under load = power well above idle)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -157,6 +236,7 @@ class ClockSampler:
 
     def __init__(self, device):
         self.proc = None
+        self.nvml = None
         self.lines = []
         self.bus = None
         try:
@@ -165,7 +245,22 @@ class ClockSampler:
         except Exception:
             self.bus = None
 
+    def region(self, running):
+        """Mark the timed region (NVML samples taken inside it are under load)."""
+        if self.nvml is not None:
+            self.nvml.in_region = running
+
     def start(self):
+        self.nvml = None
+        if self.bus:
+            try:
+                nv = NvmlPoller(self.bus)
+                if nv.ok:
+                    nv.start()
+                    self.nvml = nv
+                    return
+            except Exception:
+                self.nvml = None
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                "-lms", "100"]
         if self.bus:
@@ -184,6 +279,12 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self):
+        if self.nvml is not None:
+            try:
+                return self.nvml.stop()
+            except Exception:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml sampling failed"],
+                        "samples": 0, "samples_under_load": 0}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
                     "samples": 0, "samples_under_load": 0}
@@ -215,7 +316,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm),
-                "samples_under_load": len(loaded)}
+                "samples_under_load": len(loaded), "source": "nvidia-smi"}
 
 
 # --------------------------------------------------------------------------- dist
@@ -405,6 +506,8 @@ def measure(w, wr, dist, dev, args, peaks, peak_src, clocks_on):
     t_end = torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.region(True)
     t_start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -412,6 +515,8 @@ def measure(w, wr, dist, dev, args, peaks, peak_src, clocks_on):
         ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.region(False)
     dist.barrier()
     clock_rec = clocks.stop() if clocks else None
     elapsed = dist.max(t_start.elapsed_time(t_end) / 1e3, dev)

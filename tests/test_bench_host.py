@@ -63,3 +63,80 @@ def test_traffic_record_needs_the_current_code(monkeypatch):
     assert recorded > bench.algorithmic_bytes(synth.WORKLOADS[3]) // 2
     monkeypatch.setattr(bench, "source_sha", lambda kind: "0" * 16)
     assert bench.read_traffic("fwd", name) is None
+
+
+class FakeNvml:
+    """Stands in for the driver's NVML library: answers the read-only queries
+    the bench makes, writing through the ctypes references it is given."""
+
+    def __init__(self, mhz=1965, max_mhz=2070, mw=950000, reasons=0x4, init_status=0,
+                 new_reason_call=True):
+        self.mhz, self.max_mhz, self.mw, self.reasons = mhz, max_mhz, mw, reasons
+        self.init_status = init_status
+        self.calls = []
+        if new_reason_call:
+            self.nvmlDeviceGetCurrentClocksEventReasons = self._reasons
+        else:
+            self.nvmlDeviceGetCurrentClocksThrottleReasons = self._reasons
+
+    def nvmlInit_v2(self):
+        return self.init_status
+
+    def nvmlShutdown(self):
+        self.calls.append("shutdown")
+        return 0
+
+    def nvmlDeviceGetHandleByPciBusId_v2(self, bus, ref):
+        self.calls.append(bus)
+        ref._obj.value = 1234
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, h, kind, ref):
+        assert kind == 1  # the SM clock
+        ref._obj.value = self.mhz
+        return 0
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind, ref):
+        ref._obj.value = self.max_mhz
+        return 0
+
+    def nvmlDeviceGetPowerUsage(self, h, ref):
+        ref._obj.value = self.mw
+        return 0
+
+    def _reasons(self, h, ref):
+        ref._obj.value = self.reasons
+        return 0
+
+
+def _poll(lib, before=0.01, inside=0.03):
+    import time
+    p = bench.NvmlPoller("00000000:01:00.0", lib=lib)
+    assert p.ok
+    p.start()
+    time.sleep(before)
+    p.in_region = True
+    time.sleep(inside)
+    p.in_region = False
+    return p.stop()
+
+
+def test_nvml_poller_counts_samples_inside_the_timed_region():
+    lib = FakeNvml()
+    rec = _poll(lib)
+    assert rec["samples_under_load"] > 0 and rec["samples"] >= rec["samples_under_load"]
+    assert rec["sm_mhz"] == 1965 and rec["sm_max_mhz"] == 2070
+    assert rec["reasons"] == ["sw_power_cap"]
+    assert rec["source"].startswith("nvml")
+    assert lib.calls[0] == b"00000000:01:00.0" and lib.calls[-1] == "shutdown"
+
+
+def test_nvml_poller_names_every_throttle_reason_and_takes_the_older_call():
+    rec = _poll(FakeNvml(reasons=0x4 | 0x8 | 0x20 | 0x40 | 0x1, new_reason_call=False))
+    assert rec["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap",
+                              "sw_thermal_slowdown"]
+
+
+def test_nvml_poller_reports_failure_instead_of_raising():
+    assert not bench.NvmlPoller("00000000:01:00.0", lib=FakeNvml(init_status=1)).ok
+    assert not bench.NvmlPoller("00000000:01:00.0", lib=object()).ok
