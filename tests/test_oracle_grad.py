@@ -155,3 +155,32 @@ def test_chunked_pins_catch_planted_mistakes(monkeypatch, mutant):
     monkeypatch.setattr(forms, "ut_chunk_grad", mutant)
     with pytest.raises(AssertionError):
         test_chunked_backward_matches_finite_differences(7, 4, True)
+
+
+@pytest.mark.parametrize("n_h,C", [(2, 4), (3, 8)])
+def test_chunked_backward_on_the_extended_sequence(n_h, C):
+    # DeltaProduct ([DP] §4.1): the chunked backward on the extended sequence
+    # (gate on each token's first sub-step, readout on its last) gives the
+    # gradients of the token recurrence: dq from the readout rows, d log g
+    # from the first sub-steps, k, v and beta per sub-step
+    rng = np.random.default_rng(90 + n_h)
+    T, dk, dv = 7, 4, 3
+    q = rng.standard_normal((T, dk))
+    k = unit(rng.standard_normal((T, n_h, dk)))
+    v = rng.standard_normal((T, n_h, dv))
+    beta = rng.uniform(0.1, 1.8, (T, n_h))
+    g = rng.uniform(0.4, 1.0, T)
+    S0 = rng.standard_normal((dk, dv)) * 0.5
+    dout = rng.standard_normal((T, dv))
+    dST = rng.standard_normal((dk, dv))
+    ref = forms.recurrent_grad(q, k, v, beta, g, S0, dout, dST, n_h=n_h)
+    qx, kx, vx, bx, gx, idx = forms.extend_sequence(q, k, v, beta, g, n_h)
+    dox = np.zeros((T * n_h, dv))
+    dox[idx] = dout
+    got = forms.ut_chunk_grad(qx, kx, vx, bx, np.log(gx), S0, dox, dST, C=C)
+    np.testing.assert_allclose(got[0][idx], ref[0], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got[1].reshape(T, n_h, dk), ref[1], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got[2].reshape(T, n_h, dv), ref[2], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got[3].reshape(T, n_h), ref[3], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got[4][0::n_h], ref[4] * g, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got[5], ref[5], rtol=1e-10, atol=1e-12)
