@@ -392,3 +392,13 @@ def test_bwd_rejects_before_launch(lib, kw, status):
 
 def test_bwd_empty_batch_is_ok_without_gpu(lib):
     assert bwd(lib, B=0) == wr.DELTA_OK
+
+
+def test_bwd_rejects_a_grid_too_large_for_its_column_groups(lib):
+    # B*H = 2^30 passes the per-head limit, but four groups of 32 value
+    # columns (dv = 128) would need 2^32 CTAs; the pointers are spaced far
+    # enough apart that no range overlaps, and nothing is dereferenced
+    span = 1 << 44
+    kw = {n: span * (i + 1) for i, n in enumerate(("q", "k", "v", "beta", "dout", "gq", "gk",
+                                                    "gv", "gb"))}
+    assert bwd(lib, B=1 << 15, H=1 << 15, T=1, dk=16, dv=128, **kw) == wr.DELTA_ERR_UNSUPPORTED
