@@ -1,7 +1,10 @@
 /*
  * delta.h -- C ABI of libdelta: the forward pass of delta-rule linear
  * attention (DeltaNet, Gated DeltaNet, Gated DeltaProduct) and its
- * single-token decode step, for one NVIDIA GB300 (sm_103a).
+ * single-token decode step, for one NVIDIA GB300 (sm_103a); around them the
+ * input prologue (delta_prologue and the *_prologue calls), the channel-wise
+ * gate (delta_fwd_kda, delta_step_kda), the gradients (delta_bwd) and two
+ * diagnostics on the outputs (delta_state_erank, delta_attention_map).
  *
  * The operation.  For every batch row b and head h, independently, a state
  * S in R^{dk x dv} runs through the recurrence
@@ -46,8 +49,8 @@
  * (delta_ut_transform) over every chunk at once, then the state pass
  * (delta_fwd_with_ut), one CTA per (b, h).  Every other shape in the
  * supported set -- all DELTA_F32 I/O, head dims below 128, chunk 16 or 32 --
- * runs a float32 CUDA-core kernel meant for correctness checks, several
- * hundred times slower (about 0.1 % of the HBM roofline at B8 H16 T4096).
+ * runs a float32 CUDA-core kernel meant for correctness checks, about two
+ * hundred times slower (39.5 ms against 0.18 ms at B8 H16 T4096, d = 128).
  * delta_step has one kernel for every supported shape (HBM-bound at
  * dk = dv = 128).
  */
