@@ -402,3 +402,33 @@ def test_bwd_rejects_a_grid_too_large_for_its_column_groups(lib):
     kw = {n: span * (i + 1) for i, n in enumerate(("q", "k", "v", "beta", "dout", "gq", "gk",
                                                     "gv", "gb"))}
     assert bwd(lib, B=1 << 15, H=1 << 15, T=1, dk=16, dv=128, **kw) == wr.DELTA_ERR_UNSUPPORTED
+
+
+def test_every_compute_binding_refuses_cpu_tensors(lib):
+    # no CPU fallback anywhere: each compute call raises on host tensors
+    # before reaching the library
+    import torch
+    B, T, H, d = 1, 4, 1, 16
+    q, k, v = torch.zeros(B, T, H, d), torch.zeros(B, T, H, d), torch.zeros(B, T, H, d)
+    beta, g = torch.zeros(B, T, H), torch.ones(B, T, H)
+    state = torch.zeros(B, H, d, d)
+    alpha_t, alpha_1 = torch.ones(B, T, H, d), torch.ones(B, H, d)
+    q1, k1, b1, g1 = q[:, 0], k[:, :1], beta[:, :1], g[:, 0]
+    calls = [
+        lambda: wr.delta_fwd(q, k, v, beta, g),
+        lambda: wr.delta_bwd(q, k, v, beta, g, state, v, state),
+        lambda: wr.delta_fwd_kda(q, k, v, beta, alpha_t),
+        lambda: wr.delta_step_kda(q1, k1, k1, b1, alpha_1, state),
+        lambda: wr.delta_prologue(q, k, beta),
+        lambda: wr.delta_fwd_prologue(q, k, v, beta, g),
+        lambda: wr.delta_fwd_static_scratch(q, k, v, beta, g),
+        lambda: wr.delta_state_erank(state),
+        lambda: wr.delta_attention_map(q, k, beta, g),
+        lambda: wr.delta_ut_transform(k, beta, g),
+        lambda: wr.delta_fwd_with_ut(q, k, v, beta, g, None, torch.zeros(1, 64, 64)),
+        lambda: wr.delta_step(q1, k1, k1, b1, g1, state),
+        lambda: wr.delta_step_prologue(q1, k1, k1, b1, g1, state),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="needs CUDA tensors"):
+            call()
