@@ -369,6 +369,64 @@ def kda_recurrent(q, k, v, beta, alpha, S0=None, n_h=1):
     return o, S
 
 
+
+def kda_chunk(q, k, v, beta, alpha, S0=None, n_h=1, C=16):
+    """The chunkwise form of the channel-wise gate: the gated chunkwise
+    algorithm of [DR] §2.3 and §3 (which that page states for the whole delta
+    family, KDA included) with the scalar cumulative log gate replaced by one
+    per key channel, gc [C, dk], so that every decay ratio moves inside the
+    sum over the key dimension:
+        A_rj = beta_r sum_d k_rd k_jd exp(gc_rd - gc_jd)      (r > j)
+        P_rj = sum_d q_rd k_jd exp(gc_rd - gc_jd)             (j <= r)
+        T    = (I + A)^{-1} diag(beta),  W = T (K * exp(gc)),  U = T V
+        Vt   = U - W S,  O = (Q * exp(gc)) S + P Vt
+        S   <- Diag(exp(gc_C)) S + (K * exp(gc_C - gc))^T Vt
+    run on the [DP] §4.1 extended sequence (alpha on each token's first
+    sub-step, readout on its last).  The ratio is formed only for j <= r (mask
+    before the exponential), so no exponent is positive.  Shapes as
+    kda_recurrent; returns o [T, dv] and the final state (float64)."""
+    q = np.asarray(q, float)
+    T, dk = q.shape
+    k = np.asarray(k, float).reshape(T, n_h, dk)
+    v = np.asarray(v, float)
+    v = v.reshape(T, n_h, v.shape[-1])
+    dv = v.shape[-1]
+    L = T * n_h
+    K, V = k.reshape(L, dk), v.reshape(L, dv)
+    bt = np.asarray(beta, float).reshape(L)
+    lg = np.zeros((L, dk))
+    with np.errstate(divide="ignore"):
+        # log alpha clamped at -80, so that alpha = 0 (a reset of that row)
+        # stays finite: exp(-80) is below float64 resolution next to 1
+        lg[0::n_h] = np.maximum(np.log(np.asarray(alpha, float)), -80.0)
+    Q = np.zeros((L, dk))
+    Q[n_h - 1::n_h] = q
+    NT = -(-L // C)
+    pad = NT * C - L
+    if pad:
+        K, V, Q, lg = (np.concatenate([x, np.zeros((pad,) + x.shape[1:])]) for x in (K, V, Q, lg))
+        bt = np.concatenate([bt, np.zeros(pad)])
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((NT * C, dv))
+    strict = np.tril(np.ones((C, C), dtype=bool), -1)
+    incl = np.tril(np.ones((C, C), dtype=bool))
+    for n in range(NT):
+        sl = slice(n * C, (n + 1) * C)
+        Kc, Vc, Qc, bc = K[sl], V[sl], Q[sl], bt[sl]
+        gc = np.cumsum(lg[sl], axis=0)                       # [C, dk]
+        # ratio[r, j, d] = exp(gc_rd - gc_jd), formed only where j <= r
+        diff = np.where(incl[:, :, None], gc[:, None, :] - gc[None, :, :], -np.inf)
+        ratio = np.exp(diff)
+        A = np.where(strict, bc[:, None] * np.einsum("rd,jd,rjd->rj", Kc, Kc, ratio), 0.0)
+        P = np.einsum("rd,jd,rjd->rj", Qc, Kc, ratio)
+        Tm = solve_triangular(np.eye(C) + A, np.diag(bc), lower=True, unit_diagonal=True)
+        W = Tm @ (Kc * np.exp(gc))
+        Vt = Tm @ Vc - W @ S
+        o[sl] = (Qc * np.exp(gc)) @ S + P @ Vt
+        S = np.exp(gc[-1])[:, None] * S + (Kc * np.exp(gc[-1][None, :] - gc)).T @ Vt
+    return o[n_h - 1:L:n_h], S
+
+
 # --------------------------------------------------------------------------
 # gradients of the recurrence (no page gives them: float64 autograd)
 # --------------------------------------------------------------------------

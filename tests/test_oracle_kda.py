@@ -102,3 +102,51 @@ def test_pins_catch_planted_mistakes(monkeypatch, mutant):
     monkeypatch.setattr(forms, "kda_recurrent", mutant)
     with pytest.raises(AssertionError):
         test_kda_is_the_dplr_reduction_of_the_delta_rule_page()
+
+
+@pytest.mark.parametrize("n_h,C,T", [(1, 4, 12), (2, 8, 13), (3, 16, 9), (1, 64, 20)])
+def test_chunked_kda_equals_the_recurrence(n_h, C, T):
+    # the chunkwise form with the per-channel ratio inside the key sums (the
+    # reading the CUDA-core kernel implements) is exact: several chunks, ragged
+    # tails, DeltaProduct sub-steps
+    rng = np.random.default_rng(30 + n_h + C)
+    q, k, v, beta, alpha, S0 = inputs(rng, T=T, n_h=n_h)
+    o1, S1 = forms.kda_recurrent(q, k, v, beta, alpha, S0, n_h=n_h)
+    o2, S2 = forms.kda_chunk(q, k, v, beta, alpha, S0, n_h=n_h, C=C)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S2, S1, rtol=1e-12, atol=1e-12)
+
+
+def test_chunked_kda_with_a_reset_inside_a_chunk():
+    # alpha = 0 on some channels mid-chunk: the chunked form clamps log alpha
+    # at -80 and still matches the exact recurrence
+    rng = np.random.default_rng(35)
+    q, k, v, beta, alpha, S0 = inputs(rng, T=10)
+    alpha[3, :2] = 0.0
+    alpha[6, 4] = 0.0
+    o1, S1 = forms.kda_recurrent(q, k, v, beta, alpha, S0)
+    o2, S2 = forms.kda_chunk(q, k, v, beta, alpha, S0, C=8)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S2, S1, rtol=1e-12, atol=1e-12)
+
+
+def _channel_mean_gate(q, k, v, beta, alpha, S0=None, n_h=1, C=16):
+    # a plausible slip: one gate per token (the channel mean) instead of one
+    # per key channel
+    a = np.repeat(np.asarray(alpha).mean(axis=1, keepdims=True), np.shape(alpha)[1], axis=1)
+    return forms._kda_chunk_ok(q, k, v, beta, a, S0, n_h=n_h, C=C)
+
+
+def _gate_on_last_substep(q, k, v, beta, alpha, S0=None, n_h=1, C=16):
+    # another: the gate applied after a token's sub-steps (shift the tokens'
+    # gates one token later, so the decay lands after the previous updates)
+    a = np.concatenate([np.ones((1, np.shape(alpha)[1])), np.asarray(alpha)[:-1]])
+    return forms._kda_chunk_ok(q, k, v, beta, a, S0, n_h=n_h, C=C)
+
+
+@pytest.mark.parametrize("mutant", [_channel_mean_gate, _gate_on_last_substep])
+def test_chunked_kda_pins_catch_planted_mistakes(monkeypatch, mutant):
+    monkeypatch.setattr(forms, "_kda_chunk_ok", forms.kda_chunk, raising=False)
+    monkeypatch.setattr(forms, "kda_chunk", mutant)
+    with pytest.raises(AssertionError):
+        test_chunked_kda_equals_the_recurrence(2, 8, 13)
