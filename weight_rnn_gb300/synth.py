@@ -13,6 +13,12 @@ describe: keys and queries are SiLU'd and L2-normalised per token and head
 "DeltaProduct …" reading notes §2.2), beta = sigmoid (or 2*sigmoid to allow
 negative eigenvalues, "DeltaProduct …" §2.2), and the gate is a Mamba-2 style
 exp(-softplus(x) * 0.1) per token and head.
+
+The SiLU and normalisation here only give the forward's inputs the shape of
+that layer's outputs (the forward takes normalised keys).  The input
+prologue, which computes the same maps as part of the method, is implemented
+separately by its kernel and by the oracle, and both are tested on raw draws
+that do not pass through this module.
 """
 from __future__ import annotations
 
